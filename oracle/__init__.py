@@ -1,0 +1,202 @@
+"""CPU oracle for the W8A8 block-FP8 matmul -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline
+leg (and its ``--impl reference`` arm) may import this package.  The product
+path (``block_scaled_fp8_w8a8_gb300``) never imports it; the two share no code
+besides the seeded input generator ``block_scaled_fp8_w8a8_gb300.synth``, which
+holds none of the matmul's arithmetic.
+
+The operator ("feat: optimize w8a8 block fp8 matmul for Hopper", FlagGems-vllm
+PR #693, Description: per-token/per-block FP8 E4M3 inputs with
+[block_n, block_k] de-quant scales; Numerical safety: FP32 accumulation, cast
+to bf16 / fp16 / fp32):
+
+    C[m,n] = cast_out( sum_g a_s[m,g] * b_s[n // block_n, g] * sum_{k in g} A[m,k] * B[n,k] )
+
+Two independent implementations live here and are checked against each other
+and against closed forms in ``tests/test_oracle.py``:
+
+* ``reference_numpy``: the definition with numpy, one float64 matmul per K
+  group (each group sum is exact, see ``w8a8_oracle.c``), scales applied and
+  groups summed in ascending order.
+* ``reference_c`` / ``reference_c_sampled``: plain C loops (``w8a8_oracle.c``),
+  multithreaded over rows, for full-size shapes and sampled elements.
+
+Both return double; ``cast_out`` rounds once to the output dtype (round to
+nearest, ties to even), with the rounding written out in ``round_to_format``.
+
+Every function here is pinned by a ``-m "not gpu"`` test; nothing is
+"parity unpinned".
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import subprocess
+import sys
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "w8a8_oracle.c")
+_LIB = os.path.join(_HERE, "_build", "libw8a8_oracle.so")
+_lib = None
+
+
+def e4m3fn_value(code: int) -> float:
+    """Decode one OCP E4M3FN byte: sign, 4-bit exponent (bias 7), 3-bit mantissa;
+    exponent 0 is subnormal (f * 2^-9); S.1111.111 is NaN; no infinities."""
+    s, e, f = (code >> 7) & 1, (code >> 3) & 0xF, code & 0x7
+    if e == 0xF and f == 0x7:
+        return math.nan
+    mag = f * 2.0 ** -9 if e == 0 else (1.0 + f / 8.0) * 2.0 ** (e - 7)
+    return -mag if s else mag
+
+
+def e4m3fn_table() -> np.ndarray:
+    """All 256 E4M3FN codes decoded exactly to float64."""
+    return np.array([e4m3fn_value(c) for c in range(256)], dtype=np.float64)
+
+
+_TABLE = e4m3fn_table()
+
+
+def _np(x):
+    if hasattr(x, "detach"):
+        x = x.detach().cpu().numpy()
+    return np.ascontiguousarray(x)
+
+
+def reference_numpy(A, a_s, B, b_s, block_n: int = 128, block_k: int = 128) -> np.ndarray:
+    """The definition in float64, one exact matmul per K group, groups in order."""
+    A, B = _np(A).astype(np.uint8), _np(B).astype(np.uint8)
+    a_s, b_s = _np(a_s).astype(np.float32), _np(b_s).astype(np.float32)
+    M, K = A.shape
+    N, Kb = B.shape
+    assert K == Kb
+    G = -(-K // block_k)
+    assert a_s.shape == (M, G) and b_s.shape == (-(-N // block_n), G)
+    Ad, Bd = _TABLE[A], _TABLE[B]
+    nb = np.arange(N) // block_n
+    C = np.zeros((M, N), dtype=np.float64)
+    for g in range(G):
+        k0, k1 = g * block_k, min((g + 1) * block_k, K)
+        p = Ad[:, k0:k1] @ Bd[:, k0:k1].T                      # exact group sums
+        s = a_s[:, g].astype(np.float64)[:, None] * b_s[nb, g].astype(np.float64)[None, :]
+        C = C + s * p
+    return C
+
+
+def build(force: bool = False) -> str:
+    """Compile the C oracle into oracle/_build/ (gcc, no fast-math, no FMA contraction)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        os.makedirs(os.path.dirname(_LIB), exist_ok=True)
+        tmp = _LIB + f".tmp{os.getpid()}"
+        cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC",
+               "-shared", "-pthread", _SRC, "-o", tmp, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        lib = ctypes.CDLL(build())
+        i64, p = ctypes.c_int64, ctypes.c_void_p
+        lib.oracle_w8a8_block_fp8.argtypes = [p, p, p, p, p, i64, i64, i64, i64, i64, ctypes.c_int]
+        lib.oracle_w8a8_block_fp8.restype = ctypes.c_int
+        lib.oracle_w8a8_block_fp8_sampled.argtypes = [p, p, p, p, p, i64, i64, i64, i64, i64,
+                                                      p, i64, ctypes.c_int]
+        lib.oracle_w8a8_block_fp8_sampled.restype = ctypes.c_int
+        lib.oracle_e4m3fn_table.argtypes = [p]
+        lib.oracle_e4m3fn_table.restype = None
+        _lib = lib
+    return _lib
+
+
+def default_threads() -> int:
+    return max(1, len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count() or 1)
+
+
+def c_table() -> np.ndarray:
+    out = np.zeros(256, dtype=np.float64)
+    _load().oracle_e4m3fn_table(out.ctypes.data)
+    return out
+
+
+def _prep(A, a_s, B, b_s, block_n, block_k):
+    A, B = _np(A).astype(np.uint8), _np(B).astype(np.uint8)
+    a_s, b_s = _np(a_s).astype(np.float32), _np(b_s).astype(np.float32)
+    M, K = A.shape
+    N = B.shape[0]
+    G = -(-K // block_k) if K else 0
+    assert B.shape[1] == K and a_s.shape == (M, G) and b_s.shape == (-(-N // block_n), G)
+    return A, a_s, B, b_s, M, N, K
+
+
+def reference_c(A, a_s, B, b_s, block_n: int = 128, block_k: int = 128,
+                threads: int | None = None) -> np.ndarray:
+    """Full [M, N] float64 product with the C oracle."""
+    A, a_s, B, b_s, M, N, K = _prep(A, a_s, B, b_s, block_n, block_k)
+    C = np.zeros((M, N), dtype=np.float64)
+    rc = _load().oracle_w8a8_block_fp8(A.ctypes.data, a_s.ctypes.data, B.ctypes.data,
+                                       b_s.ctypes.data, C.ctypes.data, M, N, K, block_n,
+                                       block_k, threads or default_threads())
+    if rc != 0:
+        raise ValueError("oracle rejected its arguments")
+    return C
+
+
+def reference_c_sampled(A, a_s, B, b_s, rows, cols, block_n: int = 128, block_k: int = 128,
+                        threads: int | None = None) -> np.ndarray:
+    """C[rows[i], cols[i]] in float64 for each i, with the C oracle."""
+    A, a_s, B, b_s, M, N, K = _prep(A, a_s, B, b_s, block_n, block_k)
+    pairs = np.ascontiguousarray(np.stack([np.asarray(rows, dtype=np.int64),
+                                           np.asarray(cols, dtype=np.int64)], axis=1))
+    out = np.zeros(pairs.shape[0], dtype=np.float64)
+    rc = _load().oracle_w8a8_block_fp8_sampled(A.ctypes.data, a_s.ctypes.data, B.ctypes.data,
+                                               b_s.ctypes.data, out.ctypes.data, M, N, K,
+                                               block_n, block_k, pairs.ctypes.data,
+                                               pairs.shape[0], threads or default_threads())
+    if rc != 0:
+        raise ValueError("oracle rejected its arguments")
+    return out
+
+
+# (significand bits incl. the hidden one, exponent of the smallest subnormal,
+#  largest finite value) of each output format, IEEE 754 binary16 / binary32
+#  and bfloat16 (binary32 with a 7-bit fraction).
+_FORMATS = {
+    "bf16": (8, -133, (2.0 - 2.0 ** -7) * 2.0 ** 127),
+    "fp16": (11, -24, 65504.0),
+    "fp32": (24, -149, (2.0 - 2.0 ** -23) * 2.0 ** 127),
+}
+
+
+def round_to_format(C: np.ndarray, dtype: str) -> np.ndarray:
+    """Round float64 values once, to nearest with ties to even, onto the grid of
+    ``dtype`` ('bf16', 'fp16' or 'fp32'); overflow goes to +-inf, NaN stays NaN.
+    The result is float64 holding values exactly representable in ``dtype``."""
+    p, emin_sub, vmax = _FORMATS[dtype]
+    x = np.asarray(C, dtype=np.float64)
+    _, e = np.frexp(x)                       # |x| = m * 2^e with 0.5 <= m < 1
+    q = np.maximum(e - p, emin_sub)          # exponent of one unit in the last place
+    with np.errstate(invalid="ignore", over="ignore"):
+        r = np.ldexp(np.rint(np.ldexp(x, -q)), q)   # np.rint: ties to even
+        r = np.where(np.abs(r) > vmax, np.copysign(np.inf, x), r)
+    return r
+
+
+def cast_out(C: np.ndarray, dtype: str):
+    """``cast_out`` of the definition: round-to-nearest-even into the output
+    dtype; returns a torch CPU tensor of that dtype (the conversion from the
+    already-rounded float64 values is exact)."""
+    import torch
+    r = torch.from_numpy(np.ascontiguousarray(round_to_format(C, dtype)))
+    return r.to({"bf16": torch.bfloat16, "fp16": torch.float16, "fp32": torch.float32}[dtype])
+
+
+if __name__ == "__main__":  # pragma: no cover - manual build helper
+    print(build(force="--force" in sys.argv))
