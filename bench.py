@@ -1,0 +1,511 @@
+"""Benchmark of the W8A8 block-FP8 matmul on GB300 (one JSON line on stdout).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+A step is one pass over every shape of the workload (default: the short-K
+decode sweep N=4096, K=256, M in {1, 16, 100, 184, 214}) on one seeded
+synthetic input set.  Inputs are block-quantised N(0,1) data made by
+block_scaled_fp8_w8a8_gb300.synth; the shapes stand in for the
+DeepSeek-V4-Flash trace grid of "feat: optimize w8a8 block fp8 matmul for
+Hopper" (FlagGems-vllm PR #693, Performance).
+
+Timing: every step reads a different input set out of a rotation whose total
+size exceeds twice the L2 cache, so each step streams its operands from HBM.
+Each step is one CUDA-graph replay of the workload's kernel launches; K steps
+are bracketed by a barrier and torch.cuda.synchronize() and timed with CUDA
+events; the K-step block is repeated until about a second has been timed and
+the median block is reported.  nvidia-smi samples the clocks meanwhile.
+
+Under torchrun (N > 1) every rank runs the same workload on its own GPU as an
+independent replica (the operator has no exchange step); the reported time is
+the maximum over ranks and the value counts the work of all ranks.
+
+--impl reference times the CPU oracle (oracle/, plain C, double) on this
+machine's host cores, on the same workload and metric.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from block_scaled_fp8_w8a8_gb300 import synth  # noqa: E402
+
+METRIC = "TFLOP/s and GB/s per (M,N,K) shape; % of FP8 tensor / HBM roofline"
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="decode_n4096_k256", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--out-dtype", default="bf16", choices=["bf16", "fp16", "fp32"])
+    ap.add_argument("--min-seconds", type=float, default=1.0,
+                    help="repeat the K-step block until this much time has been timed")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    return ap.parse_args()
+
+
+def peaks():
+    try:
+        with open(PEAKS_FILE) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
+
+
+def workload_units(shapes, out_bytes):
+    flops = sum(synth.algorithmic_flops(*s) for s in shapes)
+    nbytes = sum(synth.algorithmic_bytes(*s, out_bytes=out_bytes) for s in shapes)
+    return flops, nbytes
+
+
+def bound_of(shapes):
+    """'tensor' when the workload's arithmetic intensity is above the ridge
+    (about 550 FLOP/B for dense FP8 against HBM), else 'hbm'."""
+    flops, nbytes = workload_units(shapes, 2)
+    return "tensor" if flops / nbytes > 550 else "hbm"
+
+
+# ---------------------------------------------------------------------- distributed
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return rank, world
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons during a region."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.path or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax = float(parts[2])
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        loaded = [s for s in sm if smax and s > 0.5 * smax] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------- our implementation
+
+class Workload:
+    """Device-resident rotating input sets and one CUDA graph per set."""
+
+    def __init__(self, name, out_dtype, l2_bytes):
+        import block_scaled_fp8_w8a8_gb300 as w8
+        self.w8 = w8
+        spec = synth.WORKLOADS[name]
+        self.shapes = spec["shapes"]
+        self.out_code = w8.out_code(out_dtype)
+        self.out_bytes = 4 if out_dtype == "fp32" else 2
+        tdt = {"bf16": torch.bfloat16, "fp16": torch.float16, "fp32": torch.float32}[out_dtype]
+        host = [synth.make_inputs(M, N, K, seed=0, outlier_p=spec["outlier_p"])
+                for (M, N, K) in self.shapes]
+        self.host = host
+        _, per_set = workload_units(self.shapes, self.out_bytes)
+        self.sets = max(2, int(-(-2 * l2_bytes // per_set)) + 1)
+        self.data = []
+        for r in range(self.sets):
+            items = []
+            for x, (M, N, K) in zip(host, self.shapes):
+                dev = [t.to("cuda") for t in (x.A, x.a_s, x.B, x.b_s)]
+                C = torch.empty((M, N), dtype=tdt, device="cuda")
+                items.append((dev, C))
+            self.data.append(items)
+        # plans and split-K workspaces (one per set and shape, so graphs are independent)
+        self.plans = [w8.w8a8_block_fp8_plan(M, N, K, self.out_code)[1] for (M, N, K) in self.shapes]
+        self.ws = []
+        for r in range(self.sets):
+            row = []
+            for (M, N, K), plan in zip(self.shapes, self.plans):
+                nb = plan.workspace_bytes
+                row.append(torch.zeros(max(nb, 256), dtype=torch.uint8, device="cuda") if nb else None)
+            self.ws.append(row)
+        self.graphs = []
+
+    def launch(self, r, i, stream):
+        (A, a_s, B, b_s), C = self.data[r][i]
+        M, N, K = self.shapes[i]
+        o = self.w8.options(pdl=1)
+        ws = self.ws[r][i]
+        if ws is not None:
+            o.workspace_dev = ws.data_ptr()
+            o.workspace_bytes = ws.numel()
+        st = self.w8.w8a8_block_fp8_matmul_ex(A, a_s, B, b_s, C, M, N, K, 128, 128,
+                                              self.out_code, stream, o)
+        self.w8.check(st)
+
+    def step_eager(self, r, stream):
+        for i in range(len(self.shapes)):
+            self.launch(r, i, stream)
+
+    def capture(self):
+        stream = torch.cuda.Stream()
+        torch.cuda.synchronize()
+        for r in range(self.sets):          # warm every set once outside capture
+            self.step_eager(r, stream)
+        stream.synchronize()
+        for r in range(self.sets):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                self.step_eager(r, torch.cuda.current_stream())
+            self.graphs.append(g)
+        torch.cuda.synchronize()
+
+    def capture_single(self, i, count):
+        """A graph of `count` launches of shape i, rotating over the sets."""
+        stream = torch.cuda.Stream()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for j in range(count):
+                self.launch(j % self.sets, i, torch.cuda.current_stream())
+        torch.cuda.synchronize()
+        return g
+
+
+def time_blocks(fn, steps, world, min_seconds):
+    """Median time of K-step blocks (each bracketed by barrier + synchronize)."""
+    times = []
+    total = 0.0
+    while True:
+        barrier(world)
+        torch.cuda.synchronize()
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record()
+        for k in range(steps):
+            fn(k)
+        end.record()
+        torch.cuda.synchronize()
+        barrier(world)
+        t = max_over_ranks(start.elapsed_time(end) / 1e3, world)
+        times.append(t)
+        total += t
+        if total >= min_seconds or len(times) >= 200:
+            break
+    return statistics.median(times), len(times)
+
+
+def run_ours(args, rank, world):
+    import block_scaled_fp8_w8a8_gb300 as w8
+    hbm, bf16, peak_kind = peaks()
+    dev = torch.cuda.current_device()
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    wl = Workload(args.workload, args.out_dtype, l2)
+    wl.capture()
+    shapes = wl.shapes
+    flops, nbytes = workload_units(shapes, wl.out_bytes)
+    bound = bound_of(shapes)
+
+    for k in range(args.warmup):
+        wl.graphs[k % wl.sets].replay()
+    torch.cuda.synchronize()
+
+    with ClockSampler(dev) as clk:
+        t_step_blocks, nblocks = time_blocks(lambda k: wl.graphs[k % wl.sets].replay(),
+                                             args.steps, world, args.min_seconds)
+    clocks = clk.summary()
+    t_step = t_step_blocks / args.steps
+
+    # Per-shape launch durations: a graph of L launches of one shape (rotating sets).
+    per_shape = []
+    L = max(wl.sets, 64)
+    for i, (M, N, K) in enumerate(shapes):
+        g = wl.capture_single(i, L)
+        for _ in range(2):
+            g.replay()
+        torch.cuda.synchronize()
+        t_blk, _ = time_blocks(lambda k: g.replay(), 5, 1, 0.2)
+        t = t_blk / (5 * L)
+        fl = synth.algorithmic_flops(M, N, K)
+        by = synth.algorithmic_bytes(M, N, K, out_bytes=wl.out_bytes)
+        plan = wl.plans[i]
+        per_shape.append({"M": M, "N": N, "K": K, "us": round(t * 1e6, 3),
+                          "tflops": round(fl / t / 1e12, 3), "gbs": round(by / t / 1e9, 1),
+                          "variant": {1: "tiled", 2: "swapab", 3: "splitk"}.get(plan.variant, "?"),
+                          "split_k": plan.split_k, "m_tile": plan.m_tile,
+                          "block_n_tile": plan.block_n_tile})
+    dom = max(range(len(shapes)), key=lambda i: per_shape[i]["us"])
+    d = per_shape[dom]
+    if bound == "hbm":
+        achieved = d["gbs"]
+        peak = hbm
+        unit = "GB/s"
+    else:
+        achieved = d["tflops"]
+        peak = 2.0 * bf16          # dense FP8 = 2 x the measured bf16 rate (nominal ratio)
+        unit = "TFLOP/s"
+    roofline = {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
+                "frac": round(achieved / peak, 4), "traffic": None,
+                "kernel": f"M={d['M']} N={d['N']} K={d['K']} ({d['variant']})",
+                "peak_source": f"{peak_kind}" + (" (bf16 x 2, nominal fp8/bf16 ratio)" if bound == "tensor" else "")}
+
+    # End to end through the host-buffer entry point (pinned host memory).
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(wl, args, world)
+
+    result = {
+        "metric": METRIC,
+        "value": None, "unit": None,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(t_step * 1e3, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "fp8e4m3*fp8e4m3->f32 (out " + args.out_dtype + ")",
+        "data": "synthetic (seeded N(0,1), block-quantised to E4M3 with amax/448 scales)",
+        "config": {"workload": args.workload, "shapes": [list(s) for s in shapes],
+                   "l2": f"rotating {wl.sets} input sets of {nbytes / 1e6:.2f} MB (> 2x L2 "
+                         f"{l2 / 1e6:.0f} MB); CUDA-graph replay per step",
+                   "timed_blocks": nblocks, "parallelism": f"replicas x{world}"},
+        "gpu_launches": args.steps * len(shapes),
+        "tflops": round(flops * world / t_step / 1e12, 4),
+        "gbs": round(nbytes * world / t_step / 1e9, 2),
+        "per_shape": per_shape,
+        "roofline": roofline,
+        "clocks": clocks,
+    }
+    if bound == "hbm":
+        result["value"], result["unit"] = result["gbs"], "GB/s"
+    else:
+        result["value"], result["unit"] = result["tflops"], "TFLOP/s"
+    if e2e is not None:
+        result["e2e"] = e2e
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(shapes, wl.host, args.out_dtype, bound,
+                                              args.cpu_seconds)
+    return result
+
+
+def run_e2e(wl, args, world):
+    w8 = wl.w8
+    shapes = wl.shapes
+    pinned = [[t.pin_memory() for t in (x.A, x.a_s, x.B, x.b_s)] for x in wl.host]
+    tdt = {2: torch.bfloat16, 4: torch.float32}[wl.out_bytes]
+    outs = [torch.empty((M, N), dtype=tdt).pin_memory() for (M, N, K) in shapes]
+    stage = []
+    for (M, N, K) in shapes:
+        nb = w8.w8a8_block_fp8_host_staging_size(M, N, K, wl.out_code)
+        stage.append(torch.empty(nb, dtype=torch.uint8, device="cuda"))
+    stream = torch.cuda.current_stream()
+    h2d = sum(sum(t.numel() * t.element_size() for t in p) for p in pinned)
+    d2h = sum(o.numel() * o.element_size() for o in outs)
+
+    def step(_k):
+        for i, (M, N, K) in enumerate(shapes):
+            o = w8.options()
+            if wl.plans[i].workspace_bytes:
+                ws = wl.ws[0][i]
+                o.workspace_dev = ws.data_ptr()
+                o.workspace_bytes = ws.numel()
+            st = w8.w8a8_block_fp8_matmul_host(*pinned[i], outs[i], M, N, K, 128, 128,
+                                               wl.out_code, stage[i], stage[i].numel(),
+                                               stream, o)
+            w8.check(st)
+        stream.synchronize()    # the step's result is on the host
+
+    for k in range(max(1, args.warmup)):
+        step(k)
+    t_blk, _ = time_blocks(step, args.steps, world, 0.5)
+    t = t_blk / args.steps
+    flops, nbytes = workload_units(shapes, wl.out_bytes)
+    bound = bound_of(shapes)
+    value = nbytes * world / t / 1e9 if bound == "hbm" else flops * world / t / 1e12
+    return {"value": round(value, 3), "unit": "GB/s" if bound == "hbm" else "TFLOP/s",
+            "ms_per_step": round(t * 1e3, 4), "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "path": "w8a8_block_fp8_matmul_host (C ABI, pinned host buffers)"}
+
+
+# ---------------------------------------------------------------------- CPU oracle
+
+def _cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def oracle_sample_step(shapes, host, rows_per_shape):
+    """One oracle pass over a row sample of every shape; returns (flops, bytes) done."""
+    import numpy as np
+    import oracle
+    fl = by = 0
+    for (M, N, K), x in zip(shapes, host):
+        r = min(M, rows_per_shape)
+        rows = np.linspace(0, M - 1, r).astype(np.int64)
+        oracle.reference_c(x.A[rows], x.a_s[rows], x.B, x.b_s)
+        fl += synth.algorithmic_flops(r, N, K)
+        by += synth.algorithmic_bytes(r, N, K)
+    return fl, by
+
+
+def rows_for_budget(shapes, seconds_per_step):
+    """Rows per shape so that one oracle pass takes about seconds_per_step on this host
+    (assumes about 0.3 G multiply-adds per second per core)."""
+    macs_per_row = sum(N * K for (M, N, K) in shapes)
+    budget = 0.3e9 * _cores() * seconds_per_step
+    return max(1, int(budget // macs_per_row))
+
+
+def cpu_baseline(shapes, host, out_dtype, bound, seconds):
+    rows = min(max(M for M, _, _ in shapes), rows_for_budget(shapes, 1.0))
+    fl = by = 0
+    t0 = time.perf_counter()
+    n = 0
+    while True:
+        f, b = oracle_sample_step(shapes, host, rows)
+        fl += f
+        by += b
+        n += 1
+        if time.perf_counter() - t0 >= seconds or n >= 1000:
+            break
+    dt = time.perf_counter() - t0
+    value = by / dt / 1e9 if bound == "hbm" else fl / dt / 1e12
+    return {"value": round(value, 6), "unit": "GB/s" if bound == "hbm" else "TFLOP/s",
+            "cores": _cores(), "kind": "oracle",
+            "sample": f"{n} passes of up to {rows} rows per shape (all rows where M <= {rows}) "
+                      f"through the C oracle in {dt:.1f} s"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    spec = synth.WORKLOADS[args.workload]
+    shapes = spec["shapes"]
+    host = [synth.make_inputs(M, N, K, seed=0, outlier_p=spec["outlier_p"]) for (M, N, K) in shapes]
+    bound = bound_of(shapes)
+    budget = max(0.05, 120.0 / max(1, args.steps + args.warmup))
+    rows = min(max(M for M, _, _ in shapes), rows_for_budget(shapes, min(budget, 2.0)))
+    for _ in range(args.warmup):
+        oracle_sample_step(shapes, host, rows)
+    t0 = time.perf_counter()
+    fl = by = 0
+    for _ in range(args.steps):
+        f, b = oracle_sample_step(shapes, host, rows)
+        fl += f
+        by += b
+    dt = time.perf_counter() - t0
+    value = by / dt / 1e9 if bound == "hbm" else fl / dt / 1e12
+    unit = "GB/s" if bound == "hbm" else "TFLOP/s"
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": unit,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded N(0,1), block-quantised to E4M3 with amax/448 scales)",
+            "config": {"workload": args.workload, "shapes": [list(s) for s in shapes]},
+            "cpu_baseline": {"value": round(value, 6), "unit": unit, "cores": _cores(),
+                             "kind": "oracle",
+                             "sample": f"each step: up to {rows} rows per shape through the C "
+                                       f"oracle (double, all host cores)"},
+            "e2e": {"value": round(value, 6), "unit": unit, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse()
+    rank, world = dist_setup(args)
+    if args.impl == "reference":
+        res = run_reference(args, rank, world)
+    else:
+        res = run_ours(args, rank, world)
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,1 +1,66 @@
-"""GB300-native (sm_103a) W8A8 block-FP8 matmul."""
+"""GB300-native (sm_103a) W8A8 block-FP8 matmul.
+
+    C[m,n] = cast_out( sum_g a_s[m,g] * b_s[n/128,g] * sum_{k in g} A[m,k] * B[n,k] )
+
+("feat: optimize w8a8 block fp8 matmul for Hopper", FlagGems-vllm PR #693,
+Description and Numerical safety.)  The compute runs in the hand-written CUDA
+kernels of the shared library built from ``csrc/``; this package only
+marshals arguments to its C ABI (``include/w8a8_block_fp8.h``) and uses
+PyTorch for device memory and streams.  Loading is lazy, so that the seeded
+input generator ``synth`` can be imported without the library.
+"""
+from __future__ import annotations
+
+from ._binding import (  # noqa: F401
+    EXPORTED, W8A8Error, W8A8_OK, W8A8_ERR_INVALID_ARG, W8A8_ERR_UNSUPPORTED, W8A8_ERR_CUDA,
+    W8A8_ERR_DEVICE_TIMEOUT, W8A8_ERR_WORKSPACE, W8A8_ERR_NO_DEVICE, W8A8_OUT_BF16,
+    W8A8_OUT_FP16, W8A8_OUT_FP32, W8A8_VARIANT_AUTO, W8A8_VARIANT_TILED, W8A8_VARIANT_SWAPAB,
+    W8A8_VARIANT_SPLITK, check, library_path, load_library, w8a8_abi_version,
+    w8a8_block_fp8_host_staging_size, w8a8_block_fp8_matmul, w8a8_block_fp8_matmul_ex,
+    w8a8_block_fp8_matmul_host, w8a8_block_fp8_plan, w8a8_block_fp8_workspace_size,
+    w8a8_get_device_status, w8a8_last_error, w8a8_options, w8a8_shutdown, w8a8_status_string,
+)
+
+_OUT_CODES = {"bf16": W8A8_OUT_BF16, "fp16": W8A8_OUT_FP16, "fp32": W8A8_OUT_FP32}
+
+
+def out_code(dtype) -> int:
+    """W8A8_OUT_* code of a torch dtype or of 'bf16' / 'fp16' / 'fp32'."""
+    if isinstance(dtype, str):
+        return _OUT_CODES[dtype]
+    import torch
+    return {torch.bfloat16: W8A8_OUT_BF16, torch.float16: W8A8_OUT_FP16,
+            torch.float32: W8A8_OUT_FP32}[dtype]
+
+
+def options(**kw) -> w8a8_options:
+    """A w8a8_options with the given fields set (the rest zero = defaults)."""
+    o = w8a8_options()
+    for k, v in kw.items():
+        setattr(o, k, v)
+    return o
+
+
+def matmul(A, a_s, B, b_s, out_dtype="bf16", out=None, stream=None, **opts):
+    """C = A B^T with block de-quantisation, on CUDA tensors.
+
+    A: uint8 or float8_e4m3fn [M, K]; a_s: float32 [M, K/128]; B: uint8 or
+    float8_e4m3fn [N, K]; b_s: float32 [ceil(N/128), K/128].  ``out`` (a
+    preallocated [M, N] tensor) is optional; keyword options map to
+    w8a8_options fields.  Raises W8A8Error on a non-zero status.
+    """
+    import torch
+    M, K = A.shape
+    N = B.shape[0]
+    code = out_code(out_dtype)
+    if out is None:
+        tdt = {W8A8_OUT_BF16: torch.bfloat16, W8A8_OUT_FP16: torch.float16,
+               W8A8_OUT_FP32: torch.float32}[code]
+        out = torch.empty((M, N), dtype=tdt, device=A.device)
+    for t in (A, a_s, B, b_s, out):
+        if not t.is_contiguous():
+            raise W8A8Error(W8A8_ERR_UNSUPPORTED, "tensors must be contiguous row-major")
+    st = w8a8_block_fp8_matmul_ex(A, a_s, B, b_s, out, M, N, K, 128, 128, code, stream,
+                                  options(**opts) if opts else None)
+    check(st)
+    return out

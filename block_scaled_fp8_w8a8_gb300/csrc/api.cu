@@ -1,0 +1,634 @@
+// C ABI of the W8A8 block-FP8 matmul: argument validation, the (M, N, K)
+// dispatcher, TMA descriptor encoding, workspaces and launches.
+//
+// The page ("feat: optimize w8a8 block fp8 matmul for Hopper", FlagGems-vllm
+// PR #693, Description and Numerical safety) routes each (M, N, K) to a
+// specialised kernel behind a shape guard and keeps a generic kernel as the
+// fall-through.  Here every kernel covers the whole supported problem set, so
+// the dispatcher only chooses speed; the guards become the argument checks
+// that run before any CUDA call.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <utility>
+
+#include "../../include/w8a8_block_fp8.h"
+#include "dispatch_table.h"
+#include "kernels.cuh"
+
+using namespace w8a8;
+
+namespace {
+
+thread_local char g_last_error[512] = "";
+
+w8a8_status fail(w8a8_status st, const char *fmt, ...)
+{
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+w8a8_status cuda_fail(cudaError_t e, const char *what)
+{
+    return fail(W8A8_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+constexpr unsigned long long kDefaultWaitLimit = 1ull << 32;   // ~2 s at 2 GHz
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+    bool ready = false;
+    bool supported = false;
+    int sm_count = 0;
+    int major = 0, minor = 0;
+    size_t smem_optin = 0;
+    unsigned *status = nullptr;
+};
+
+std::mutex g_mutex;
+DeviceInfo g_devices[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+// Per-(device, stream) split-K workspace owned by the library.
+struct Workspace {
+    void *ptr = nullptr;
+    size_t bytes = 0;
+};
+std::map<std::pair<int, cudaStream_t>, Workspace> g_workspaces;
+
+w8a8_status current_device(int *dev_out, DeviceInfo *info_out)
+{
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return fail(W8A8_ERR_NO_DEVICE, "no CUDA device: %s", cudaGetErrorString(e));
+    if (dev < 0 || dev >= kMaxDevices)
+        return fail(W8A8_ERR_NO_DEVICE, "device ordinal %d out of range", dev);
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceInfo &d = g_devices[dev];
+    if (!d.ready) {
+        cudaDeviceProp prop;
+        e = cudaGetDeviceProperties(&prop, dev);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "cudaGetDeviceProperties");
+        d.sm_count = prop.multiProcessorCount;
+        d.major = prop.major;
+        d.minor = prop.minor;
+        d.smem_optin = prop.sharedMemPerBlockOptin;
+        d.supported = prop.major == 10;   // the tcgen05 / TMEM family (sm_100, sm_103)
+        if (d.supported) {
+            e = status_word_address(&d.status);
+            if (e != cudaSuccess)
+                return cuda_fail(e, "status word lookup (is the library built for this GPU?)");
+        }
+        if (!g_encode) {
+            cudaDriverEntryPointQueryResult q;
+            void *fn = nullptr;
+            e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                 cudaEnableDefault, &q);
+            if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
+                return fail(W8A8_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+        }
+        d.ready = true;
+    }
+    if (!d.supported)
+        return fail(W8A8_ERR_NO_DEVICE, "device %d is sm_%d%d; this library needs sm_100/sm_103",
+                    dev, d.major, d.minor);
+    *dev_out = dev;
+    *info_out = d;
+    return W8A8_OK;
+}
+
+// 2-D uint8 tensor map over a row-major [rows, cols] matrix; boxes of
+// 128 columns (one K group, 128 bytes) by box_rows rows, 128-byte swizzle,
+// out-of-range elements read as zero.
+w8a8_status encode_u8_map(CUtensorMap *map, const void *base, int64_t rows, int64_t cols,
+                          int box_rows)
+{
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols)};
+    cuuint32_t box[2] = {128u, static_cast<cuuint32_t>(box_rows)};
+    cuuint32_t elem[2] = {1u, 1u};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims,
+                          strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(W8A8_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for [%lld, %lld] box %d",
+                    static_cast<int>(r), static_cast<long long>(rows),
+                    static_cast<long long>(cols), box_rows);
+    return W8A8_OK;
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+w8a8_status check_problem(int64_t M, int64_t N, int64_t K, int block_n, int block_k, int out)
+{
+    if (M < 0 || N < 0 || K < 0)
+        return fail(W8A8_ERR_INVALID_ARG, "negative size (M=%lld N=%lld K=%lld)",
+                    (long long)M, (long long)N, (long long)K);
+    if (out < W8A8_OUT_BF16 || out > W8A8_OUT_FP32)
+        return fail(W8A8_ERR_INVALID_ARG, "unknown out_dtype %d", out);
+    if (block_n != 128 || block_k != 128)
+        return fail(W8A8_ERR_UNSUPPORTED, "block_n=%d block_k=%d: only [128, 128] scale blocks",
+                    block_n, block_k);
+    if (N < 1 || K < 128)
+        return fail(W8A8_ERR_UNSUPPORTED, "N=%lld K=%lld: need N >= 1 and K >= 128",
+                    (long long)N, (long long)K);
+    if (K % 128 != 0)
+        return fail(W8A8_ERR_UNSUPPORTED, "K=%lld is not a multiple of 128", (long long)K);
+    if (N % 16 != 0)
+        return fail(W8A8_ERR_UNSUPPORTED, "N=%lld is not a multiple of 16", (long long)N);
+    if (M > (1ll << 31) - 1 || N > (1ll << 31) - 1 || K > (1ll << 31) - 1)
+        return fail(W8A8_ERR_UNSUPPORTED, "sizes must be below 2^31");
+    return W8A8_OK;
+}
+
+w8a8_status check_options(const w8a8_options *o)
+{
+    if (!o)
+        return W8A8_OK;
+    if (o->variant < W8A8_VARIANT_AUTO || o->variant > W8A8_VARIANT_SPLITK)
+        return fail(W8A8_ERR_INVALID_ARG, "unknown variant %d", o->variant);
+    if (o->split_k < 0 || o->stages < 0 || o->stages > 8 || o->grid_limit < 0 || o->m_tile < 0 ||
+        o->debug_skip_load < 0)
+        return fail(W8A8_ERR_INVALID_ARG, "negative or out-of-range option");
+    if (o->block_n_tile != 0 && o->block_n_tile != 128 && o->block_n_tile != 256)
+        return fail(W8A8_ERR_INVALID_ARG, "block_n_tile must be 0, 128 or 256");
+    if (o->m_tile != 0 && (o->m_tile % 16 != 0 || o->m_tile > 256))
+        return fail(W8A8_ERR_INVALID_ARG, "m_tile must be a multiple of 16 up to 256");
+    return W8A8_OK;
+}
+
+int mt_for(int mma_n)
+{
+    return mma_n <= 32 ? 32 : mma_n <= 64 ? 64 : mma_n <= 128 ? 128 : 256;
+}
+
+// The launch plan of one call.
+struct Plan {
+    int variant;      // W8A8_VARIANT_TILED / SWAPAB / SPLITK
+    int bn;           // tiled
+    int stages;
+    int grid;         // tiled: persistent CTAs
+    int mma_n, mt, m_tiles, splits, gps;   // swap family
+    size_t smem;
+};
+
+w8a8_status make_plan(int64_t M, int64_t N, int64_t K, const w8a8_options *o,
+                      const DeviceInfo &dev, Plan *pl)
+{
+    const int G = static_cast<int>(K / 128);
+    const int NB = static_cast<int>(cdiv(N, 128));
+    std::memset(pl, 0, sizeof(*pl));
+    int variant = o ? o->variant : W8A8_VARIANT_AUTO;
+    int split_hint = o ? o->split_k : 0;
+    int mtile_hint = o ? o->m_tile : 0;
+    int bn_hint = o ? o->block_n_tile : 0;
+    int stage_hint = o ? o->stages : 0;
+
+    if (variant == W8A8_VARIANT_AUTO) {
+        const TableEntry *t = lookup_tuned(M, N, K);
+        if (t) {
+            variant = t->variant;
+            if (!split_hint) split_hint = t->split_k;
+            if (!mtile_hint) mtile_hint = t->m_tile;
+            if (!bn_hint) bn_hint = t->block_n_tile;
+            if (!stage_hint) stage_hint = t->stages;
+        } else if (M <= 256) {
+            variant = W8A8_VARIANT_SWAPAB;
+            const int64_t ctas = NB;
+            if (ctas * 2 <= dev.sm_count && G >= 4)
+                variant = W8A8_VARIANT_SPLITK;
+        } else {
+            variant = W8A8_VARIANT_TILED;
+        }
+    }
+    pl->variant = variant;
+
+    if (variant == W8A8_VARIANT_TILED) {
+        int bn = bn_hint ? bn_hint : (N % 256 == 0 ? 256 : 128);
+        int stages = bn == 256 ? 4 : (stage_hint == 4 ? 4 : 6);
+        const int64_t tiles = cdiv(M, 128) * cdiv(N, bn);
+        int64_t grid = std::min<int64_t>(tiles, dev.sm_count);
+        if (o && o->grid_limit)
+            grid = std::min<int64_t>(grid, o->grid_limit);
+        pl->bn = bn;
+        pl->stages = stages;
+        pl->grid = static_cast<int>(std::max<int64_t>(grid, 1));
+        pl->smem = tiled_smem_bytes(bn, stages);
+        if (pl->smem == 0 || pl->smem > dev.smem_optin)
+            return fail(W8A8_ERR_UNSUPPORTED, "tiled kernel needs %zu B of shared memory",
+                        pl->smem);
+        return W8A8_OK;
+    }
+
+    // swap-AB family
+    int m_tiles, mma_n;
+    if (mtile_hint) {
+        mma_n = mtile_hint;
+        m_tiles = static_cast<int>(cdiv(M, mma_n));
+    } else {
+        m_tiles = static_cast<int>(cdiv(M, 256));
+        mma_n = static_cast<int>(cdiv(cdiv(M, m_tiles), 16) * 16);
+    }
+    mma_n = std::max(mma_n, 16);
+    const int mt = mt_for(mma_n);
+    int splits = 1;
+    if (variant == W8A8_VARIANT_SPLITK) {
+        if (split_hint) {
+            splits = split_hint;
+        } else {
+            const int64_t ctas = static_cast<int64_t>(NB) * m_tiles;
+            splits = static_cast<int>(std::max<int64_t>(1, dev.sm_count / std::max<int64_t>(ctas, 1)));
+        }
+        splits = std::min(std::max(splits, 1), G);
+    }
+    int gps = static_cast<int>(cdiv(G, splits));
+    splits = static_cast<int>(cdiv(G, gps));       // every split non-empty
+    int max_stages = std::min(8, gps);
+    int stages = stage_hint ? std::min(stage_hint, max_stages) : max_stages;
+    while (stages > 1 && swapab_smem_bytes(mt, stages, gps) > dev.smem_optin)
+        --stages;
+    if (stages < 2 && gps > 1 && swapab_smem_bytes(mt, 2, gps) > dev.smem_optin)
+        return fail(W8A8_ERR_UNSUPPORTED,
+                    "K=%lld is too long for one swap-AB CTA; use the split-K variant",
+                    (long long)K);
+    pl->mma_n = mma_n;
+    pl->mt = mt;
+    pl->m_tiles = m_tiles;
+    pl->splits = splits;
+    pl->gps = gps;
+    pl->stages = stages;
+    pl->smem = swapab_smem_bytes(mt, stages, gps);
+    if (splits == 1)
+        pl->variant = W8A8_VARIANT_SWAPAB;
+    return W8A8_OK;
+}
+
+size_t splitk_workspace_bytes(int64_t M, int64_t N, const Plan &pl)
+{
+    if (pl.variant != W8A8_VARIANT_SPLITK || pl.splits <= 1)
+        return 0;
+    const size_t partial = static_cast<size_t>(pl.splits) * M * N * 4;
+    const size_t partial_aligned = (partial + 255) / 256 * 256;
+    const size_t counters = static_cast<size_t>(pl.m_tiles) * cdiv(N, 128) * 4;
+    return partial_aligned + (counters + 255) / 256 * 256;
+}
+
+w8a8_status library_workspace(int dev, cudaStream_t stream, size_t bytes, void **out)
+{
+    std::lock_guard<std::mutex> lock(g_mutex);
+    Workspace &w = g_workspaces[std::make_pair(dev, stream)];
+    if (w.bytes >= bytes) {
+        *out = w.ptr;
+        return W8A8_OK;
+    }
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    cudaError_t e = cudaStreamIsCapturing(stream, &cap);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaStreamIsCapturing");
+    if (cap != cudaStreamCaptureStatusNone)
+        return fail(W8A8_ERR_WORKSPACE,
+                    "split-K workspace would have to grow during stream capture; "
+                    "pass w8a8_options.workspace_dev or call once before capturing");
+    if (w.ptr) {
+        e = cudaFree(w.ptr);   // synchronises with work still using it
+        w.ptr = nullptr;
+        w.bytes = 0;
+        if (e != cudaSuccess)
+            return cuda_fail(e, "cudaFree(workspace)");
+    }
+    e = cudaMalloc(&w.ptr, bytes);
+    if (e != cudaSuccess) {
+        w.ptr = nullptr;
+        return cuda_fail(e, "cudaMalloc(workspace)");
+    }
+    e = cudaMemset(w.ptr, 0, bytes);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaMemset(workspace)");
+    w.bytes = bytes;
+    *out = w.ptr;
+    return W8A8_OK;
+}
+
+w8a8_status run(const void *A, const float *a_s, const void *B, const float *b_s, void *C,
+                int64_t M, int64_t N, int64_t K, int block_n, int block_k, int out,
+                cudaStream_t stream, const w8a8_options *o)
+{
+    g_last_error[0] = '\0';
+    w8a8_status st = check_problem(M, N, K, block_n, block_k, out);
+    if (st != W8A8_OK)
+        return st;
+    if ((st = check_options(o)) != W8A8_OK)
+        return st;
+    if (M == 0)
+        return W8A8_OK;
+    if (!A || !a_s || !B || !b_s || !C)
+        return fail(W8A8_ERR_INVALID_ARG, "null pointer argument");
+    if (!aligned(A, 16) || !aligned(B, 16) || !aligned(C, 16))
+        return fail(W8A8_ERR_UNSUPPORTED, "A, B and C must be 16-byte aligned");
+    if (!aligned(a_s, 4) || !aligned(b_s, 4))
+        return fail(W8A8_ERR_UNSUPPORTED, "a_s and b_s must be 4-byte aligned");
+
+    int dev;
+    DeviceInfo info;
+    if ((st = current_device(&dev, &info)) != W8A8_OK)
+        return st;
+    Plan pl;
+    if ((st = make_plan(M, N, K, o, info, &pl)) != W8A8_OK)
+        return st;
+
+    const int G = static_cast<int>(K / 128);
+    const int NB = static_cast<int>(cdiv(N, 128));
+    const unsigned long long limit =
+        (o && o->wait_limit_cycles) ? o->wait_limit_cycles : kDefaultWaitLimit;
+    const int debug_skip = (o && o->debug_skip_load > 0) ? o->debug_skip_load - 1 : -1;
+    LaunchCfg cfg;
+    cfg.stages = pl.stages;
+    cfg.grid = pl.grid;
+    cfg.pdl = o ? o->pdl : 0;
+    cfg.stream = stream;
+
+    cudaError_t e;
+    if (pl.variant == W8A8_VARIANT_TILED) {
+        CUtensorMap mA, mB;
+        if ((st = encode_u8_map(&mA, A, M, K, 128)) != W8A8_OK ||
+            (st = encode_u8_map(&mB, B, N, K, pl.bn)) != W8A8_OK)
+            return st;
+        TiledParams p;
+        p.a_s = a_s;
+        p.b_s = b_s;
+        p.C = C;
+        p.M = static_cast<int>(M);
+        p.N = static_cast<int>(N);
+        p.K = static_cast<int>(K);
+        p.G = G;
+        p.NB = NB;
+        p.num_m_tiles = static_cast<int>(cdiv(M, 128));
+        p.num_n_tiles = static_cast<int>(cdiv(N, pl.bn));
+        p.num_tiles = p.num_m_tiles * p.num_n_tiles;
+        p.out_kind = out;
+        p.debug_skip_tma = debug_skip;
+        p.status = info.status;
+        p.wait_limit = limit;
+        e = launch_tiled(mA, mB, p, pl.bn, cfg);
+    } else {
+        CUtensorMap mW, mX;
+        if ((st = encode_u8_map(&mW, B, N, K, 128)) != W8A8_OK ||
+            (st = encode_u8_map(&mX, A, M, K, pl.mma_n)) != W8A8_OK)
+            return st;
+        SwapParams p;
+        p.a_s = a_s;
+        p.b_s = b_s;
+        p.C = C;
+        p.ws = nullptr;
+        p.counters = nullptr;
+        const size_t ws_bytes = splitk_workspace_bytes(M, N, pl);
+        if (ws_bytes) {
+            void *ws = o ? o->workspace_dev : nullptr;
+            if (ws) {
+                if (o->workspace_bytes < ws_bytes || !aligned(ws, 256))
+                    return fail(W8A8_ERR_WORKSPACE,
+                                "workspace of %zu bytes at %p: need %zu bytes, 256-byte aligned",
+                                o->workspace_bytes, ws, ws_bytes);
+            } else if ((st = library_workspace(dev, stream, ws_bytes, &ws)) != W8A8_OK) {
+                return st;
+            }
+            const size_t partial = static_cast<size_t>(pl.splits) * M * N * 4;
+            p.ws = static_cast<float *>(ws);
+            p.counters = reinterpret_cast<unsigned *>(static_cast<char *>(ws) +
+                                                      (partial + 255) / 256 * 256);
+        }
+        p.M = static_cast<int>(M);
+        p.N = static_cast<int>(N);
+        p.K = static_cast<int>(K);
+        p.G = G;
+        p.NB = NB;
+        p.mma_n = pl.mma_n;
+        p.num_m_tiles = pl.m_tiles;
+        p.splits = pl.splits;
+        p.groups_per_split = pl.gps;
+        p.out_kind = out;
+        p.debug_skip_tma = debug_skip;
+        p.status = info.status;
+        p.wait_limit = limit;
+        e = launch_swapab(mW, mX, p, pl.mt, cfg);
+    }
+    if (e != cudaSuccess)
+        return cuda_fail(e, "kernel launch");
+    return W8A8_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+w8a8_status w8a8_block_fp8_matmul(const void *A_dev, const float *a_s_dev, const void *B_dev,
+                                  const float *b_s_dev, void *C_dev, int64_t M, int64_t N,
+                                  int64_t K, int block_n, int block_k, w8a8_out_dtype out_dtype,
+                                  w8a8_stream_t stream)
+{
+    return run(A_dev, a_s_dev, B_dev, b_s_dev, C_dev, M, N, K, block_n, block_k, out_dtype,
+               reinterpret_cast<cudaStream_t>(stream), nullptr);
+}
+
+w8a8_status w8a8_block_fp8_matmul_ex(const void *A_dev, const float *a_s_dev, const void *B_dev,
+                                     const float *b_s_dev, void *C_dev, int64_t M, int64_t N,
+                                     int64_t K, int block_n, int block_k,
+                                     w8a8_out_dtype out_dtype, w8a8_stream_t stream,
+                                     const w8a8_options *opts)
+{
+    return run(A_dev, a_s_dev, B_dev, b_s_dev, C_dev, M, N, K, block_n, block_k, out_dtype,
+               reinterpret_cast<cudaStream_t>(stream), opts);
+}
+
+size_t w8a8_block_fp8_host_staging_size(int64_t M, int64_t N, int64_t K, w8a8_out_dtype out)
+{
+    if (check_problem(M, N, K, 128, 128, out) != W8A8_OK)
+        return 0;
+    const int64_t G = K / 128;
+    auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+    const size_t ob = out == W8A8_OUT_FP32 ? 4 : 2;
+    return up(M * K) + up(M * G * 4) + up(N * K) + up(cdiv(N, 128) * G * 4) + up(M * N * ob);
+}
+
+w8a8_status w8a8_block_fp8_matmul_host(const void *A_host, const float *a_s_host,
+                                       const void *B_host, const float *b_s_host, void *C_host,
+                                       int64_t M, int64_t N, int64_t K, int block_n, int block_k,
+                                       w8a8_out_dtype out_dtype, void *staging_dev,
+                                       size_t staging_bytes, w8a8_stream_t stream,
+                                       const w8a8_options *opts)
+{
+    g_last_error[0] = '\0';
+    w8a8_status st = check_problem(M, N, K, block_n, block_k, out_dtype);
+    if (st != W8A8_OK)
+        return st;
+    if (M == 0)
+        return W8A8_OK;
+    if (!A_host || !a_s_host || !B_host || !b_s_host || !C_host || !staging_dev)
+        return fail(W8A8_ERR_INVALID_ARG, "null pointer argument");
+    const size_t need = w8a8_block_fp8_host_staging_size(M, N, K, out_dtype);
+    if (staging_bytes < need || !aligned(staging_dev, 256))
+        return fail(W8A8_ERR_WORKSPACE, "staging of %zu bytes: need %zu, 256-byte aligned",
+                    staging_bytes, need);
+    const int64_t G = K / 128;
+    auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+    const size_t ob = out_dtype == W8A8_OUT_FP32 ? 4 : 2;
+    char *p = static_cast<char *>(staging_dev);
+    char *dA = p;
+    char *das = dA + up(M * K);
+    char *dB = das + up(M * G * 4);
+    char *dbs = dB + up(N * K);
+    char *dC = dbs + up(cdiv(N, 128) * G * 4);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const struct {
+        void *dst;
+        const void *src;
+        size_t n;
+    } copies[4] = {{dA, A_host, static_cast<size_t>(M * K)},
+                   {das, a_s_host, static_cast<size_t>(M * G * 4)},
+                   {dB, B_host, static_cast<size_t>(N * K)},
+                   {dbs, b_s_host, static_cast<size_t>(cdiv(N, 128) * G * 4)}};
+    for (const auto &c : copies) {
+        cudaError_t e = cudaMemcpyAsync(c.dst, c.src, c.n, cudaMemcpyHostToDevice, s);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "cudaMemcpyAsync(host to device)");
+    }
+    st = run(dA, reinterpret_cast<const float *>(das), dB, reinterpret_cast<const float *>(dbs),
+             dC, M, N, K, block_n, block_k, out_dtype, s, opts);
+    if (st != W8A8_OK)
+        return st;
+    cudaError_t e = cudaMemcpyAsync(C_host, dC, static_cast<size_t>(M * N * ob),
+                                    cudaMemcpyDeviceToHost, s);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaMemcpyAsync(device to host)");
+    return W8A8_OK;
+}
+
+size_t w8a8_block_fp8_workspace_size(int64_t M, int64_t N, int64_t K, const w8a8_options *opts)
+{
+    if (check_problem(M, N, K, 128, 128, W8A8_OUT_BF16) != W8A8_OK || check_options(opts) != W8A8_OK)
+        return 0;
+    int dev;
+    DeviceInfo info;
+    if (current_device(&dev, &info) != W8A8_OK)
+        return 0;
+    Plan pl;
+    if (make_plan(M, N, K, opts, info, &pl) != W8A8_OK)
+        return 0;
+    return splitk_workspace_bytes(M, N, pl);
+}
+
+w8a8_status w8a8_block_fp8_plan(int64_t M, int64_t N, int64_t K, w8a8_out_dtype out_dtype,
+                                const w8a8_options *opts, w8a8_options *plan_out)
+{
+    g_last_error[0] = '\0';
+    if (!plan_out)
+        return fail(W8A8_ERR_INVALID_ARG, "plan_out is NULL");
+    w8a8_status st = check_problem(M, N, K, 128, 128, out_dtype);
+    if (st != W8A8_OK || (st = check_options(opts)) != W8A8_OK)
+        return st;
+    int dev;
+    DeviceInfo info;
+    if ((st = current_device(&dev, &info)) != W8A8_OK)
+        return st;
+    Plan pl;
+    if ((st = make_plan(M, N, K, opts, info, &pl)) != W8A8_OK)
+        return st;
+    std::memset(plan_out, 0, sizeof(*plan_out));
+    plan_out->variant = pl.variant;
+    plan_out->split_k = pl.splits;
+    plan_out->block_n_tile = pl.bn;
+    plan_out->m_tile = pl.mma_n;
+    plan_out->stages = pl.stages;
+    plan_out->grid_limit = pl.grid;
+    plan_out->workspace_bytes = splitk_workspace_bytes(M, N, pl);
+    return W8A8_OK;
+}
+
+w8a8_status w8a8_get_device_status(unsigned *detail_out)
+{
+    g_last_error[0] = '\0';
+    int dev;
+    DeviceInfo info;
+    w8a8_status st = current_device(&dev, &info);
+    if (st != W8A8_OK)
+        return st;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaDeviceSynchronize");
+    unsigned word = 0, zero = 0;
+    e = cudaMemcpy(&word, info.status, sizeof(word), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "reading the status word");
+    if (word != 0) {
+        e = cudaMemcpy(info.status, &zero, sizeof(zero), cudaMemcpyHostToDevice);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "clearing the status word");
+        // A kernel that gave up may have left split-K arrival counters raised:
+        // drop the cached workspaces of this device so they start from zero.
+        std::lock_guard<std::mutex> lock(g_mutex);
+        for (auto it = g_workspaces.begin(); it != g_workspaces.end();) {
+            if (it->first.first == dev) {
+                cudaFree(it->second.ptr);
+                it = g_workspaces.erase(it);
+            } else {
+                ++it;
+            }
+        }
+    }
+    if (detail_out)
+        *detail_out = word;
+    if (word == 0)
+        return W8A8_OK;
+    return fail(static_cast<w8a8_status>(word & 0xFFu), "device wait site %u gave up",
+                (word >> 8) & 0xFFu);
+}
+
+const char *w8a8_status_string(w8a8_status s)
+{
+    switch (s) {
+    case W8A8_OK: return "W8A8_OK";
+    case W8A8_ERR_INVALID_ARG: return "W8A8_ERR_INVALID_ARG: invalid argument";
+    case W8A8_ERR_UNSUPPORTED: return "W8A8_ERR_UNSUPPORTED: problem outside the supported set";
+    case W8A8_ERR_CUDA: return "W8A8_ERR_CUDA: a CUDA call failed";
+    case W8A8_ERR_DEVICE_TIMEOUT: return "W8A8_ERR_DEVICE_TIMEOUT: a bounded device wait ran out";
+    case W8A8_ERR_WORKSPACE: return "W8A8_ERR_WORKSPACE: workspace too small or misaligned";
+    case W8A8_ERR_NO_DEVICE: return "W8A8_ERR_NO_DEVICE: no usable sm_100-family device";
+    default: return "unknown w8a8_status";
+    }
+}
+
+const char *w8a8_last_error(void) { return g_last_error; }
+
+int w8a8_abi_version(void) { return W8A8_ABI_VERSION; }
+
+void w8a8_shutdown(void)
+{
+    std::lock_guard<std::mutex> lock(g_mutex);
+    int cur = -1;
+    cudaGetDevice(&cur);
+    for (auto &kv : g_workspaces) {
+        cudaSetDevice(kv.first.first);
+        cudaFree(kv.second.ptr);
+    }
+    g_workspaces.clear();
+    if (cur >= 0)
+        cudaSetDevice(cur);
+}
+
+}  // extern "C"

@@ -1,0 +1,368 @@
+// Swap-AB W8A8 block-FP8 matmul for decode-size M on sm_103a, with an optional
+// deterministic split of the K groups.
+//
+// Operation ("feat: optimize w8a8 block fp8 matmul for Hopper", FlagGems-vllm
+// PR #693, Description):
+//   C[m,n] = cast( sum_g a_s[m,g] * b_s[n/128,g] * sum_{k in g} A[m,k] B[n,k] )
+//
+// The page's swap_ab idea: compute C^T = B A^T so that the few tokens sit on
+// the MMA's N dimension and 128 weight rows fill its M dimension.  Here one
+// CTA owns exactly one 128-row block of B, so b_s[n/128, g] is one scalar per
+// group for the whole CTA, and it is folded into the per-token scale once
+// (s[g][j] = a_s[m0+j, g] * b_s[nb, g]) before the main loop -- the page's
+// short_k256 pre-fold.  The swap_ab_splitk idea: grid.y CTAs split the K
+// groups of one tile; each writes its fp32 partial tile to a workspace and the
+// last CTA to arrive (an atomic ticket, no spinning) sums the partials in
+// split order 0..S-1 and casts, so the result is the same bit for bit on
+// every run (the page's atomic_add version is not).
+//
+// Per CTA: warp 0 TMA producer (B block 128 x 128 B and the token tile
+// mma_n x 128 B per group), warp 1 MMA issuer (tcgen05.mma kind::f8f6f4,
+// M = 128, N = mma_n, 4 x K=32 per group) into one of two TMEM buffers,
+// 1 or 2 promotion warpgroups: thread = weight row n, columns = tokens.
+#include "kernels.cuh"
+#include "ptx.cuh"
+
+namespace w8a8 {
+
+namespace {
+
+constexpr int kMaxStages = 8;
+
+template <int MT> struct SwapLayout {
+    static constexpr int kPromoWG = MT > 128 ? 2 : 1;
+    static constexpr int kCols = MT / kPromoWG;      // token columns per promotion thread
+    static constexpr int kThreads = 128 + 128 * kPromoWG;
+    static constexpr uint32_t kWBytes = 128u * 128u;
+    static constexpr uint32_t kXBytes = static_cast<uint32_t>(MT) * 128u;
+    static constexpr uint32_t kTmemCols = 2 * MT < 32 ? 32 : 2 * MT;
+    static constexpr int kBars = 2 * kMaxStages + 5;
+    static size_t smem(int stages, int gps)
+    {
+        return 1024 + static_cast<size_t>(stages) * (kWBytes + kXBytes) +
+               static_cast<size_t>(gps) * MT * 4 + kBars * 8 + 16;
+    }
+};
+
+__device__ __forceinline__ void store_one(void *C, size_t idx, float v, int out_kind)
+{
+    if (out_kind == OUT_BF16)
+        static_cast<__nv_bfloat16 *>(C)[idx] = __float2bfloat16_rn(v);
+    else if (out_kind == OUT_FP16)
+        static_cast<__half *>(C)[idx] = __float2half_rn(v);
+    else
+        static_cast<float *>(C)[idx] = v;
+}
+
+template <int MT>
+__global__ void __launch_bounds__(SwapLayout<MT>::kThreads, 1)
+    k_swapab(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+             const SwapParams p, const int stages)
+{
+    using L = SwapLayout<MT>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const uint32_t sW = smem_addr(smem);
+    const uint32_t sX = sW + stages * L::kWBytes;
+    float *sscale = reinterpret_cast<float *>(smem + stages * (L::kWBytes + L::kXBytes));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sscale + p.groups_per_split * MT);
+    const uint32_t bar0 = smem_addr(bars);
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (kMaxStages + s); };
+    auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * kMaxStages + b); };
+    auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * kMaxStages + 2 + b); };
+    const uint32_t drain_bar = bar0 + 8u * (2 * kMaxStages + 4);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + L::kBars);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    volatile int *last_flag = reinterpret_cast<volatile int *>(tmem_slot + 2);
+
+    const uint32_t warp = warp_index(), lane = lane_index();
+    const int nb = blockIdx.x;                 // 128-row block of B (and of C's columns)
+    const int split = blockIdx.y;
+    const int m0 = blockIdx.z * p.mma_n;
+    const int g_begin = split * p.groups_per_split;
+    const int g_end = min(p.G, g_begin + p.groups_per_split);
+    const int ng = g_end - g_begin;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < stages; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(tfull_bar(b), 1);
+            mbar_init(tempty_bar(b), 4 * L::kPromoWG);
+        }
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        *last_flag = 0;
+        mbar_fence_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_map(&tmW);
+        tma_prefetch_map(&tmX);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_addr(tmem_slot), L::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem_base = *tmem_slot;
+    const WaitGuard guard{abort_flag, p.status, p.wait_limit};
+
+    grid_launch_dependents();
+    grid_dependency_wait();
+
+    if (warp < 4) {
+        if constexpr (L::kPromoWG == 2)
+            regs_dealloc<40>();
+        if (warp == 0 && lane == 0) {
+            // ---------------------------------------------------------- TMA producer
+            const uint32_t tx = L::kWBytes + static_cast<uint32_t>(p.mma_n) * 128u;
+            int stage = 0;
+            uint32_t phase = 0;
+            int issued = 0;
+            bool ok = true;
+            for (int g = g_begin; g < g_end; ++g) {
+                if (!wait_bounded(empty_bar(stage), phase ^ 1u, guard, SITE_SWAP_PRODUCER)) {
+                    ok = false;
+                    break;
+                }
+                if (issued != p.debug_skip_tma) {
+                    mbar_arrive_expect_tx(full_bar(stage), tx);
+                    tma_load_2d(sW + stage * L::kWBytes, &tmW, full_bar(stage), g * 128, nb * 128);
+                    tma_load_2d(sX + stage * L::kXBytes, &tmX, full_bar(stage), g * 128, m0);
+                }
+                ++issued;
+                if (++stage == stages) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            if (ok) {
+                // Tail: wait until the MMA has released every stage, so that no
+                // commit arrives on this CTA's shared memory after it exits.
+                for (int s = 0; s < stages && ok; ++s) {
+                    ok = wait_bounded(empty_bar(stage), phase ^ 1u, guard, SITE_SWAP_PRODUCER);
+                    if (++stage == stages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            } else {
+                for (int s = 0; s < stages; ++s) {
+                    const bool this_round = s < stage;
+                    if (!this_round && issued < stages && s >= issued)
+                        continue;
+                    wait_drain(full_bar(s), this_round ? phase : (phase ^ 1u), p.status,
+                               p.wait_limit, (SITE_DRAIN << 8) | 4u);
+                }
+            }
+        } else if (warp == 1 && lane == 0) {
+            // ---------------------------------------------------------- MMA issuer
+            const uint32_t idesc = idesc_e4m3_f32(128, static_cast<uint32_t>(p.mma_n));
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            for (int i = 0; i < ng; ++i) {
+                const uint32_t buf = i & 1;
+                const uint32_t bphase = (i >> 1) & 1;
+                if (!wait_bounded(tempty_bar(buf), bphase ^ 1u, guard, SITE_SWAP_MMA_TMEM) ||
+                    !wait_bounded(full_bar(stage), phase, guard, SITE_SWAP_MMA_FULL)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
+                const uint32_t d = tmem_base + buf * MT;
+                const uint64_t ad = sw128_kmajor_desc(sW + stage * L::kWBytes);
+                const uint64_t bd = sw128_kmajor_desc(sX + stage * L::kXBytes);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_e4m3(d, ad + 2u * kk, bd + 2u * kk, idesc, kk > 0 ? 1u : 0u);
+                mma_commit(empty_bar(stage));
+                mma_commit(tfull_bar(buf));
+                if (++stage == stages) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            if (!ok) {
+                mma_commit(drain_bar);
+                wait_drain(drain_bar, 0, p.status, p.wait_limit, (SITE_DRAIN << 8) | 4u);
+            }
+        }
+        __syncwarp();
+    } else {
+        // -------------------------------------------------------------- promotion + epilogue
+        if constexpr (L::kPromoWG == 2)
+            regs_alloc<232>();
+        const int tid = static_cast<int>(threadIdx.x) - 128;
+        constexpr int kPromoThreads = 128 * L::kPromoWG;
+        const int h = tid / 128;                             // column half
+        const uint32_t q = warp & 3u;                        // TMEM lane quarter
+        const int n = nb * 128 + static_cast<int>(q * 32 + lane);
+        const int c0 = h * L::kCols;                         // first token column of this thread
+
+        // Folded scales s[g][j] = a_s[m0+j, g] * b_s[nb, g] (zero past M and mma_n).
+        for (int idx = tid; idx < ng * MT; idx += kPromoThreads) {
+            const int gl = idx / MT, j = idx - gl * MT;
+            const int m = m0 + j;
+            float v = 0.f;
+            if (j < p.mma_n && m < p.M) {
+                const int g = g_begin + gl;
+                v = __ldg(p.a_s + static_cast<size_t>(m) * p.G + g) *
+                    __ldg(p.b_s + static_cast<size_t>(nb) * p.G + g);
+            }
+            sscale[idx] = v;
+        }
+        named_barrier(1, kPromoThreads);
+
+        float acc[L::kCols];
+#pragma unroll
+        for (int j = 0; j < L::kCols; ++j)
+            acc[j] = 0.f;
+        bool ok = true;
+        for (int i = 0; i < ng; ++i) {
+            const uint32_t buf = i & 1;
+            const uint32_t bphase = (i >> 1) & 1;
+            ok = __all_sync(0xffffffffu,
+                            wait_bounded(tfull_bar(buf), bphase, guard, SITE_SWAP_PROMOTE));
+            if (!ok)
+                break;
+            tc_fence_after_sync();
+            const uint32_t taddr = tmem_base + ((q * 32u) << 16) + buf * MT + c0;
+            const float *sc = sscale + i * MT + c0;
+#pragma unroll
+            for (int c = 0; c < L::kCols / 32; ++c) {
+                if (c0 + 32 * c < p.mma_n) {
+                    float v[32];
+                    tmem_load_32cols(taddr + 32u * c, v);
+#pragma unroll
+                    for (int j = 0; j < 32; j += 4) {
+                        const float4 s4 = *reinterpret_cast<const float4 *>(sc + 32 * c + j);
+                        acc[32 * c + j + 0] = fmaf(s4.x, v[j + 0], acc[32 * c + j + 0]);
+                        acc[32 * c + j + 1] = fmaf(s4.y, v[j + 1], acc[32 * c + j + 1]);
+                        acc[32 * c + j + 2] = fmaf(s4.z, v[j + 2], acc[32 * c + j + 2]);
+                        acc[32 * c + j + 3] = fmaf(s4.w, v[j + 3], acc[32 * c + j + 3]);
+                    }
+                }
+            }
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(tempty_bar(buf));
+        }
+
+        ok = named_barrier_and(1, kPromoThreads, ok);   // one decision for all promotion warps
+        if (ok) {
+            const bool n_ok = n < p.N;
+            if (p.splits == 1) {
+#pragma unroll
+                for (int j = 0; j < L::kCols; ++j) {
+                    const int m = m0 + c0 + j;
+                    if (n_ok && c0 + j < p.mma_n && m < p.M)
+                        store_one(p.C, static_cast<size_t>(m) * p.N + n, acc[j], p.out_kind);
+                }
+            } else {
+                // Deterministic split-K: publish this split's partial tile, take a
+                // ticket; the last arrival sums the splits in order 0..S-1.
+                float *ws = p.ws + static_cast<size_t>(split) * p.M * p.N;
+#pragma unroll
+                for (int j = 0; j < L::kCols; ++j) {
+                    const int m = m0 + c0 + j;
+                    if (n_ok && c0 + j < p.mma_n && m < p.M)
+                        ws[static_cast<size_t>(m) * p.N + n] = acc[j];
+                }
+                __threadfence();
+                named_barrier(1, kPromoThreads);
+                const int tile = blockIdx.z * gridDim.x + blockIdx.x;
+                if (tid == 0) {
+                    const unsigned prev = atomicAdd(p.counters + tile, 1u);
+                    *last_flag = (prev == static_cast<unsigned>(p.splits - 1)) ? 1 : 0;
+                }
+                named_barrier(1, kPromoThreads);
+                if (*last_flag) {
+                    __threadfence();
+#pragma unroll 4
+                    for (int j = 0; j < L::kCols; ++j) {
+                        const int m = m0 + c0 + j;
+                        if (n_ok && c0 + j < p.mma_n && m < p.M) {
+                            const size_t off = static_cast<size_t>(m) * p.N + n;
+                            float sum = 0.f;
+                            for (int s = 0; s < p.splits; ++s)
+                                sum += __ldcg(p.ws + static_cast<size_t>(s) * p.M * p.N + off);
+                            store_one(p.C, off, sum, p.out_kind);
+                        }
+                    }
+                    if (tid == 0)
+                        p.counters[tile] = 0u;   // ready for the next call
+                }
+            }
+        }
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem_base, L::kTmemCols);
+    }
+}
+
+template <int MT>
+cudaError_t launch_swapab_t(const CUtensorMap &tmW, const CUtensorMap &tmX, const SwapParams &p,
+                            const LaunchCfg &cfg)
+{
+    using L = SwapLayout<MT>;
+    auto kernel = k_swapab<MT>;
+    const size_t smem = L::smem(cfg.stages, p.groups_per_split);
+    static volatile int smem_set[kMaxDeviceFlags] = {};
+    cudaError_t e = ensure_smem_limit(kernel, smem_set);
+    if (e != cudaSuccess)
+        return e;
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = dim3((p.N + 127) / 128, p.splits, p.num_m_tiles);
+    lc.blockDim = dim3(L::kThreads, 1, 1);
+    lc.dynamicSmemBytes = smem;
+    lc.stream = cfg.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    lc.attrs = attr;
+    lc.numAttrs = cfg.pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&lc, kernel, tmW, tmX, p, cfg.stages);
+}
+
+}  // namespace
+
+size_t swapab_smem_bytes(int mt, int stages, int gps)
+{
+    if (stages < 1 || stages > kMaxStages)
+        return 0;
+    switch (mt) {
+    case 32: return SwapLayout<32>::smem(stages, gps);
+    case 64: return SwapLayout<64>::smem(stages, gps);
+    case 128: return SwapLayout<128>::smem(stages, gps);
+    case 256: return SwapLayout<256>::smem(stages, gps);
+    default: return 0;
+    }
+}
+
+cudaError_t launch_swapab(const CUtensorMap &tmW, const CUtensorMap &tmX, const SwapParams &p,
+                          int mt, const LaunchCfg &cfg)
+{
+    if (cfg.stages < 1 || cfg.stages > kMaxStages)
+        return cudaErrorInvalidValue;
+    switch (mt) {
+    case 32: return launch_swapab_t<32>(tmW, tmX, p, cfg);
+    case 64: return launch_swapab_t<64>(tmW, tmX, p, cfg);
+    case 128: return launch_swapab_t<128>(tmW, tmX, p, cfg);
+    case 256: return launch_swapab_t<256>(tmW, tmX, p, cfg);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace w8a8

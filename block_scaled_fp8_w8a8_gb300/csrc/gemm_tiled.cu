@@ -1,0 +1,344 @@
+// Tiled W8A8 block-FP8 matmul for large M on sm_103a (tokens on the MMA M side).
+//
+// Operation ("feat: optimize w8a8 block fp8 matmul for Hopper", FlagGems-vllm
+// PR #693, Description; Numerical safety: FP32 accumulation, one cast):
+//   C[m,n] = cast( sum_g a_s[m,g] * b_s[n/128,g] * sum_{k in g} A[m,k] B[n,k] )
+//
+// One persistent CTA per SM walks 128 x BN output tiles (grouped raster so
+// that concurrently running tiles share A and B panels in L2).  Per CTA:
+//   warp 0      TMA producer: one 128-wide K group of A (128 x 128 B) and of
+//               B (BN x 128 B) per shared-memory stage, 128-byte swizzled.
+//   warp 1      MMA issuer: 4 x tcgen05.mma kind::f8f6f4 (K = 32 each) turn
+//               one stage into the group's fp32 partial P_g in a TMEM buffer;
+//               commits free the stage and publish the buffer.
+//   warps 4..   BN/128 promotion warpgroups: each thread owns one row and 128
+//               columns; per group it reads P_g from TMEM (tcgen05.ld), applies
+//               the scale a_s[m,g] * b_s[n/128,g] with an fp32 FMA into its
+//               register accumulator, and releases the buffer.  After the last
+//               group it casts and stores its row segment.
+// TMEM holds 512 / BN partial buffers of BN columns (all 512 columns), so the
+// MMA can run up to that many groups ahead of the promotion, including across
+// the epilogue of the previous tile.
+//
+// The block-wise scales are arbitrary fp32 values (amax / 448), which the
+// hardware's block-scaled MMA kinds (power-of-two scale factors per 32 K
+// elements) cannot represent; hence the per-group software promotion.
+#include "kernels.cuh"
+#include "ptx.cuh"
+
+namespace w8a8 {
+
+namespace {
+
+constexpr int kGroupRaster = 16;   // M tiles per raster group
+
+__device__ __forceinline__ void tile_coords(int t, int num_m, int num_n, int &mb, int &nb)
+{
+    const int per_group = kGroupRaster * num_n;
+    const int gid = t / per_group;
+    const int first_m = gid * kGroupRaster;
+    const int gm = min(num_m - first_m, kGroupRaster);
+    const int r = t - gid * per_group;
+    mb = first_m + r % gm;
+    nb = r / gm;
+}
+
+// Store 128 consecutive fp32 accumulators of one row as out_kind, in 16-byte chunks,
+// skipping chunks at or beyond column N (N is a multiple of 16).
+__device__ __forceinline__ void store_row128(const float (&acc)[128], void *C, size_t row_off,
+                                             int col0, int N, int out_kind)
+{
+    if (out_kind == OUT_FP32) {
+        float *dst = static_cast<float *>(C) + row_off + col0;
+#pragma unroll
+        for (int c = 0; c < 32; ++c)
+            if (col0 + 4 * c < N)
+                *reinterpret_cast<float4 *>(dst + 4 * c) =
+                    make_float4(acc[4 * c], acc[4 * c + 1], acc[4 * c + 2], acc[4 * c + 3]);
+    } else {
+        uint16_t *dst = static_cast<uint16_t *>(C) + row_off + col0;
+        const bool bf = out_kind == OUT_BF16;
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+            if (col0 + 8 * c < N) {
+                uint4 v;
+                const float *a = &acc[8 * c];
+                v.x = bf ? pack_bf16x2(a[0], a[1]) : pack_f16x2(a[0], a[1]);
+                v.y = bf ? pack_bf16x2(a[2], a[3]) : pack_f16x2(a[2], a[3]);
+                v.z = bf ? pack_bf16x2(a[4], a[5]) : pack_f16x2(a[4], a[5]);
+                v.w = bf ? pack_bf16x2(a[6], a[7]) : pack_f16x2(a[6], a[7]);
+                *reinterpret_cast<uint4 *>(dst + 8 * c) = v;
+            }
+        }
+    }
+}
+
+template <int BN, int STAGES> struct TiledLayout {
+    static constexpr int kPromoWG = BN / 128;
+    static constexpr int kThreads = 128 + 128 * kPromoWG;
+    static constexpr uint32_t kABytes = 128u * 128u;
+    static constexpr uint32_t kBBytes = static_cast<uint32_t>(BN) * 128u;
+    static constexpr int kBufs = 512 / BN;                  // TMEM partial buffers
+    static constexpr uint32_t kTmemCols = 512;
+    static constexpr int kBars = 2 * STAGES + 2 * kBufs + 1;
+    static constexpr size_t kSmem = 1024 + STAGES * (kABytes + kBBytes) + kBars * 8 + 16;
+};
+
+template <int BN, int STAGES>
+__global__ void __launch_bounds__(TiledLayout<BN, STAGES>::kThreads, 1)
+    k_tiled(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+            const TiledParams p)
+{
+    using L = TiledLayout<BN, STAGES>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const uint32_t sA = smem_addr(smem);
+    const uint32_t sB = sA + STAGES * L::kABytes;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + STAGES * (L::kABytes + L::kBBytes));
+    const uint32_t bar0 = smem_addr(bars);
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+    auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
+    auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + L::kBufs + b); };
+    const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 2 * L::kBufs);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + L::kBars);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const uint32_t warp = warp_index(), lane = lane_index();
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int b = 0; b < L::kBufs; ++b) {
+            mbar_init(tfull_bar(b), 1);
+            mbar_init(tempty_bar(b), 4 * L::kPromoWG);
+        }
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        mbar_fence_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_map(&tmA);
+        tma_prefetch_map(&tmB);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_addr(tmem_slot), L::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem_base = *tmem_slot;
+    const WaitGuard guard{abort_flag, p.status, p.wait_limit};
+
+    grid_launch_dependents();
+    grid_dependency_wait();
+
+    if (warp < 4) {
+        if constexpr (L::kPromoWG == 2)
+            regs_dealloc<40>();
+        if (warp == 0 && lane == 0) {
+            // ---------------------------------------------------------- TMA producer
+            int stage = 0;
+            uint32_t phase = 0;
+            long long issued = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+                int mb, nb;
+                tile_coords(t, p.num_m_tiles, p.num_n_tiles, mb, nb);
+                for (int g = 0; g < p.G; ++g) {
+                    if (!wait_bounded(empty_bar(stage), phase ^ 1u, guard, SITE_TILED_PRODUCER)) {
+                        ok = false;
+                        break;
+                    }
+                    if (issued != p.debug_skip_tma) {
+                        mbar_arrive_expect_tx(full_bar(stage), L::kABytes + L::kBBytes);
+                        tma_load_2d(sA + stage * L::kABytes, &tmA, full_bar(stage), g * 128, mb * 128);
+                        tma_load_2d(sB + stage * L::kBBytes, &tmB, full_bar(stage), g * 128, nb * BN);
+                    }
+                    ++issued;
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (ok) {
+                // Tail: wait until the MMA has released every stage, so that no
+                // commit arrives on this CTA's shared memory after it exits.
+                for (int s = 0; s < STAGES && ok; ++s) {
+                    ok = wait_bounded(empty_bar(stage), phase ^ 1u, guard, SITE_TILED_PRODUCER);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            } else {
+                // Drain: wait for the loads still landing in this CTA's shared memory.
+                for (int s = 0; s < STAGES; ++s) {
+                    const bool this_round = s < stage;
+                    if (!this_round && issued < STAGES && s >= issued)
+                        continue;
+                    wait_drain(full_bar(s), this_round ? phase : (phase ^ 1u), p.status, p.wait_limit,
+                               (SITE_DRAIN << 8) | 4u);
+                }
+            }
+        } else if (warp == 1 && lane == 0) {
+            // ---------------------------------------------------------- MMA issuer
+            constexpr uint32_t idesc = idesc_e4m3_f32(128, BN);
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t it = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+                for (int g = 0; g < p.G; ++g) {
+                    const uint32_t buf = it % L::kBufs;
+                    const uint32_t bphase = (it / L::kBufs) & 1u;
+                    if (!wait_bounded(tempty_bar(buf), bphase ^ 1u, guard, SITE_TILED_MMA_TMEM) ||
+                        !wait_bounded(full_bar(stage), phase, guard, SITE_TILED_MMA_FULL)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    const uint32_t d = tmem_base + buf * BN;
+                    const uint64_t ad = sw128_kmajor_desc(sA + stage * L::kABytes);
+                    const uint64_t bd = sw128_kmajor_desc(sB + stage * L::kBBytes);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_e4m3(d, ad + 2u * kk, bd + 2u * kk, idesc, kk > 0 ? 1u : 0u);
+                    mma_commit(empty_bar(stage));
+                    mma_commit(tfull_bar(buf));
+                    ++it;
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                mma_commit(drain_bar);
+                wait_drain(drain_bar, 0, p.status, p.wait_limit, (SITE_DRAIN << 8) | 4u);
+            }
+        }
+        __syncwarp();
+    } else {
+        // -------------------------------------------------------------- promotion + epilogue
+        if constexpr (L::kPromoWG == 2)
+            regs_alloc<232>();
+        const int h = static_cast<int>(warp / 4) - 1;      // promotion warpgroup: column half
+        const uint32_t q = warp & 3u;                      // TMEM lane quarter of this warp
+        const int row = static_cast<int>(q * 32 + lane);
+        uint32_t it = 0;
+        for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
+            int mb, nb;
+            tile_coords(t, p.num_m_tiles, p.num_n_tiles, mb, nb);
+            const int m = mb * 128 + row;
+            const int col0 = nb * BN + h * 128;
+            const bool m_ok = m < p.M;
+            const bool n_ok = col0 < p.N;
+            const float *as_row = p.a_s + static_cast<size_t>(m_ok ? m : 0) * p.G;
+            const float *bs_row = p.b_s + static_cast<size_t>(n_ok ? col0 / 128 : 0) * p.G;
+            float acc[128];
+#pragma unroll
+            for (int j = 0; j < 128; ++j)
+                acc[j] = 0.f;
+            float sa = m_ok ? __ldg(as_row) : 0.f;
+            float sb = __ldg(bs_row);
+            bool ok = true;
+            for (int g = 0; g < p.G; ++g) {
+                const float s = sa * sb;
+                if (g + 1 < p.G) {
+                    sa = m_ok ? __ldg(as_row + g + 1) : 0.f;
+                    sb = __ldg(bs_row + g + 1);
+                }
+                const uint32_t buf = it % L::kBufs;
+                const uint32_t bphase = (it / L::kBufs) & 1u;
+                // All lanes wait; the warp proceeds only if every lane saw the
+                // buffer (tcgen05.ld below is a warp-wide instruction).
+                ok = __all_sync(0xffffffffu,
+                                wait_bounded(tfull_bar(buf), bphase, guard, SITE_TILED_PROMOTE));
+                if (!ok)
+                    break;
+                tc_fence_after_sync();
+                const uint32_t taddr = tmem_base + ((q * 32u) << 16) + buf * BN + h * 128;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    float v[32];
+                    tmem_load_32cols(taddr + 32u * c, v);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        acc[32 * c + j] = fmaf(s, v[j], acc[32 * c + j]);
+                }
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(tempty_bar(buf));
+                ++it;
+            }
+            if (!ok)
+                break;
+            if (m_ok && n_ok)
+                store_row128(acc, p.C, static_cast<size_t>(m) * p.N, col0, p.N, p.out_kind);
+        }
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem_base, L::kTmemCols);
+    }
+}
+
+template <int BN, int STAGES>
+cudaError_t launch_tiled_t(const CUtensorMap &tmA, const CUtensorMap &tmB, const TiledParams &p,
+                           const LaunchCfg &cfg)
+{
+    using L = TiledLayout<BN, STAGES>;
+    auto kernel = k_tiled<BN, STAGES>;
+    static volatile int smem_set[kMaxDeviceFlags] = {};
+    cudaError_t e = ensure_smem_limit(kernel, smem_set);
+    if (e != cudaSuccess)
+        return e;
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = dim3(cfg.grid, 1, 1);
+    lc.blockDim = dim3(L::kThreads, 1, 1);
+    lc.dynamicSmemBytes = L::kSmem;
+    lc.stream = cfg.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    lc.attrs = attr;
+    lc.numAttrs = cfg.pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&lc, kernel, tmA, tmB, p);
+}
+
+}  // namespace
+
+size_t tiled_smem_bytes(int bn, int stages)
+{
+    if (bn == 256 && stages == 4)
+        return TiledLayout<256, 4>::kSmem;
+    if (bn == 128 && stages == 6)
+        return TiledLayout<128, 6>::kSmem;
+    if (bn == 128 && stages == 4)
+        return TiledLayout<128, 4>::kSmem;
+    return 0;
+}
+
+cudaError_t launch_tiled(const CUtensorMap &tmA, const CUtensorMap &tmB, const TiledParams &p,
+                         int bn, const LaunchCfg &cfg)
+{
+    if (bn == 256 && cfg.stages == 4)
+        return launch_tiled_t<256, 4>(tmA, tmB, p, cfg);
+    if (bn == 128 && cfg.stages == 6)
+        return launch_tiled_t<128, 6>(tmA, tmB, p, cfg);
+    if (bn == 128 && cfg.stages == 4)
+        return launch_tiled_t<128, 4>(tmA, tmB, p, cfg);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace w8a8

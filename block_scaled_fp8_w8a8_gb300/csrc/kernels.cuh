@@ -1,0 +1,103 @@
+// Parameter blocks and host-side launchers of the sm_103a kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace w8a8 {
+
+enum OutKind : int { OUT_BF16 = 0, OUT_FP16 = 1, OUT_FP32 = 2 };
+
+// Wait sites recorded in the device status word (bits 8..15) when a bounded wait runs out.
+enum WaitSite : uint32_t {
+    SITE_TILED_PRODUCER = 1,
+    SITE_TILED_MMA_TMEM = 2,
+    SITE_TILED_MMA_FULL = 3,
+    SITE_TILED_PROMOTE = 4,
+    SITE_SWAP_PRODUCER = 5,
+    SITE_SWAP_MMA_TMEM = 6,
+    SITE_SWAP_MMA_FULL = 7,
+    SITE_SWAP_PROMOTE = 8,
+    SITE_DRAIN = 9,
+};
+
+// Tokens on the MMA M side: one CTA per SM walks 128 x BN output tiles.
+struct TiledParams {
+    const float *a_s;      // [M, G]
+    const float *b_s;      // [NB, G]
+    void *C;               // [M, N]
+    int M, N, K, G, NB;
+    int num_m_tiles, num_n_tiles, num_tiles;
+    int out_kind;
+    int debug_skip_tma;    // test hook: >= 0 makes the producer skip that many-th load (no TMA issued)
+    unsigned *status;
+    unsigned long long wait_limit;
+};
+
+// Swap-AB: weights on the MMA M side (128 rows of B = one b_s row block),
+// `mma_n` tokens on the MMA N side; optional split of the K groups over
+// gridDim.y CTAs with an ordered reduction by the last CTA of each tile.
+struct SwapParams {
+    const float *a_s;      // [M, G]
+    const float *b_s;      // [NB, G]
+    void *C;               // [M, N]
+    float *ws;             // [splits, M, N] fp32 partials (splits > 1)
+    unsigned *counters;    // [num_m_tiles * NB] arrival counters (splits > 1), zero between calls
+    int M, N, K, G, NB;
+    int mma_n;             // tokens per tile, multiple of 16, <= the kernel's MT
+    int num_m_tiles;
+    int splits;
+    int groups_per_split;
+    int out_kind;
+    int debug_skip_tma;
+    unsigned *status;
+    unsigned long long wait_limit;
+};
+
+struct LaunchCfg {
+    int stages;
+    int grid;        // persistent kernels: number of CTAs
+    int pdl;
+    cudaStream_t stream;
+};
+
+// Shared memory bytes each kernel configuration needs (0 = unsupported configuration).
+size_t tiled_smem_bytes(int bn, int stages);
+size_t swapab_smem_bytes(int mt, int stages, int groups_per_split);
+
+cudaError_t launch_tiled(const CUtensorMap &tmA, const CUtensorMap &tmB, const TiledParams &p,
+                         int bn, const LaunchCfg &cfg);
+cudaError_t launch_swapab(const CUtensorMap &tmW, const CUtensorMap &tmX, const SwapParams &p,
+                          int mt, const LaunchCfg &cfg);
+
+// Raise `kernel`'s dynamic shared-memory limit to the device maximum, once per
+// device per kernel: `flags` is a per-kernel array of kMaxDeviceFlags words.
+// Doing it once keeps the call out of stream captures that follow the first
+// (eager) launch.
+constexpr int kMaxDeviceFlags = 64;
+template <typename Kernel>
+cudaError_t ensure_smem_limit(Kernel kernel, volatile int *flags)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    if (dev < 0 || dev >= kMaxDeviceFlags)
+        return cudaErrorInvalidDevice;
+    if (flags[dev])
+        return cudaSuccess;
+    int optin = 0;
+    e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (e != cudaSuccess)
+        return e;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+    if (e == cudaSuccess)
+        flags[dev] = 1;
+    return e;
+}
+
+// Device address of the per-device status word (for the current device).
+cudaError_t status_word_address(unsigned **out);
+
+}  // namespace w8a8

@@ -1,0 +1,191 @@
+/*
+ * w8a8_block_fp8.h -- C ABI of the GB300 (sm_103a) W8A8 block-FP8 matmul.
+ *
+ * The operation ("feat: optimize w8a8 block fp8 matmul for Hopper",
+ * FlagGems-vllm PR #693, Description and Numerical safety sections):
+ *
+ *   C[m,n] = cast_out( sum_g a_s[m,g] * b_s[n/128, g] * sum_{k in group g} A[m,k] * B[n,k] )
+ *
+ *   A    FP8 E4M3 (OCP "FN" encoding) activations, [M, K] row-major (row stride K bytes)
+ *   a_s  fp32 de-quantisation scales, one per token per 128-wide K group,
+ *        [M, K/128] row-major
+ *   B    FP8 E4M3 weights, [N, K] row-major (row stride K bytes): C = A * B^T
+ *   b_s  fp32 de-quantisation scales, one per [128, 128] weight block,
+ *        [ceil(N/128), K/128] row-major
+ *   C    [M, N] row-major in bf16, fp16 or fp32 (round to nearest even)
+ *
+ * The group products are accumulated in fp32 on the tensor cores, promoted
+ * into an fp32 accumulator with the product of the two scales, and the sum is
+ * cast once at the end, as the page's Numerical safety section states for every
+ * path of the operator.
+ *
+ * Conventions for every call below:
+ *  - Pointers named *_dev are DEVICE pointers owned by the caller.  The
+ *    library keeps no reference to them after the call returns.  Calls are
+ *    asynchronous on `stream` (a cudaStream_t; NULL is the legacy default
+ *    stream): the caller keeps the buffers alive until the stream has passed
+ *    the call.  C is fully overwritten; it need not be initialised.
+ *  - Supported problems (anything else returns W8A8_ERR_UNSUPPORTED before any
+ *    CUDA call; the shape guards of the page's Numerical safety section):
+ *    block_n == block_k == 128, K % 128 == 0, N % 16 == 0, M >= 0, N >= 1,
+ *    K >= 128, A/B/C 16-byte aligned, a_s/b_s 4-byte aligned, dense
+ *    row-major tensors.  M == 0 returns W8A8_OK and launches nothing.
+ *  - Errors are returned synchronously as w8a8_status; a human-readable detail
+ *    string for the calling thread's last error is available from
+ *    w8a8_last_error().  A device-side wait that gives up (a bounded wait that
+ *    ran out) is recorded in a per-device status word read by
+ *    w8a8_get_device_status(); kernels never trap.
+ *  - Thread safety: calls may be made from several host threads.  Concurrent
+ *    calls that use the split-K variant on different streams must each pass
+ *    their own workspace (see w8a8_options).
+ */
+#ifndef W8A8_BLOCK_FP8_H
+#define W8A8_BLOCK_FP8_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define W8A8_ABI_VERSION 1
+
+/* Same type as cudaStream_t; declared here so that the header needs no CUDA include. */
+typedef struct CUstream_st *w8a8_stream_t;
+
+typedef enum {
+    W8A8_OK = 0,
+    W8A8_ERR_INVALID_ARG = 1,     /* null pointer, negative size, bad enum          */
+    W8A8_ERR_UNSUPPORTED = 2,     /* outside the supported problem set (see above)  */
+    W8A8_ERR_CUDA = 3,            /* a CUDA runtime/driver call failed               */
+    W8A8_ERR_DEVICE_TIMEOUT = 4,  /* a bounded device-side wait ran out              */
+    W8A8_ERR_WORKSPACE = 5,       /* caller workspace too small / misaligned         */
+    W8A8_ERR_NO_DEVICE = 6        /* no usable sm_100-family device is current       */
+} w8a8_status;
+
+typedef enum { W8A8_OUT_BF16 = 0, W8A8_OUT_FP16 = 1, W8A8_OUT_FP32 = 2 } w8a8_out_dtype;
+
+/* Kernel variants.  AUTO lets the (M, N, K) dispatcher choose. */
+typedef enum {
+    W8A8_VARIANT_AUTO = 0,
+    W8A8_VARIANT_TILED = 1,   /* tokens on the MMA M side: 128 x BN tiles, for large M       */
+    W8A8_VARIANT_SWAPAB = 2,  /* C^T = B A^T: 128 weight rows per MMA, tokens on MMA N       */
+    W8A8_VARIANT_SPLITK = 3   /* swap-AB with the K groups split over CTAs + ordered reduce */
+} w8a8_variant;
+
+/*
+ * Optional controls for w8a8_block_fp8_matmul_ex.  Zero-initialise and set
+ * what you need; every zero field means "library default".
+ *   variant            force a kernel variant (w8a8_variant); AUTO = dispatcher
+ *   split_k            number of K splits for W8A8_VARIANT_SPLITK (0 = choose)
+ *   block_n_tile       TILED only: 128 or 256 output columns per tile (0 = choose)
+ *   m_tile             SWAPAB/SPLITK only: tokens per tile, multiple of 16, <= 256 (0 = choose)
+ *   stages             shared-memory pipeline depth 1..8 (0 = choose)
+ *   grid_limit         TILED only: cap on the number of persistent CTAs (0 = one per SM)
+ *   pdl                1 = launch with programmatic dependent launch, so that the
+ *                      kernel's prologue overlaps the previous kernel on the stream
+ *   debug_skip_load    test hook: n > 0 makes the producer of every CTA skip its
+ *                      n-th operand load, so that a bounded device wait runs out
+ *                      and the call surfaces W8A8_ERR_DEVICE_TIMEOUT through
+ *                      w8a8_get_device_status(); C is then undefined.  0 = off.
+ *   workspace_dev      SPLITK only: caller-owned device scratch of workspace_bytes
+ *                      bytes, 256-byte aligned, at least
+ *                      w8a8_block_fp8_workspace_size() bytes, all zero before its
+ *                      first use (every call leaves its counter words zero again).
+ *                      NULL = a per-device, per-stream workspace the library
+ *                      allocates on first use (not during stream capture).
+ *   wait_limit_cycles  bound of every device-side wait in SM clock cycles
+ *                      (0 = 2^32 cycles, about 2 s)
+ */
+typedef struct {
+    int variant;
+    int split_k;
+    int block_n_tile;
+    int m_tile;
+    int stages;
+    int grid_limit;
+    int pdl;
+    int debug_skip_load;
+    void *workspace_dev;
+    size_t workspace_bytes;
+    unsigned long long wait_limit_cycles;
+    unsigned long long reserved[4];
+} w8a8_options;
+
+/*
+ * C = A * B^T with block de-quantisation, as defined at the top of this file.
+ * block_n and block_k give the scale granularity and must both be 128.
+ * All pointers are device pointers; asynchronous on `stream`.
+ */
+w8a8_status w8a8_block_fp8_matmul(const void *A_dev, const float *a_s_dev,
+                                  const void *B_dev, const float *b_s_dev, void *C_dev,
+                                  int64_t M, int64_t N, int64_t K, int block_n, int block_k,
+                                  w8a8_out_dtype out_dtype, w8a8_stream_t stream);
+
+/* As w8a8_block_fp8_matmul, with explicit options (opts may be NULL). */
+w8a8_status w8a8_block_fp8_matmul_ex(const void *A_dev, const float *a_s_dev,
+                                     const void *B_dev, const float *b_s_dev, void *C_dev,
+                                     int64_t M, int64_t N, int64_t K, int block_n, int block_k,
+                                     w8a8_out_dtype out_dtype, w8a8_stream_t stream,
+                                     const w8a8_options *opts);
+
+/*
+ * End-to-end call on HOST buffers: copies A, a_s, B and b_s from host memory
+ * (pinned memory gives asynchronous copies) into `staging_dev`, runs the
+ * matmul, and copies C back into host memory, all in order on `stream`.  The
+ * call returns once the work is enqueued; synchronise `stream` before reading
+ * C_host.  staging_dev is caller-owned device memory of at least
+ * w8a8_block_fp8_host_staging_size(M, N, K, out_dtype) bytes, 256-byte aligned.
+ */
+w8a8_status w8a8_block_fp8_matmul_host(const void *A_host, const float *a_s_host,
+                                       const void *B_host, const float *b_s_host, void *C_host,
+                                       int64_t M, int64_t N, int64_t K, int block_n, int block_k,
+                                       w8a8_out_dtype out_dtype, void *staging_dev,
+                                       size_t staging_bytes, w8a8_stream_t stream,
+                                       const w8a8_options *opts);
+
+/* Bytes of device staging that w8a8_block_fp8_matmul_host needs (0 for bad sizes). */
+size_t w8a8_block_fp8_host_staging_size(int64_t M, int64_t N, int64_t K, w8a8_out_dtype out_dtype);
+
+/*
+ * Bytes of split-K workspace a call with these options needs (0 when the
+ * variant the call would run needs none).  The workspace holds the fp32
+ * partial sums [split_k, M, N] followed by one 32-bit arrival counter per
+ * output tile; the counters must be zero before first use and are left zero.
+ */
+size_t w8a8_block_fp8_workspace_size(int64_t M, int64_t N, int64_t K, const w8a8_options *opts);
+
+/*
+ * Which variant (and its parameters) the dispatcher picks for a problem;
+ * writes into *plan_out (zero-initialised first).  No CUDA call is made
+ * except a cached query of the current device's SM count.
+ */
+w8a8_status w8a8_block_fp8_plan(int64_t M, int64_t N, int64_t K, w8a8_out_dtype out_dtype,
+                                const w8a8_options *opts, w8a8_options *plan_out);
+
+/*
+ * Synchronises the current device, then reads and clears its device status
+ * word.  W8A8_OK when no device-side wait has run out since the last read;
+ * otherwise W8A8_ERR_DEVICE_TIMEOUT, with *detail_out (if not NULL) set to the
+ * raw status word (low byte: status; next byte: the wait site).
+ */
+w8a8_status w8a8_get_device_status(unsigned *detail_out);
+
+/* Static description of a status code (never NULL). */
+const char *w8a8_status_string(w8a8_status status);
+
+/* Detail string of the calling thread's last error ("" if none). */
+const char *w8a8_last_error(void);
+
+/* W8A8_ABI_VERSION of the loaded library. */
+int w8a8_abi_version(void);
+
+/* Releases cached workspaces of every device this thread's calls touched. */
+void w8a8_shutdown(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* W8A8_BLOCK_FP8_H */

@@ -1,0 +1,181 @@
+"""GPU parity: the sm_103a kernels through the C ABI against the CPU oracle.
+
+Operator: "feat: optimize w8a8 block fp8 matmul for Hopper" (FlagGems-vllm
+PR #693), Description and Numerical safety.  Every case compares element by
+element with the bound in helpers.py; full-size workloads compare sampled
+rows that cover every 128-row tile and the ragged tail.
+"""
+import numpy as np
+import pytest
+import torch
+
+import block_scaled_fp8_w8a8_gb300 as w8
+import oracle
+from block_scaled_fp8_w8a8_gb300 import synth
+from helpers import OUT_TORCH, assert_close, reference_rows, rms_estimate, sample_rows, to_device
+
+pytestmark = pytest.mark.gpu
+
+VARIANTS = {
+    "tiled256": dict(variant=w8.W8A8_VARIANT_TILED, block_n_tile=256),
+    "tiled128": dict(variant=w8.W8A8_VARIANT_TILED, block_n_tile=128),
+    "swapab": dict(variant=w8.W8A8_VARIANT_SWAPAB),
+    "splitk": dict(variant=w8.W8A8_VARIANT_SPLITK),
+    "auto": dict(),
+}
+
+
+def run(x, out="bf16", **opts):
+    A, a_s, B, b_s = to_device(x)
+    C = w8.matmul(A, a_s, B, b_s, out_dtype=out, **opts)
+    torch.cuda.synchronize()
+    st, word = w8.w8a8_get_device_status()
+    assert st == w8.W8A8_OK, f"device status {word:#x}"
+    return C
+
+
+# ------------------------------------------------------------------ PR #693's reference shape
+
+@pytest.mark.parametrize("variant", list(VARIANTS))
+@pytest.mark.parametrize("out", ["bf16", "fp16", "fp32"])
+def test_pr1_shape_all_variants(variant, out):
+    """64 x 512 x 256, seed 0: every variant and every output dtype."""
+    x = synth.make_inputs(64, 512, 256, seed=0)
+    ref = oracle.reference_c(x.A, x.a_s, x.B, x.b_s)
+    C = run(x, out, **VARIANTS[variant])
+    assert C.dtype == OUT_TORCH[out]
+    assert_close(C, ref, what=f"{variant}/{out}")
+
+
+# ------------------------------------------------------------------ edge shapes
+
+EDGE = [(1, 128, 128), (2, 16, 128), (7, 144, 384), (16, 400, 256), (127, 256, 512),
+        (129, 272, 256), (255, 128, 640), (257, 384, 256), (300, 160, 384), (33, 1024, 1152)]
+
+
+@pytest.mark.parametrize("M,N,K", EDGE)
+@pytest.mark.parametrize("variant", ["tiled256", "tiled128", "swapab", "splitk"])
+def test_edge_shapes(M, N, K, variant):
+    """Ragged M and N tails, single-group K, N not a multiple of 128 or 256."""
+    x = synth.make_inputs(M, N, K, seed=M + N + K)
+    ref = oracle.reference_c(x.A, x.a_s, x.B, x.b_s)
+    C = run(x, "fp32", **VARIANTS[variant])
+    assert_close(C, ref, what=f"{variant} {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("m_tile", [16, 32, 48, 64, 96, 128, 160, 208, 256])
+def test_swapab_token_tiles(m_tile):
+    """Every token-tile size (MMA N) of the swap-AB kernel, with several tiles per M."""
+    x = synth.make_inputs(300, 256, 384, seed=m_tile)
+    ref = oracle.reference_c(x.A, x.a_s, x.B, x.b_s)
+    for variant in ("swapab", "splitk"):
+        C = run(x, "fp32", m_tile=m_tile, **VARIANTS[variant])
+        assert_close(C, ref, what=f"{variant} m_tile={m_tile}")
+
+
+@pytest.mark.parametrize("splits", [1, 2, 3, 5, 8, 32])
+def test_splitk_counts(splits):
+    x = synth.make_inputs(70, 512, 4096, seed=splits, outlier_p=1e-3)
+    ref = oracle.reference_c(x.A, x.a_s, x.B, x.b_s)
+    C = run(x, "bf16", variant=w8.W8A8_VARIANT_SPLITK, split_k=splits)
+    assert_close(C, ref, what=f"splits={splits}")
+
+
+def test_splitk_deterministic():
+    """The split-K reduction sums partials in split order: identical bits every run."""
+    x = synth.make_inputs(158, 512, 4096, seed=0, outlier_p=1e-3)
+    A, a_s, B, b_s = to_device(x)
+    outs = []
+    for _ in range(10):
+        outs.append(w8.matmul(A, a_s, B, b_s, out_dtype="fp32",
+                              variant=w8.W8A8_VARIANT_SPLITK, split_k=16))
+    torch.cuda.synchronize()
+    for o in outs[1:]:
+        assert torch.equal(o.view(torch.int32), outs[0].view(torch.int32))
+
+
+def test_zero_and_extreme_inputs():
+    """All-zero codes give exact zeros; max-magnitude codes stay finite in fp32."""
+    M, N, K = 130, 256, 256
+    x = synth.make_inputs(M, N, K, seed=3)
+    x.A.zero_()
+    for variant in ("tiled256", "swapab"):
+        C = run(x, "fp32", **VARIANTS[variant])
+        assert torch.count_nonzero(C) == 0
+    y = synth.make_inputs(M, N, K, seed=4)
+    y.A.fill_(0x7E)
+    y.B.fill_(0xFE)
+    ref = oracle.reference_c(y.A, y.a_s, y.B, y.b_s)
+    for variant in ("tiled256", "swapab"):
+        assert_close(run(y, "fp32", **VARIANTS[variant]), ref, what=f"extreme {variant}")
+
+
+def test_unit_scale_cast_is_round_to_nearest_even():
+    """Unit scales, one K group and codes of +-{0.5, 1, 2, 4}: every product is a
+    power of two and every partial sum a multiple of 1/4 below 2^11, so the fp32
+    accumulation is exact whatever the order or the tensor core's internal
+    alignment width.  The bf16 and fp16 outputs (which do round here, ties
+    included) must then equal the oracle's single rounding of the exact result."""
+    M, N, K = 96, 256, 128
+    g = torch.Generator().manual_seed(9)
+    codes = torch.tensor([0x30, 0x38, 0x40, 0x48, 0xB0, 0xB8, 0xC0, 0xC8], dtype=torch.uint8)
+    A = codes[torch.randint(0, 8, (M, K), generator=g)]
+    B = codes[torch.randint(0, 8, (N, K), generator=g)]
+    x = synth.W8A8Inputs(A, torch.ones(M, 1), B, torch.ones(2, 1))
+    ref = oracle.reference_c(x.A, x.a_s, x.B, x.b_s)
+    assert np.abs(ref).max() < 2 ** 11
+    for out in ("bf16", "fp16"):
+        want = oracle.cast_out(ref, out)
+        for variant in ("tiled128", "tiled256", "swapab"):
+            C = run(x, out, **VARIANTS[variant]).cpu()
+            assert torch.equal(C.view(torch.int16), want.view(torch.int16)), (out, variant)
+
+
+# ------------------------------------------------------------------ the workload shapes, full size
+
+ALL_SHAPES = [(name, s) for name, w in synth.WORKLOADS.items() for s in w["shapes"]]
+
+
+@pytest.mark.parametrize("name,shape", ALL_SHAPES, ids=lambda v: str(v))
+def test_workload_shapes(name, shape):
+    """Every workload shape at full size through the dispatcher (AUTO), as the
+    benchmark launches it; sampled rows for the large prefill shapes."""
+    M, N, K = shape
+    x = synth.make_inputs(M, N, K, seed=0, outlier_p=synth.WORKLOADS[name]["outlier_p"])
+    C = run(x, "bf16")
+    rows = sample_rows(M)
+    ref = reference_rows(x, rows)
+    assert_close(C[torch.from_numpy(rows).cuda()], ref, rms=rms_estimate(ref), what=f"{shape}")
+
+
+# ------------------------------------------------------------------ host-buffer (end-to-end) call
+
+def test_host_buffer_call_matches_device_call():
+    M, N, K = 100, 4096, 256
+    x = synth.make_inputs(M, N, K, seed=0)
+    dev = run(x, "bf16")
+    pin = [t.pin_memory() for t in (x.A, x.a_s, x.B, x.b_s)]
+    C_host = torch.empty((M, N), dtype=torch.bfloat16).pin_memory()
+    nbytes = w8.w8a8_block_fp8_host_staging_size(M, N, K, w8.W8A8_OUT_BF16)
+    staging = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    st = w8.w8a8_block_fp8_matmul_host(*pin, C_host, M, N, K, staging_dev=staging,
+                                       staging_bytes=nbytes, stream=stream)
+    w8.check(st)
+    stream.synchronize()
+    assert torch.equal(C_host.view(torch.int16), dev.cpu().view(torch.int16))
+
+
+def test_invalid_calls_do_not_launch():
+    x = synth.make_inputs(8, 128, 256, seed=0)
+    A, a_s, B, b_s = to_device(x)
+    C = torch.empty((8, 128), dtype=torch.bfloat16, device="cuda")
+    assert w8.w8a8_block_fp8_matmul(A, a_s, B, b_s, C, 8, 128, 256, 64, 128) == w8.W8A8_ERR_UNSUPPORTED
+    assert w8.w8a8_block_fp8_matmul(A.data_ptr() + 1, a_s, B, b_s, C, 8, 128, 256) == w8.W8A8_ERR_UNSUPPORTED
+    assert w8.w8a8_block_fp8_matmul(A, a_s, B, b_s, C, 0, 128, 256) == w8.W8A8_OK
+    ws = torch.empty(16, dtype=torch.uint8, device="cuda")
+    o = w8.options(variant=w8.W8A8_VARIANT_SPLITK, split_k=2, workspace_dev=ws.data_ptr(),
+                   workspace_bytes=16)
+    assert w8.w8a8_block_fp8_matmul_ex(A, a_s, B, b_s, C, 8, 128, 256, opts=o) == w8.W8A8_ERR_WORKSPACE
+    torch.cuda.synchronize()
+    assert w8.w8a8_get_device_status()[0] == w8.W8A8_OK
