@@ -58,8 +58,13 @@ def parse():
     ap.add_argument("--out-dtype", default="bf16", choices=["bf16", "fp16", "fp32"])
     ap.add_argument("--min-seconds", type=float, default=1.0,
                     help="repeat the K-step block until this much time has been timed")
+    ap.add_argument("--shapes", default=None,
+                    help="override the workload's shapes, e.g. '214x4096x256,16x512x4096' "
+                         "(for profiling one kernel)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-shape", action="store_true",
+                    help="skip the per-shape launch timing (keeps an ncu launch list short)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     return ap.parse_args()
 
@@ -185,11 +190,11 @@ class ClockSampler:
 class Workload:
     """Device-resident rotating input sets and one CUDA graph per set."""
 
-    def __init__(self, name, out_dtype, l2_bytes):
+    def __init__(self, name, out_dtype, l2_bytes, shapes=None):
         import block_scaled_fp8_w8a8_gb300 as w8
         self.w8 = w8
         spec = synth.WORKLOADS[name]
-        self.shapes = spec["shapes"]
+        self.shapes = shapes or spec["shapes"]
         self.out_code = w8.out_code(out_dtype)
         self.out_bytes = 4 if out_dtype == "fp32" else 2
         tdt = {"bf16": torch.bfloat16, "fp16": torch.float16, "fp32": torch.float32}[out_dtype]
@@ -284,7 +289,10 @@ def run_ours(args, rank, world):
     hbm, bf16, peak_kind = peaks()
     dev = torch.cuda.current_device()
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    wl = Workload(args.workload, args.out_dtype, l2)
+    override = None
+    if args.shapes:
+        override = [tuple(int(v) for v in s.split("x")) for s in args.shapes.split(",")]
+    wl = Workload(args.workload, args.out_dtype, l2, override)
     wl.capture()
     shapes = wl.shapes
     flops, nbytes = workload_units(shapes, wl.out_bytes)
@@ -303,7 +311,7 @@ def run_ours(args, rank, world):
     # Per-shape launch durations: a graph of L launches of one shape (rotating sets).
     per_shape = []
     L = max(wl.sets, 64)
-    for i, (M, N, K) in enumerate(shapes):
+    for i, (M, N, K) in enumerate(shapes if not args.no_per_shape else []):
         g = wl.capture_single(i, L)
         for _ in range(2):
             g.replay()
@@ -318,8 +326,12 @@ def run_ours(args, rank, world):
                           "variant": {1: "tiled", 2: "swapab", 3: "splitk"}.get(plan.variant, "?"),
                           "split_k": plan.split_k, "m_tile": plan.m_tile,
                           "block_n_tile": plan.block_n_tile})
-    dom = max(range(len(shapes)), key=lambda i: per_shape[i]["us"])
-    d = per_shape[dom]
+    if per_shape:
+        dom = max(range(len(shapes)), key=lambda i: per_shape[i]["us"])
+        d = per_shape[dom]
+    else:   # whole step as one unit
+        d = {"M": "all", "N": "-", "K": "-", "variant": "step", "us": t_step * 1e6,
+             "gbs": round(nbytes / t_step / 1e9, 1), "tflops": round(flops / t_step / 1e12, 3)}
     if bound == "hbm":
         achieved = d["gbs"]
         peak = hbm

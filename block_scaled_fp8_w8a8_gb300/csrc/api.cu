@@ -279,14 +279,19 @@ w8a8_status make_plan(int64_t M, int64_t N, int64_t K, const w8a8_options *o,
     return W8A8_OK;
 }
 
+// Split-K workspace layout: a fixed region of kCounterWords arrival counters
+// at the start (so that it stays all-zero whatever sequence of shapes reuses
+// the workspace: every call returns its counters to zero), then the fp32
+// partials [splits, M, N].
+constexpr size_t kCounterWords = 65536;
+constexpr size_t kCounterBytes = kCounterWords * 4;
+
 size_t splitk_workspace_bytes(int64_t M, int64_t N, const Plan &pl)
 {
     if (pl.variant != W8A8_VARIANT_SPLITK || pl.splits <= 1)
         return 0;
     const size_t partial = static_cast<size_t>(pl.splits) * M * N * 4;
-    const size_t partial_aligned = (partial + 255) / 256 * 256;
-    const size_t counters = static_cast<size_t>(pl.m_tiles) * cdiv(N, 128) * 4;
-    return partial_aligned + (counters + 255) / 256 * 256;
+    return kCounterBytes + (partial + 255) / 256 * 256;
 }
 
 w8a8_status library_workspace(int dev, cudaStream_t stream, size_t bytes, void **out)
@@ -399,6 +404,9 @@ w8a8_status run(const void *A, const float *a_s, const void *B, const float *b_s
         p.counters = nullptr;
         const size_t ws_bytes = splitk_workspace_bytes(M, N, pl);
         if (ws_bytes) {
+            if (static_cast<size_t>(pl.m_tiles) * NB > kCounterWords)
+                return fail(W8A8_ERR_UNSUPPORTED, "split-K over %lld output tiles (max %zu)",
+                            static_cast<long long>(pl.m_tiles) * NB, kCounterWords);
             void *ws = o ? o->workspace_dev : nullptr;
             if (ws) {
                 if (o->workspace_bytes < ws_bytes || !aligned(ws, 256))
@@ -408,10 +416,8 @@ w8a8_status run(const void *A, const float *a_s, const void *B, const float *b_s
             } else if ((st = library_workspace(dev, stream, ws_bytes, &ws)) != W8A8_OK) {
                 return st;
             }
-            const size_t partial = static_cast<size_t>(pl.splits) * M * N * 4;
-            p.ws = static_cast<float *>(ws);
-            p.counters = reinterpret_cast<unsigned *>(static_cast<char *>(ws) +
-                                                      (partial + 255) / 256 * 256);
+            p.counters = static_cast<unsigned *>(ws);
+            p.ws = reinterpret_cast<float *>(static_cast<char *>(ws) + kCounterBytes);
         }
         p.M = static_cast<int>(M);
         p.N = static_cast<int>(N);

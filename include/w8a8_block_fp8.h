@@ -150,9 +150,12 @@ size_t w8a8_block_fp8_host_staging_size(int64_t M, int64_t N, int64_t K, w8a8_ou
 
 /*
  * Bytes of split-K workspace a call with these options needs (0 when the
- * variant the call would run needs none).  The workspace holds the fp32
- * partial sums [split_k, M, N] followed by one 32-bit arrival counter per
- * output tile; the counters must be zero before first use and are left zero.
+ * variant the call would run needs none).  Layout: a fixed block of 65536
+ * 32-bit arrival counters (256 KiB, one per output tile in use; at most 65536
+ * tiles) followed by the fp32 partial sums [split_k, M, N].  The counter block
+ * must be zero before the workspace's first use; every completed call leaves
+ * it zero again, so one workspace can serve any sequence of shapes on one
+ * stream.  After a W8A8_ERR_DEVICE_TIMEOUT, zero it again.
  */
 size_t w8a8_block_fp8_workspace_size(int64_t M, int64_t N, int64_t K, const w8a8_options *opts);
 

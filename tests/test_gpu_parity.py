@@ -179,3 +179,20 @@ def test_invalid_calls_do_not_launch():
     assert w8.w8a8_block_fp8_matmul_ex(A, a_s, B, b_s, C, 8, 128, 256, opts=o) == w8.W8A8_ERR_WORKSPACE
     torch.cuda.synchronize()
     assert w8.w8a8_get_device_status()[0] == w8.W8A8_OK
+
+
+def test_splitk_workspace_reused_across_shapes():
+    """One caller-owned workspace serves a sequence of different split-K shapes:
+    the counter block stays zero between calls."""
+    shapes = [(16, 512, 4096), (158, 512, 4096), (7, 144, 384), (64, 1024, 1024),
+              (300, 256, 2048), (16, 512, 4096)]
+    o = w8.options(variant=w8.W8A8_VARIANT_SPLITK, split_k=8)
+    nbytes = max(w8.w8a8_block_fp8_workspace_size(M, N, K, o) for (M, N, K) in shapes)
+    ws = torch.zeros(nbytes, dtype=torch.uint8, device="cuda")
+    for i, (M, N, K) in enumerate(shapes):
+        x = synth.make_inputs(M, N, K, seed=100 + i)
+        ref = oracle.reference_c(x.A, x.a_s, x.B, x.b_s)
+        C = run(x, "fp32", variant=w8.W8A8_VARIANT_SPLITK, split_k=8,
+                workspace_dev=ws.data_ptr(), workspace_bytes=nbytes)
+        assert_close(C, ref, what=f"reuse {M}x{N}x{K}")
+    assert torch.count_nonzero(ws[:65536 * 4]) == 0
