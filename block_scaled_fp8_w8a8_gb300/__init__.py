@@ -18,6 +18,7 @@ from ._binding import (  # noqa: F401
     W8A8_VARIANT_SPLITK, check, library_path, load_library, w8a8_abi_version,
     w8a8_block_fp8_host_staging_size, w8a8_block_fp8_matmul, w8a8_block_fp8_matmul_ex,
     w8a8_block_fp8_matmul_host, w8a8_block_fp8_plan, w8a8_block_fp8_workspace_size,
+    w8a8_block_fp8_matmul_splitk_noalloc, W8A8_NOALLOC_SCRATCH_BYTES,
     w8a8_get_device_status, w8a8_last_error, w8a8_options, w8a8_shutdown, w8a8_status_string,
 )
 

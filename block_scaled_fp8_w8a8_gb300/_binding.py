@@ -29,6 +29,7 @@ EXPORTED = (
     "w8a8_block_fp8_matmul",
     "w8a8_block_fp8_matmul_ex",
     "w8a8_block_fp8_matmul_host",
+    "w8a8_block_fp8_matmul_splitk_noalloc",
     "w8a8_block_fp8_host_staging_size",
     "w8a8_block_fp8_workspace_size",
     "w8a8_block_fp8_plan",
@@ -87,6 +88,9 @@ def load_library():
                                              opt_p]
     lib.w8a8_block_fp8_matmul_host.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i32, i32, i32,
                                                vp, sz, vp, opt_p]
+    lib.w8a8_block_fp8_matmul_splitk_noalloc.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i32,
+                                                         i32, i32, i32, vp]
+    lib.w8a8_block_fp8_matmul_splitk_noalloc.restype = ctypes.c_int
     lib.w8a8_block_fp8_host_staging_size.argtypes = [i64, i64, i64, i32]
     lib.w8a8_block_fp8_host_staging_size.restype = sz
     lib.w8a8_block_fp8_workspace_size.argtypes = [i64, i64, i64, opt_p]
@@ -155,6 +159,19 @@ def w8a8_block_fp8_matmul_host(A_host, a_s_host, B_host, b_s_host, C_host, M, N,
         _ptr(A_host), _ptr(a_s_host), _ptr(B_host), _ptr(b_s_host), _ptr(C_host), M, N, K,
         block_n, block_k, out_dtype, _ptr(staging_dev), staging_bytes, _stream(stream),
         _opts(opts))
+
+
+W8A8_NOALLOC_SCRATCH_BYTES = 8 << 20
+
+
+def w8a8_block_fp8_matmul_splitk_noalloc(A, a_s, B, b_s, C, M, N, K, block_n=128, block_k=128,
+                                         out_dtype=W8A8_OUT_BF16, split_k=0, stream=None) -> int:
+    """Split-K matmul whose scratch is a fixed array inside the library, for
+    callers that cannot allocate device memory; see the header for the limits
+    (W8A8_NOALLOC_SCRATCH_BYTES) and for why overlapping calls race."""
+    return load_library().w8a8_block_fp8_matmul_splitk_noalloc(
+        _ptr(A), _ptr(a_s), _ptr(B), _ptr(b_s), _ptr(C), M, N, K, block_n, block_k, out_dtype,
+        split_k, _stream(stream))
 
 
 def w8a8_block_fp8_host_staging_size(M, N, K, out_dtype=W8A8_OUT_BF16) -> int:

@@ -441,6 +441,15 @@ w8a8_status run(const void *A, const float *a_s, const void *B, const float *b_s
 
 }  // namespace
 
+namespace w8a8 {
+// Lets other translation units of the library report an error through
+// w8a8_last_error(); returns `st`.
+w8a8_status record_error(w8a8_status st, const char *message)
+{
+    return fail(st, "%s", message);
+}
+}  // namespace w8a8
+
 extern "C" {
 
 w8a8_status w8a8_block_fp8_matmul(const void *A_dev, const float *a_s_dev, const void *B_dev,

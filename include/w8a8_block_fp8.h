@@ -145,6 +145,43 @@ w8a8_status w8a8_block_fp8_matmul_host(const void *A_host, const float *a_s_host
                                        size_t staging_bytes, w8a8_stream_t stream,
                                        const w8a8_options *opts);
 
+/*
+ * Split-K matmul that allocates nothing (no counterpart in the paper: this is
+ * an addition of this library for callers that cannot allocate).
+ *
+ * Who needs it: callers that must not or cannot allocate device memory while
+ * they run -- a serving runtime that reserves the device's memory in its own
+ * pool at start-up and forbids later allocations, a plugin inside a host
+ * application that owns the device memory and gives it no allocator, or
+ * latency-critical code where cudaMalloc / cudaFree would implicitly
+ * synchronise the device.  The regular split-K path needs scratch for its
+ * partial sums and either takes it from the caller or allocates it; this one
+ * uses a fixed array of W8A8_NOALLOC_SCRATCH_BYTES in device memory that is
+ * part of the library itself (every GPU that loads the library holds it until
+ * the process exits), and calls no cudaMalloc, cudaFree or other allocating
+ * routine.
+ *
+ * Same operation, arguments and errors as w8a8_block_fp8_matmul with the
+ * split-K variant forced; split_k = 0 lets the dispatcher choose the split
+ * count.  A problem whose scratch (the 256 KiB counter block plus
+ * split_k * M * N * 4 bytes of partial sums) exceeds the array is rejected
+ * with W8A8_ERR_WORKSPACE before anything is launched.
+ *
+ * The first call on each device does a one-time set-up (it looks up the
+ * array's device address with that device current); make that first call
+ * before any stream capture.  All calls share the one array, which keeps the
+ * last call's contents (each call zeroes the counters it uses): calls that
+ * overlap on the GPU -- e.g. on two streams without ordering between them --
+ * race and give wrong results.  Order them (one stream, or events).
+ */
+#define W8A8_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
+w8a8_status w8a8_block_fp8_matmul_splitk_noalloc(const void *A_dev, const float *a_s_dev,
+                                                 const void *B_dev, const float *b_s_dev,
+                                                 void *C_dev, int64_t M, int64_t N, int64_t K,
+                                                 int block_n, int block_k,
+                                                 w8a8_out_dtype out_dtype, int split_k,
+                                                 w8a8_stream_t stream);
+
 /* Bytes of device staging that w8a8_block_fp8_matmul_host needs (0 for bad sizes). */
 size_t w8a8_block_fp8_host_staging_size(int64_t M, int64_t N, int64_t K, w8a8_out_dtype out_dtype);
 
