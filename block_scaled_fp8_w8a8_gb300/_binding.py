@@ -51,6 +51,8 @@ class w8a8_options(ctypes.Structure):
         ("grid_limit", ctypes.c_int),
         ("pdl", ctypes.c_int),
         ("debug_skip_load", ctypes.c_int),
+        ("weights_static", ctypes.c_int),
+        ("reserved_i", ctypes.c_int * 3),
         ("workspace_dev", ctypes.c_void_p),
         ("workspace_bytes", ctypes.c_size_t),
         ("wait_limit_cycles", ctypes.c_ulonglong),

@@ -131,6 +131,28 @@ w8a8_status encode_u8_map(CUtensorMap *map, const void *base, int64_t rows, int6
     return W8A8_OK;
 }
 
+// 2-D tensor map over the row-major [rows, cols] output C in its dtype; boxes
+// of 128 columns by box_rows rows, no swizzle (dense rows in shared memory).
+w8a8_status encode_out_map(CUtensorMap *map, void *base, int64_t rows, int64_t cols, int out,
+                           int box_rows)
+{
+    const int eb = out == W8A8_OUT_FP32 ? 4 : 2;
+    const CUtensorMapDataType dt = out == W8A8_OUT_FP32   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                   : out == W8A8_OUT_FP16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                          : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * eb};
+    cuuint32_t box[2] = {128u, static_cast<cuuint32_t>(box_rows)};
+    cuuint32_t elem[2] = {1u, 1u};
+    CUresult r = g_encode(map, dt, 2, base, dims, strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(W8A8_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for C [%lld, %lld]",
+                    static_cast<int>(r), static_cast<long long>(rows), static_cast<long long>(cols));
+    return W8A8_OK;
+}
+
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -188,7 +210,7 @@ struct Plan {
     size_t smem;
 };
 
-w8a8_status make_plan(int64_t M, int64_t N, int64_t K, const w8a8_options *o,
+w8a8_status make_plan(int64_t M, int64_t N, int64_t K, int out_bytes, const w8a8_options *o,
                       const DeviceInfo &dev, Plan *pl)
 {
     const int G = static_cast<int>(K / 128);
@@ -261,9 +283,9 @@ w8a8_status make_plan(int64_t M, int64_t N, int64_t K, const w8a8_options *o,
     splits = static_cast<int>(cdiv(G, gps));       // every split non-empty
     int max_stages = std::min(8, gps);
     int stages = stage_hint ? std::min(stage_hint, max_stages) : max_stages;
-    while (stages > 1 && swapab_smem_bytes(mt, stages, gps) > dev.smem_optin)
+    while (stages > 1 && swapab_smem_bytes(mt, stages, gps, out_bytes) > dev.smem_optin)
         --stages;
-    if (stages < 2 && gps > 1 && swapab_smem_bytes(mt, 2, gps) > dev.smem_optin)
+    if (stages < 2 && gps > 1 && swapab_smem_bytes(mt, 2, gps, out_bytes) > dev.smem_optin)
         return fail(W8A8_ERR_UNSUPPORTED,
                     "K=%lld is too long for one swap-AB CTA; use the split-K variant",
                     (long long)K);
@@ -273,7 +295,7 @@ w8a8_status make_plan(int64_t M, int64_t N, int64_t K, const w8a8_options *o,
     pl->splits = splits;
     pl->gps = gps;
     pl->stages = stages;
-    pl->smem = swapab_smem_bytes(mt, stages, gps);
+    pl->smem = swapab_smem_bytes(mt, stages, gps, out_bytes);
     if (splits == 1)
         pl->variant = W8A8_VARIANT_SWAPAB;
     return W8A8_OK;
@@ -354,7 +376,7 @@ w8a8_status run(const void *A, const float *a_s, const void *B, const float *b_s
     if ((st = current_device(&dev, &info)) != W8A8_OK)
         return st;
     Plan pl;
-    if ((st = make_plan(M, N, K, o, info, &pl)) != W8A8_OK)
+    if ((st = make_plan(M, N, K, out == W8A8_OUT_FP32 ? 4 : 2, o, info, &pl)) != W8A8_OK)
         return st;
 
     const int G = static_cast<int>(K / 128);
@@ -392,9 +414,10 @@ w8a8_status run(const void *A, const float *a_s, const void *B, const float *b_s
         p.wait_limit = limit;
         e = launch_tiled(mA, mB, p, pl.bn, cfg);
     } else {
-        CUtensorMap mW, mX;
+        CUtensorMap mW, mX, mC;
         if ((st = encode_u8_map(&mW, B, N, K, 128)) != W8A8_OK ||
-            (st = encode_u8_map(&mX, A, M, K, pl.mma_n)) != W8A8_OK)
+            (st = encode_u8_map(&mX, A, M, K, pl.mma_n)) != W8A8_OK ||
+            (st = encode_out_map(&mC, C, M, N, out, pl.mma_n)) != W8A8_OK)
             return st;
         SwapParams p;
         p.a_s = a_s;
@@ -429,10 +452,12 @@ w8a8_status run(const void *A, const float *a_s, const void *B, const float *b_s
         p.splits = pl.splits;
         p.groups_per_split = pl.gps;
         p.out_kind = out;
+        p.out_bytes = out == W8A8_OUT_FP32 ? 4 : 2;
+        p.prefetch_weights = (o && o->pdl && o->weights_static) ? 1 : 0;
         p.debug_skip_tma = debug_skip;
         p.status = info.status;
         p.wait_limit = limit;
-        e = launch_swapab(mW, mX, p, pl.mt, cfg);
+        e = launch_swapab(mW, mX, mC, p, pl.mt, cfg);
     }
     if (e != cudaSuccess)
         return cuda_fail(e, "kernel launch");
@@ -543,7 +568,7 @@ size_t w8a8_block_fp8_workspace_size(int64_t M, int64_t N, int64_t K, const w8a8
     if (current_device(&dev, &info) != W8A8_OK)
         return 0;
     Plan pl;
-    if (make_plan(M, N, K, opts, info, &pl) != W8A8_OK)
+    if (make_plan(M, N, K, 4, opts, info, &pl) != W8A8_OK)
         return 0;
     return splitk_workspace_bytes(M, N, pl);
 }
@@ -562,7 +587,7 @@ w8a8_status w8a8_block_fp8_plan(int64_t M, int64_t N, int64_t K, w8a8_out_dtype 
     if ((st = current_device(&dev, &info)) != W8A8_OK)
         return st;
     Plan pl;
-    if ((st = make_plan(M, N, K, opts, info, &pl)) != W8A8_OK)
+    if ((st = make_plan(M, N, K, out_dtype == W8A8_OUT_FP32 ? 4 : 2, opts, info, &pl)) != W8A8_OK)
         return st;
     std::memset(plan_out, 0, sizeof(*plan_out));
     plan_out->variant = pl.variant;

@@ -20,6 +20,8 @@
 // mma_n x 128 B per group), warp 1 MMA issuer (tcgen05.mma kind::f8f6f4,
 // M = 128, N = mma_n, 4 x K=32 per group) into one of two TMEM buffers,
 // 1 or 2 promotion warpgroups: thread = weight row n, columns = tokens.
+// Unsplit tiles leave through shared memory and one TMA store; split tiles
+// through the workspace and a vectorised ordered reduction.
 #include "kernels.cuh"
 #include "ptx.cuh"
 
@@ -37,27 +39,48 @@ template <int MT> struct SwapLayout {
     static constexpr uint32_t kXBytes = static_cast<uint32_t>(MT) * 128u;
     static constexpr uint32_t kTmemCols = 2 * MT < 32 ? 32 : 2 * MT;
     static constexpr int kBars = 2 * kMaxStages + 5;
-    static size_t smem(int stages, int gps)
+    // Operand stages; after the main loop the same bytes hold the C tile.
+    __host__ __device__ static size_t area(int stages, int out_bytes)
     {
-        return 1024 + static_cast<size_t>(stages) * (kWBytes + kXBytes) +
-               static_cast<size_t>(gps) * MT * 4 + kBars * 8 + 16;
+        const size_t st = static_cast<size_t>(stages) * (kWBytes + kXBytes);
+        const size_t ct = static_cast<size_t>(MT) * 128 * out_bytes;
+        return st > ct ? st : ct;
+    }
+    static size_t smem(int stages, int gps, int out_bytes)
+    {
+        return 1024 + area(stages, out_bytes) + static_cast<size_t>(gps) * MT * 4 + kBars * 8 + 16;
     }
 };
 
-__device__ __forceinline__ void store_one(void *C, size_t idx, float v, int out_kind)
+__device__ __forceinline__ void store4(void *C, size_t idx, float4 v, int out_kind)
 {
-    if (out_kind == OUT_BF16)
-        static_cast<__nv_bfloat16 *>(C)[idx] = __float2bfloat16_rn(v);
-    else if (out_kind == OUT_FP16)
-        static_cast<__half *>(C)[idx] = __float2half_rn(v);
-    else
-        static_cast<float *>(C)[idx] = v;
+    if (out_kind == OUT_FP32) {
+        *reinterpret_cast<float4 *>(static_cast<float *>(C) + idx) = v;
+    } else {
+        uint2 u;
+        if (out_kind == OUT_BF16) {
+            u.x = pack_bf16x2(v.x, v.y);
+            u.y = pack_bf16x2(v.z, v.w);
+        } else {
+            u.x = pack_f16x2(v.x, v.y);
+            u.y = pack_f16x2(v.z, v.w);
+        }
+        *reinterpret_cast<uint2 *>(static_cast<uint16_t *>(C) + idx) = u;
+    }
+}
+
+__device__ __forceinline__ void add4(float4 &a, const float4 &b)
+{
+    a.x += b.x;
+    a.y += b.y;
+    a.z += b.z;
+    a.w += b.w;
 }
 
 template <int MT>
 __global__ void __launch_bounds__(SwapLayout<MT>::kThreads, 1)
     k_swapab(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
-             const SwapParams p, const int stages)
+             const __grid_constant__ CUtensorMap tmC, const SwapParams p, const int stages)
 {
     using L = SwapLayout<MT>;
     extern __shared__ uint8_t smem_raw[];
@@ -65,7 +88,7 @@ __global__ void __launch_bounds__(SwapLayout<MT>::kThreads, 1)
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const uint32_t sW = smem_addr(smem);
     const uint32_t sX = sW + stages * L::kWBytes;
-    float *sscale = reinterpret_cast<float *>(smem + stages * (L::kWBytes + L::kXBytes));
+    float *sscale = reinterpret_cast<float *>(smem + L::area(stages, p.out_bytes));
     uint64_t *bars = reinterpret_cast<uint64_t *>(sscale + p.groups_per_split * MT);
     const uint32_t bar0 = smem_addr(bars);
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
@@ -84,6 +107,7 @@ __global__ void __launch_bounds__(SwapLayout<MT>::kThreads, 1)
     const int g_begin = split * p.groups_per_split;
     const int g_end = min(p.G, g_begin + p.groups_per_split);
     const int ng = g_end - g_begin;
+    const bool is_producer = warp == 0 && lane == 0;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < stages; ++s) {
@@ -99,9 +123,10 @@ __global__ void __launch_bounds__(SwapLayout<MT>::kThreads, 1)
         *last_flag = 0;
         mbar_fence_init();
     }
-    if (warp == 0 && lane == 0) {
+    if (is_producer) {
         tma_prefetch_map(&tmW);
         tma_prefetch_map(&tmX);
+        tma_prefetch_map(&tmC);
     }
     if (warp == 1) {
         tmem_alloc(smem_addr(tmem_slot), L::kTmemCols);
@@ -114,28 +139,43 @@ __global__ void __launch_bounds__(SwapLayout<MT>::kThreads, 1)
     const WaitGuard guard{abort_flag, p.status, p.wait_limit};
 
     grid_launch_dependents();
-    grid_dependency_wait();
+    if (!is_producer)
+        grid_dependency_wait();     // the producer waits after its weight prefetch
 
     if (warp < 4) {
         if constexpr (L::kPromoWG == 2)
             regs_dealloc<40>();
-        if (warp == 0 && lane == 0) {
+        if (is_producer) {
             // ---------------------------------------------------------- TMA producer
             const uint32_t tx = L::kWBytes + static_cast<uint32_t>(p.mma_n) * 128u;
+            // Weights do not depend on the previous grid when the caller says so:
+            // start the first stages' B loads before waiting for it.
+            const int pre = p.prefetch_weights ? min(stages, ng) : 0;
+            for (int i = 0; i < pre; ++i) {
+                if (i != p.debug_skip_tma) {
+                    mbar_arrive_expect_tx(full_bar(i), tx);
+                    tma_load_2d(sW + i * L::kWBytes, &tmW, full_bar(i), (g_begin + i) * 128, nb * 128);
+                }
+            }
+            grid_dependency_wait();
             int stage = 0;
             uint32_t phase = 0;
             int issued = 0;
             bool ok = true;
-            for (int g = g_begin; g < g_end; ++g) {
-                if (!wait_bounded(empty_bar(stage), phase ^ 1u, guard, SITE_SWAP_PRODUCER)) {
-                    ok = false;
-                    break;
+            for (int i = 0; i < ng; ++i) {
+                const int g = g_begin + i;
+                if (i >= pre) {
+                    if (!wait_bounded(empty_bar(stage), phase ^ 1u, guard, SITE_SWAP_PRODUCER)) {
+                        ok = false;
+                        break;
+                    }
+                    if (i != p.debug_skip_tma) {
+                        mbar_arrive_expect_tx(full_bar(stage), tx);
+                        tma_load_2d(sW + stage * L::kWBytes, &tmW, full_bar(stage), g * 128, nb * 128);
+                    }
                 }
-                if (issued != p.debug_skip_tma) {
-                    mbar_arrive_expect_tx(full_bar(stage), tx);
-                    tma_load_2d(sW + stage * L::kWBytes, &tmW, full_bar(stage), g * 128, nb * 128);
+                if (i != p.debug_skip_tma)
                     tma_load_2d(sX + stage * L::kXBytes, &tmX, full_bar(stage), g * 128, m0);
-                }
                 ++issued;
                 if (++stage == stages) {
                     stage = 0;
@@ -153,6 +193,7 @@ __global__ void __launch_bounds__(SwapLayout<MT>::kThreads, 1)
                     }
                 }
             } else {
+                // Drain: wait for the loads still landing in this CTA's shared memory.
                 for (int s = 0; s < stages; ++s) {
                     const bool this_round = s < stage;
                     if (!this_round && issued < stages && s >= issued)
@@ -203,7 +244,8 @@ __global__ void __launch_bounds__(SwapLayout<MT>::kThreads, 1)
         constexpr int kPromoThreads = 128 * L::kPromoWG;
         const int h = tid / 128;                             // column half
         const uint32_t q = warp & 3u;                        // TMEM lane quarter
-        const int n = nb * 128 + static_cast<int>(q * 32 + lane);
+        const int row = static_cast<int>(q * 32 + lane);     // weight row within the block
+        const int n = nb * 128 + row;
         const int c0 = h * L::kCols;                         // first token column of this thread
 
         // Folded scales s[g][j] = a_s[m0+j, g] * b_s[nb, g] (zero past M and mma_n).
@@ -228,6 +270,8 @@ __global__ void __launch_bounds__(SwapLayout<MT>::kThreads, 1)
         for (int i = 0; i < ng; ++i) {
             const uint32_t buf = i & 1;
             const uint32_t bphase = (i >> 1) & 1;
+            // All lanes wait; the warp proceeds only if every lane saw the
+            // buffer (tcgen05.ld below is a warp-wide instruction).
             ok = __all_sync(0xffffffffu,
                             wait_bounded(tfull_bar(buf), bphase, guard, SITE_SWAP_PROMOTE));
             if (!ok)
@@ -257,49 +301,85 @@ __global__ void __launch_bounds__(SwapLayout<MT>::kThreads, 1)
         }
 
         ok = named_barrier_and(1, kPromoThreads, ok);   // one decision for all promotion warps
-        if (ok) {
-            const bool n_ok = n < p.N;
-            if (p.splits == 1) {
+        if (ok && p.splits == 1) {
+            // C tile [mma_n rows][128 cols] in the (now idle) stage area, then one
+            // TMA store; rows past M and columns past N are clipped by the store.
+            if (p.out_kind == OUT_FP32) {
+                float *tile = reinterpret_cast<float *>(smem);
 #pragma unroll
-                for (int j = 0; j < L::kCols; ++j) {
-                    const int m = m0 + c0 + j;
-                    if (n_ok && c0 + j < p.mma_n && m < p.M)
-                        store_one(p.C, static_cast<size_t>(m) * p.N + n, acc[j], p.out_kind);
-                }
+                for (int j = 0; j < L::kCols; ++j)
+                    if (c0 + j < p.mma_n)
+                        tile[(c0 + j) * 128 + row] = acc[j];
             } else {
-                // Deterministic split-K: publish this split's partial tile, take a
-                // ticket; the last arrival sums the splits in order 0..S-1.
-                float *ws = p.ws + static_cast<size_t>(split) * p.M * p.N;
+                __nv_bfloat16 *tb = reinterpret_cast<__nv_bfloat16 *>(smem);
+                __half *th = reinterpret_cast<__half *>(smem);
+                const bool bf = p.out_kind == OUT_BF16;
 #pragma unroll
                 for (int j = 0; j < L::kCols; ++j) {
-                    const int m = m0 + c0 + j;
-                    if (n_ok && c0 + j < p.mma_n && m < p.M)
-                        ws[static_cast<size_t>(m) * p.N + n] = acc[j];
-                }
-                __threadfence();
-                named_barrier(1, kPromoThreads);
-                const int tile = blockIdx.z * gridDim.x + blockIdx.x;
-                if (tid == 0) {
-                    const unsigned prev = atomicAdd(p.counters + tile, 1u);
-                    *last_flag = (prev == static_cast<unsigned>(p.splits - 1)) ? 1 : 0;
-                }
-                named_barrier(1, kPromoThreads);
-                if (*last_flag) {
-                    __threadfence();
-#pragma unroll 4
-                    for (int j = 0; j < L::kCols; ++j) {
-                        const int m = m0 + c0 + j;
-                        if (n_ok && c0 + j < p.mma_n && m < p.M) {
-                            const size_t off = static_cast<size_t>(m) * p.N + n;
-                            float sum = 0.f;
-                            for (int s = 0; s < p.splits; ++s)
-                                sum += __ldcg(p.ws + static_cast<size_t>(s) * p.M * p.N + off);
-                            store_one(p.C, off, sum, p.out_kind);
-                        }
+                    if (c0 + j < p.mma_n) {
+                        if (bf)
+                            tb[(c0 + j) * 128 + row] = __float2bfloat16_rn(acc[j]);
+                        else
+                            th[(c0 + j) * 128 + row] = __float2half_rn(acc[j]);
                     }
-                    if (tid == 0)
-                        p.counters[tile] = 0u;   // ready for the next call
                 }
+            }
+            fence_async_smem();
+            named_barrier(1, kPromoThreads);
+            if (tid == 0) {
+                tma_store_2d(&tmC, sW, nb * 128, m0);
+                tma_store_commit();
+                tma_store_wait_all();
+            }
+        } else if (ok) {
+            // Deterministic split-K: publish this split's partial tile, take a
+            // ticket; the last arrival sums the splits in order 0..S-1.
+            const bool n_ok = n < p.N;
+            float *ws = p.ws + static_cast<size_t>(split) * p.M * p.N;
+#pragma unroll
+            for (int j = 0; j < L::kCols; ++j) {
+                const int m = m0 + c0 + j;
+                if (n_ok && c0 + j < p.mma_n && m < p.M)
+                    ws[static_cast<size_t>(m) * p.N + n] = acc[j];
+            }
+            __threadfence();
+            named_barrier(1, kPromoThreads);
+            const int tile = blockIdx.z * gridDim.x + blockIdx.x;
+            if (tid == 0) {
+                const unsigned prev = atomicAdd(p.counters + tile, 1u);
+                *last_flag = (prev == static_cast<unsigned>(p.splits - 1)) ? 1 : 0;
+            }
+            named_barrier(1, kPromoThreads);
+            if (*last_flag) {
+                __threadfence();
+                // Items of 4 consecutive columns; consecutive threads take
+                // consecutive items (coalesced 16-byte loads), and each item
+                // keeps up to 8 split loads in flight before summing them in order.
+                const int rows = min(p.mma_n, p.M - m0);
+                const int c4n = min(128, p.N - nb * 128) / 4;
+                const int items = rows * c4n;
+                const size_t plane = static_cast<size_t>(p.M) * p.N;
+                for (int it = tid; it < items; it += kPromoThreads) {
+                    const int r = it / c4n, c4 = it - r * c4n;
+                    const size_t off = static_cast<size_t>(m0 + r) * p.N + nb * 128 + 4 * c4;
+                    const float *src = p.ws + off;
+                    float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
+                    int s = 0;
+                    for (; s + 8 <= p.splits; s += 8) {
+                        float4 v[8];
+#pragma unroll
+                        for (int u = 0; u < 8; ++u)
+                            v[u] = __ldcg(reinterpret_cast<const float4 *>(src + (s + u) * plane));
+#pragma unroll
+                        for (int u = 0; u < 8; ++u)
+                            add4(sum, v[u]);
+                    }
+                    for (; s < p.splits; ++s)
+                        add4(sum, __ldcg(reinterpret_cast<const float4 *>(src + s * plane)));
+                    store4(p.C, off, sum, p.out_kind);
+                }
+                if (tid == 0)
+                    p.counters[tile] = 0u;   // ready for the next call
             }
         }
     }
@@ -313,12 +393,12 @@ __global__ void __launch_bounds__(SwapLayout<MT>::kThreads, 1)
 }
 
 template <int MT>
-cudaError_t launch_swapab_t(const CUtensorMap &tmW, const CUtensorMap &tmX, const SwapParams &p,
-                            const LaunchCfg &cfg)
+cudaError_t launch_swapab_t(const CUtensorMap &tmW, const CUtensorMap &tmX, const CUtensorMap &tmC,
+                            const SwapParams &p, const LaunchCfg &cfg)
 {
     using L = SwapLayout<MT>;
     auto kernel = k_swapab<MT>;
-    const size_t smem = L::smem(cfg.stages, p.groups_per_split);
+    const size_t smem = L::smem(cfg.stages, p.groups_per_split, p.out_bytes);
     static volatile int smem_set[kMaxDeviceFlags] = {};
     cudaError_t e = ensure_smem_limit(kernel, smem_set);
     if (e != cudaSuccess)
@@ -333,34 +413,34 @@ cudaError_t launch_swapab_t(const CUtensorMap &tmW, const CUtensorMap &tmX, cons
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     lc.attrs = attr;
     lc.numAttrs = cfg.pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&lc, kernel, tmW, tmX, p, cfg.stages);
+    return cudaLaunchKernelEx(&lc, kernel, tmW, tmX, tmC, p, cfg.stages);
 }
 
 }  // namespace
 
-size_t swapab_smem_bytes(int mt, int stages, int gps)
+size_t swapab_smem_bytes(int mt, int stages, int gps, int out_bytes)
 {
     if (stages < 1 || stages > kMaxStages)
         return 0;
     switch (mt) {
-    case 32: return SwapLayout<32>::smem(stages, gps);
-    case 64: return SwapLayout<64>::smem(stages, gps);
-    case 128: return SwapLayout<128>::smem(stages, gps);
-    case 256: return SwapLayout<256>::smem(stages, gps);
+    case 32: return SwapLayout<32>::smem(stages, gps, out_bytes);
+    case 64: return SwapLayout<64>::smem(stages, gps, out_bytes);
+    case 128: return SwapLayout<128>::smem(stages, gps, out_bytes);
+    case 256: return SwapLayout<256>::smem(stages, gps, out_bytes);
     default: return 0;
     }
 }
 
-cudaError_t launch_swapab(const CUtensorMap &tmW, const CUtensorMap &tmX, const SwapParams &p,
-                          int mt, const LaunchCfg &cfg)
+cudaError_t launch_swapab(const CUtensorMap &tmW, const CUtensorMap &tmX, const CUtensorMap &tmC,
+                          const SwapParams &p, int mt, const LaunchCfg &cfg)
 {
     if (cfg.stages < 1 || cfg.stages > kMaxStages)
         return cudaErrorInvalidValue;
     switch (mt) {
-    case 32: return launch_swapab_t<32>(tmW, tmX, p, cfg);
-    case 64: return launch_swapab_t<64>(tmW, tmX, p, cfg);
-    case 128: return launch_swapab_t<128>(tmW, tmX, p, cfg);
-    case 256: return launch_swapab_t<256>(tmW, tmX, p, cfg);
+    case 32: return launch_swapab_t<32>(tmW, tmX, tmC, p, cfg);
+    case 64: return launch_swapab_t<64>(tmW, tmX, tmC, p, cfg);
+    case 128: return launch_swapab_t<128>(tmW, tmX, tmC, p, cfg);
+    case 256: return launch_swapab_t<256>(tmW, tmX, tmC, p, cfg);
     default: return cudaErrorInvalidValue;
     }
 }

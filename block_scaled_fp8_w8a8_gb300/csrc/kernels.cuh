@@ -50,6 +50,8 @@ struct SwapParams {
     int splits;
     int groups_per_split;
     int out_kind;
+    int out_bytes;         // 2 (bf16, fp16) or 4 (fp32)
+    int prefetch_weights;  // start the B loads before waiting on the previous grid
     int debug_skip_tma;
     unsigned *status;
     unsigned long long wait_limit;
@@ -64,12 +66,14 @@ struct LaunchCfg {
 
 // Shared memory bytes each kernel configuration needs (0 = unsupported configuration).
 size_t tiled_smem_bytes(int bn, int stages);
-size_t swapab_smem_bytes(int mt, int stages, int groups_per_split);
+size_t swapab_smem_bytes(int mt, int stages, int groups_per_split, int out_bytes);
 
 cudaError_t launch_tiled(const CUtensorMap &tmA, const CUtensorMap &tmB, const TiledParams &p,
                          int bn, const LaunchCfg &cfg);
-cudaError_t launch_swapab(const CUtensorMap &tmW, const CUtensorMap &tmX, const SwapParams &p,
-                          int mt, const LaunchCfg &cfg);
+// tmC: C as a 2-D [M, N] tensor of the output type, box {128 columns, mma_n rows},
+// no swizzle (used by the epilogue's TMA store when splits == 1).
+cudaError_t launch_swapab(const CUtensorMap &tmW, const CUtensorMap &tmX, const CUtensorMap &tmC,
+                          const SwapParams &p, int mt, const LaunchCfg &cfg);
 
 // Raise `kernel`'s dynamic shared-memory limit to the device maximum, once per
 // device per kernel: `flags` is a per-kernel array of kMaxDeviceFlags words.

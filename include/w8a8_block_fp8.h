@@ -85,6 +85,10 @@ typedef enum {
  *   grid_limit         TILED only: cap on the number of persistent CTAs (0 = one per SM)
  *   pdl                1 = launch with programmatic dependent launch, so that the
  *                      kernel's prologue overlaps the previous kernel on the stream
+ *   weights_static     1 = B and b_s are not written by the work that precedes this
+ *                      call on the stream; with pdl = 1 the kernel then starts
+ *                      streaming B before that work has finished (A, a_s and C
+ *                      still wait for it).  0 = everything waits.
  *   debug_skip_load    test hook: n > 0 makes the producer of every CTA skip its
  *                      n-th operand load, so that a bounded device wait runs out
  *                      and the call surfaces W8A8_ERR_DEVICE_TIMEOUT through
@@ -107,6 +111,8 @@ typedef struct {
     int grid_limit;
     int pdl;
     int debug_skip_load;
+    int weights_static;
+    int reserved_i[3];
     void *workspace_dev;
     size_t workspace_bytes;
     unsigned long long wait_limit_cycles;
