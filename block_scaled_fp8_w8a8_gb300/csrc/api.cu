@@ -231,9 +231,12 @@ w8a8_status make_plan(int64_t M, int64_t N, int64_t K, int out_bytes, const w8a8
             if (!bn_hint) bn_hint = t->block_n_tile;
             if (!stage_hint) stage_hint = t->stages;
         } else if (M <= 256) {
+            // Rules distilled from the tuning sweep: small token tiles (more
+            // CTAs) win at decode sizes; split K only when K is long and the
+            // tiles alone cannot fill half the SMs.
             variant = W8A8_VARIANT_SWAPAB;
-            const int64_t ctas = NB;
-            if (ctas * 2 <= dev.sm_count && G >= 4)
+            const int64_t ctas = NB * cdiv(M, M <= 16 ? 16 : 32);
+            if (ctas * 2 <= dev.sm_count && G >= 16)
                 variant = W8A8_VARIANT_SPLITK;
         } else {
             variant = W8A8_VARIANT_TILED;
@@ -263,6 +266,9 @@ w8a8_status make_plan(int64_t M, int64_t N, int64_t K, int out_bytes, const w8a8
     if (mtile_hint) {
         mma_n = mtile_hint;
         m_tiles = static_cast<int>(cdiv(M, mma_n));
+    } else if (M <= 512) {
+        mma_n = M <= 16 ? 16 : 32;
+        m_tiles = static_cast<int>(cdiv(M, mma_n));
     } else {
         m_tiles = static_cast<int>(cdiv(M, 256));
         mma_n = static_cast<int>(cdiv(cdiv(M, m_tiles), 16) * 16);
@@ -275,7 +281,8 @@ w8a8_status make_plan(int64_t M, int64_t N, int64_t K, int out_bytes, const w8a8
             splits = split_hint;
         } else {
             const int64_t ctas = static_cast<int64_t>(NB) * m_tiles;
-            splits = static_cast<int>(std::max<int64_t>(1, dev.sm_count / std::max<int64_t>(ctas, 1)));
+            splits = static_cast<int>(std::max<int64_t>(2, dev.sm_count / std::max<int64_t>(ctas, 1)));
+            splits = std::min(splits, 16);
         }
         splits = std::min(std::max(splits, 1), G);
     }

@@ -11,9 +11,12 @@
 //   warp 1      MMA issuer: 4 x tcgen05.mma kind::f8f6f4 (K = 32 each) turn
 //               one stage into the group's fp32 partial P_g in a TMEM buffer;
 //               commits free the stage and publish the buffer.
+//   warp 2      scale loader: cp.async gathers of a_s[m0..m0+127, g] and of the
+//               tile's b_s[., g] into a ring of shared-memory slots, so that
+//               the promotion never waits on global memory.
 //   warps 4..   BN/128 promotion warpgroups: each thread owns one row and 128
 //               columns; per group it reads P_g from TMEM (tcgen05.ld), applies
-//               the scale a_s[m,g] * b_s[n/128,g] with an fp32 FMA into its
+//               the scale a_s[m,g] * b_s[n/128,g] with paired fp32 FMAs into its
 //               register accumulator, and releases the buffer.  After the last
 //               group it casts and stores its row segment.
 // TMEM holds 512 / BN partial buffers of BN columns (all 512 columns), so the
@@ -31,6 +34,8 @@ namespace w8a8 {
 namespace {
 
 constexpr int kGroupRaster = 16;   // M tiles per raster group
+constexpr int kScaleSlots = 8;     // depth of the scale ring
+constexpr int kSlotFloats = 144;   // 128 a_s values + up to 2 b_s values, padded
 
 __device__ __forceinline__ void tile_coords(int t, int num_m, int num_n, int &mb, int &nb)
 {
@@ -43,26 +48,33 @@ __device__ __forceinline__ void tile_coords(int t, int num_m, int num_n, int &mb
     nb = r / gm;
 }
 
-// Store 128 consecutive fp32 accumulators of one row as out_kind, in 16-byte chunks,
-// skipping chunks at or beyond column N (N is a multiple of 16).
-__device__ __forceinline__ void store_row128(const float (&acc)[128], void *C, size_t row_off,
+// Store 128 consecutive fp32 accumulators (as 64 pairs) of one row as out_kind,
+// in 16-byte chunks, skipping chunks at or beyond column N (a multiple of 16).
+__device__ __forceinline__ void store_row128(const uint64_t (&acc)[64], void *C, size_t row_off,
                                              int col0, int N, int out_kind)
 {
     if (out_kind == OUT_FP32) {
         float *dst = static_cast<float *>(C) + row_off + col0;
 #pragma unroll
-        for (int c = 0; c < 32; ++c)
-            if (col0 + 4 * c < N)
-                *reinterpret_cast<float4 *>(dst + 4 * c) =
-                    make_float4(acc[4 * c], acc[4 * c + 1], acc[4 * c + 2], acc[4 * c + 3]);
+        for (int c = 0; c < 32; ++c) {
+            if (col0 + 4 * c < N) {
+                float4 v;
+                unpack2f(acc[2 * c], v.x, v.y);
+                unpack2f(acc[2 * c + 1], v.z, v.w);
+                *reinterpret_cast<float4 *>(dst + 4 * c) = v;
+            }
+        }
     } else {
         uint16_t *dst = static_cast<uint16_t *>(C) + row_off + col0;
         const bool bf = out_kind == OUT_BF16;
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
             if (col0 + 8 * c < N) {
+                float a[8];
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    unpack2f(acc[4 * c + i], a[2 * i], a[2 * i + 1]);
                 uint4 v;
-                const float *a = &acc[8 * c];
                 v.x = bf ? pack_bf16x2(a[0], a[1]) : pack_f16x2(a[0], a[1]);
                 v.y = bf ? pack_bf16x2(a[2], a[3]) : pack_f16x2(a[2], a[3]);
                 v.z = bf ? pack_bf16x2(a[4], a[5]) : pack_f16x2(a[4], a[5]);
@@ -80,8 +92,10 @@ template <int BN, int STAGES> struct TiledLayout {
     static constexpr uint32_t kBBytes = static_cast<uint32_t>(BN) * 128u;
     static constexpr int kBufs = 512 / BN;                  // TMEM partial buffers
     static constexpr uint32_t kTmemCols = 512;
-    static constexpr int kBars = 2 * STAGES + 2 * kBufs + 1;
-    static constexpr size_t kSmem = 1024 + STAGES * (kABytes + kBBytes) + kBars * 8 + 16;
+    static constexpr size_t kStageBytes = STAGES * (kABytes + kBBytes);
+    static constexpr size_t kScaleBytes = kScaleSlots * kSlotFloats * 4;
+    static constexpr int kBars = 2 * STAGES + 2 * kBufs + 2 * kScaleSlots + 1;
+    static constexpr size_t kSmem = 1024 + kStageBytes + kScaleBytes + kBars * 8 + 16;
 };
 
 template <int BN, int STAGES>
@@ -95,13 +109,18 @@ __global__ void __launch_bounds__(TiledLayout<BN, STAGES>::kThreads, 1)
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const uint32_t sA = smem_addr(smem);
     const uint32_t sB = sA + STAGES * L::kABytes;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + STAGES * (L::kABytes + L::kBBytes));
+    float *scales = reinterpret_cast<float *>(smem + L::kStageBytes);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kStageBytes + L::kScaleBytes);
     const uint32_t bar0 = smem_addr(bars);
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
     auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
     auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
     auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + L::kBufs + b); };
-    const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 2 * L::kBufs);
+    auto sfull_bar = [&](int q) { return bar0 + 8u * (2 * STAGES + 2 * L::kBufs + q); };
+    auto sempty_bar = [&](int q) {
+        return bar0 + 8u * (2 * STAGES + 2 * L::kBufs + kScaleSlots + q);
+    };
+    const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 2 * L::kBufs + 2 * kScaleSlots);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + L::kBars);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
@@ -115,6 +134,10 @@ __global__ void __launch_bounds__(TiledLayout<BN, STAGES>::kThreads, 1)
         for (int b = 0; b < L::kBufs; ++b) {
             mbar_init(tfull_bar(b), 1);
             mbar_init(tempty_bar(b), 4 * L::kPromoWG);
+        }
+        for (int q = 0; q < kScaleSlots; ++q) {
+            mbar_init(sfull_bar(q), 32);                 // one cp.async arrival per loader lane
+            mbar_init(sempty_bar(q), 4 * L::kPromoWG);
         }
         mbar_init(drain_bar, 1);
         *abort_flag = 0;
@@ -182,8 +205,8 @@ __global__ void __launch_bounds__(TiledLayout<BN, STAGES>::kThreads, 1)
                     const bool this_round = s < stage;
                     if (!this_round && issued < STAGES && s >= issued)
                         continue;
-                    wait_drain(full_bar(s), this_round ? phase : (phase ^ 1u), p.status, p.wait_limit,
-                               (SITE_DRAIN << 8) | 4u);
+                    wait_drain(full_bar(s), this_round ? phase : (phase ^ 1u), p.status,
+                               p.wait_limit, (SITE_DRAIN << 8) | 4u);
                 }
             }
         } else if (warp == 1 && lane == 0) {
@@ -222,6 +245,44 @@ __global__ void __launch_bounds__(TiledLayout<BN, STAGES>::kThreads, 1)
                 mma_commit(drain_bar);
                 wait_drain(drain_bar, 0, p.status, p.wait_limit, (SITE_DRAIN << 8) | 4u);
             }
+        } else if (warp == 2) {
+            // ---------------------------------------------------------- scale loader
+            int slot = 0;
+            uint32_t sphase = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+                int mb, nb;
+                tile_coords(t, p.num_m_tiles, p.num_n_tiles, mb, nb);
+                for (int g = 0; g < p.G; ++g) {
+                    ok = __all_sync(0xffffffffu, wait_bounded(sempty_bar(slot), sphase ^ 1u, guard,
+                                                              SITE_TILED_SCALES));
+                    if (!ok)
+                        break;
+                    const uint32_t dst = smem_addr(scales + slot * kSlotFloats);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int r = static_cast<int>(lane) + 32 * i;
+                        const int m = mb * 128 + r;
+                        const bool in = m < p.M;
+                        cp_async_4(dst + 4u * r, p.a_s + static_cast<size_t>(in ? m : 0) * p.G + g,
+                                   in ? 4u : 0u);
+                    }
+                    if (lane < static_cast<uint32_t>(L::kPromoWG)) {
+                        const int col0 = nb * BN + static_cast<int>(lane) * 128;
+                        const bool in = col0 < p.N;
+                        cp_async_4(dst + 4u * (128 + lane),
+                                   p.b_s + static_cast<size_t>(in ? col0 / 128 : 0) * p.G + g,
+                                   in ? 4u : 0u);
+                    }
+                    cp_async_arrive(sfull_bar(slot));
+                    if (++slot == kScaleSlots) {
+                        slot = 0;
+                        sphase ^= 1u;
+                    }
+                }
+            }
+            // Let every gather land before the CTA can exit.
+            asm volatile("cp.async.wait_all;" ::: "memory");
         }
         __syncwarp();
     } else {
@@ -232,45 +293,47 @@ __global__ void __launch_bounds__(TiledLayout<BN, STAGES>::kThreads, 1)
         const uint32_t q = warp & 3u;                      // TMEM lane quarter of this warp
         const int row = static_cast<int>(q * 32 + lane);
         uint32_t it = 0;
+        int slot = 0;
+        uint32_t sphase = 0;
         for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
             int mb, nb;
             tile_coords(t, p.num_m_tiles, p.num_n_tiles, mb, nb);
             const int m = mb * 128 + row;
             const int col0 = nb * BN + h * 128;
-            const bool m_ok = m < p.M;
-            const bool n_ok = col0 < p.N;
-            const float *as_row = p.a_s + static_cast<size_t>(m_ok ? m : 0) * p.G;
-            const float *bs_row = p.b_s + static_cast<size_t>(n_ok ? col0 / 128 : 0) * p.G;
-            float acc[128];
+            uint64_t acc[64];
 #pragma unroll
-            for (int j = 0; j < 128; ++j)
-                acc[j] = 0.f;
-            float sa = m_ok ? __ldg(as_row) : 0.f;
-            float sb = __ldg(bs_row);
+            for (int j = 0; j < 64; ++j)
+                acc[j] = 0ull;
             bool ok = true;
             for (int g = 0; g < p.G; ++g) {
-                const float s = sa * sb;
-                if (g + 1 < p.G) {
-                    sa = m_ok ? __ldg(as_row + g + 1) : 0.f;
-                    sb = __ldg(bs_row + g + 1);
-                }
                 const uint32_t buf = it % L::kBufs;
                 const uint32_t bphase = (it / L::kBufs) & 1u;
-                // All lanes wait; the warp proceeds only if every lane saw the
-                // buffer (tcgen05.ld below is a warp-wide instruction).
+                // All lanes wait; the warp proceeds only if every lane saw both
+                // (tcgen05.ld below is a warp-wide instruction).
                 ok = __all_sync(0xffffffffu,
-                                wait_bounded(tfull_bar(buf), bphase, guard, SITE_TILED_PROMOTE));
+                                wait_bounded(sfull_bar(slot), sphase, guard, SITE_TILED_PROMOTE) &&
+                                    wait_bounded(tfull_bar(buf), bphase, guard, SITE_TILED_PROMOTE));
                 if (!ok)
                     break;
+                const float *sl = scales + slot * kSlotFloats;
+                const float s = sl[row] * sl[128 + h];
+                const uint64_t s2 = pack2f(s, s);
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(sempty_bar(slot));
+                if (++slot == kScaleSlots) {
+                    slot = 0;
+                    sphase ^= 1u;
+                }
                 tc_fence_after_sync();
                 const uint32_t taddr = tmem_base + ((q * 32u) << 16) + buf * BN + h * 128;
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    float v[32];
-                    tmem_load_32cols(taddr + 32u * c, v);
+                for (int c = 0; c < 2; ++c) {
+                    uint32_t v[64];
+                    tmem_load_64cols(taddr + 64u * c, v);
 #pragma unroll
                     for (int j = 0; j < 32; ++j)
-                        acc[32 * c + j] = fmaf(s, v[j], acc[32 * c + j]);
+                        fma2(acc[32 * c + j], s2, pack2(v[2 * j], v[2 * j + 1]));
                 }
                 tc_fence_before_sync();
                 __syncwarp();
@@ -280,7 +343,7 @@ __global__ void __launch_bounds__(TiledLayout<BN, STAGES>::kThreads, 1)
             }
             if (!ok)
                 break;
-            if (m_ok && n_ok)
+            if (m < p.M && col0 < p.N)
                 store_row128(acc, p.C, static_cast<size_t>(m) * p.N, col0, p.N, p.out_kind);
         }
     }

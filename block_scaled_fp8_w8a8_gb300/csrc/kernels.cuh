@@ -20,6 +20,7 @@ enum WaitSite : uint32_t {
     SITE_SWAP_MMA_FULL = 7,
     SITE_SWAP_PROMOTE = 8,
     SITE_DRAIN = 9,
+    SITE_TILED_SCALES = 10,
 };
 
 // Tokens on the MMA M side: one CTA per SM walks 128 x BN output tiles.
