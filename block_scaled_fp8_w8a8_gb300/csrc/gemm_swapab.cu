@@ -270,8 +270,9 @@ __global__ void __launch_bounds__(SwapLayout<MT>::kThreads, 1)
         for (int i = 0; i < ng; ++i) {
             const uint32_t buf = i & 1;
             const uint32_t bphase = (i >> 1) & 1;
-            // All lanes wait; the warp proceeds only if every lane saw the
-            // buffer (tcgen05.ld below is a warp-wide instruction).
+            // All lanes wait (the whole warp sleeps in the barrier probe); the
+            // warp proceeds only if every lane saw the buffer (tcgen05.ld below
+            // is a warp-wide instruction).
             ok = __all_sync(0xffffffffu,
                             wait_bounded(tfull_bar(buf), bphase, guard, SITE_SWAP_PROMOTE));
             if (!ok)

@@ -162,7 +162,7 @@ __global__ void __launch_bounds__(TiledLayout<BN, STAGES>::kThreads, 1)
 
     if (warp < 4) {
         if constexpr (L::kPromoWG == 2)
-            regs_dealloc<40>();
+            regs_dealloc<56>();
         if (warp == 0 && lane == 0) {
             // ---------------------------------------------------------- TMA producer
             int stage = 0;
@@ -288,7 +288,7 @@ __global__ void __launch_bounds__(TiledLayout<BN, STAGES>::kThreads, 1)
     } else {
         // -------------------------------------------------------------- promotion + epilogue
         if constexpr (L::kPromoWG == 2)
-            regs_alloc<232>();
+            regs_alloc<224>();
         const int h = static_cast<int>(warp / 4) - 1;      // promotion warpgroup: column half
         const uint32_t q = warp & 3u;                      // TMEM lane quarter of this warp
         const int row = static_cast<int>(q * 32 + lane);
@@ -308,8 +308,9 @@ __global__ void __launch_bounds__(TiledLayout<BN, STAGES>::kThreads, 1)
             for (int g = 0; g < p.G; ++g) {
                 const uint32_t buf = it % L::kBufs;
                 const uint32_t bphase = (it / L::kBufs) & 1u;
-                // All lanes wait; the warp proceeds only if every lane saw both
-                // (tcgen05.ld below is a warp-wide instruction).
+                // All lanes wait, so that the whole warp sleeps in the barrier
+                // probe and wakes together; the warp proceeds only if every
+                // lane saw both (tcgen05.ld below is a warp-wide instruction).
                 ok = __all_sync(0xffffffffu,
                                 wait_bounded(sfull_bar(slot), sphase, guard, SITE_TILED_PROMOTE) &&
                                     wait_bounded(tfull_bar(buf), bphase, guard, SITE_TILED_PROMOTE));
@@ -327,6 +328,8 @@ __global__ void __launch_bounds__(TiledLayout<BN, STAGES>::kThreads, 1)
                 }
                 tc_fence_after_sync();
                 const uint32_t taddr = tmem_base + ((q * 32u) << 16) + buf * BN + h * 128;
+                // Two 64-column loads: TMEM load round trips, not FMA issue,
+                // bound this loop, so fewer and larger loads are faster.
 #pragma unroll
                 for (int c = 0; c < 2; ++c) {
                     uint32_t v[64];
