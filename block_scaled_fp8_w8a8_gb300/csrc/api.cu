@@ -132,9 +132,9 @@ w8a8_status encode_u8_map(CUtensorMap *map, const void *base, int64_t rows, int6
 }
 
 // 2-D tensor map over the row-major [rows, cols] output C in its dtype; boxes
-// of 128 columns by box_rows rows, no swizzle (dense rows in shared memory).
+// of box_cols columns by box_rows rows with the given shared-memory swizzle.
 w8a8_status encode_out_map(CUtensorMap *map, void *base, int64_t rows, int64_t cols, int out,
-                           int box_rows)
+                           int box_cols, int box_rows, CUtensorMapSwizzle swizzle)
 {
     const int eb = out == W8A8_OUT_FP32 ? 4 : 2;
     const CUtensorMapDataType dt = out == W8A8_OUT_FP32   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
@@ -142,10 +142,10 @@ w8a8_status encode_out_map(CUtensorMap *map, void *base, int64_t rows, int64_t c
                                                           : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * eb};
-    cuuint32_t box[2] = {128u, static_cast<cuuint32_t>(box_rows)};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
     cuuint32_t elem[2] = {1u, 1u};
     CUresult r = g_encode(map, dt, 2, base, dims, strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                          CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                          swizzle, CU_TENSOR_MAP_L2_PROMOTION_NONE,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS)
         return fail(W8A8_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for C [%lld, %lld]",
@@ -246,7 +246,8 @@ w8a8_status make_plan(int64_t M, int64_t N, int64_t K, int out_bytes, const w8a8
 
     if (variant == W8A8_VARIANT_TILED) {
         int bn = bn_hint ? bn_hint : (N % 256 == 0 ? 256 : 128);
-        int stages = bn == 256 ? 4 : (stage_hint == 4 ? 4 : 6);
+        int stages = bn == 256 ? (stage_hint == 3 ? 3 : 4)
+                               : ((stage_hint == 4 || stage_hint == 5) ? stage_hint : 6);
         const int64_t tiles = cdiv(M, 128) * cdiv(N, bn);
         int64_t grid = std::min<int64_t>(tiles, dev.sm_count);
         if (o && o->grid_limit)
@@ -399,9 +400,12 @@ w8a8_status run(const void *A, const float *a_s, const void *B, const float *b_s
 
     cudaError_t e;
     if (pl.variant == W8A8_VARIANT_TILED) {
-        CUtensorMap mA, mB;
+        CUtensorMap mA, mB, mC;
+        const int chunk_cols = out == W8A8_OUT_FP32 ? 16 : 32;   // 64 bytes of a row
         if ((st = encode_u8_map(&mA, A, M, K, 128)) != W8A8_OK ||
-            (st = encode_u8_map(&mB, B, N, K, pl.bn)) != W8A8_OK)
+            (st = encode_u8_map(&mB, B, N, K, pl.bn)) != W8A8_OK ||
+            (st = encode_out_map(&mC, C, M, N, out, chunk_cols, 32, CU_TENSOR_MAP_SWIZZLE_64B)) !=
+                W8A8_OK)
             return st;
         TiledParams p;
         p.a_s = a_s;
@@ -419,12 +423,13 @@ w8a8_status run(const void *A, const float *a_s, const void *B, const float *b_s
         p.debug_skip_tma = debug_skip;
         p.status = info.status;
         p.wait_limit = limit;
-        e = launch_tiled(mA, mB, p, pl.bn, cfg);
+        e = launch_tiled(mA, mB, mC, p, pl.bn, cfg);
     } else {
         CUtensorMap mW, mX, mC;
         if ((st = encode_u8_map(&mW, B, N, K, 128)) != W8A8_OK ||
             (st = encode_u8_map(&mX, A, M, K, pl.mma_n)) != W8A8_OK ||
-            (st = encode_out_map(&mC, C, M, N, out, pl.mma_n)) != W8A8_OK)
+            (st = encode_out_map(&mC, C, M, N, out, 128, pl.mma_n, CU_TENSOR_MAP_SWIZZLE_NONE)) !=
+                W8A8_OK)
             return st;
         SwapParams p;
         p.a_s = a_s;

@@ -48,39 +48,68 @@ __device__ __forceinline__ void tile_coords(int t, int num_m, int num_n, int &mb
     nb = r / gm;
 }
 
-// Store 128 consecutive fp32 accumulators (as 64 pairs) of one row as out_kind,
-// in 16-byte chunks, skipping chunks at or beyond column N (a multiple of 16).
-__device__ __forceinline__ void store_row128(const uint64_t (&acc)[64], void *C, size_t row_off,
-                                             int col0, int N, int out_kind)
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d)
 {
-    if (out_kind == OUT_FP32) {
-        float *dst = static_cast<float *>(C) + row_off + col0;
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+                 "r"(d)
+                 : "memory");
+}
+
+__device__ __forceinline__ uint32_t pack_out2(uint64_t pair, bool bf)
+{
+    float lo, hi;
+    unpack2f(pair, lo, hi);
+    return bf ? pack_bf16x2(lo, hi) : pack_f16x2(lo, hi);
+}
+
+// Epilogue of one warp: its 32 rows (lane = row) x 128 accumulator columns
+// (64 fp32 pairs) go out in chunks of 64 bytes per row.  Each chunk is written
+// to one of the warp's EB buffers of 2 KB in the layout a TMA store with the
+// 64-byte swizzle reads (16-byte piece j of row r at r*64 + 16*(j ^ ((r >> 1) & 3)),
+// which also spreads a quarter-warp's 16-byte writes over all banks), then one
+// lane issues the store of the box {64 bytes of columns, 32 rows} at (x, y).
+// A buffer is rewritten only once the store that last used it (EB stores
+// earlier, possibly in the previous tile) has finished reading it.
+template <int EB>
+__device__ __forceinline__ void store_tile_rows(const uint64_t (&acc)[64], const CUtensorMap *tmC,
+                                                uint32_t buf0, uint32_t lane, int col0, int y,
+                                                int N, int out_kind)
+{
+    const uint32_t sw = (lane >> 1) & 3u;
+    const bool fp32 = out_kind == OUT_FP32;
+    const bool bf = out_kind == OUT_BF16;
+    const int chunks = fp32 ? 8 : 4;
+    const int ccols = fp32 ? 16 : 32;
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-            if (col0 + 4 * c < N) {
-                float4 v;
-                unpack2f(acc[2 * c], v.x, v.y);
-                unpack2f(acc[2 * c + 1], v.z, v.w);
-                *reinterpret_cast<float4 *>(dst + 4 * c) = v;
+    for (int k = 0; k < 8; ++k) {
+        const int x = col0 + ccols * k;
+        if (k >= chunks || x >= N)
+            break;
+        const uint32_t buf = buf0 + 2048u * (k % EB);
+        if (lane == 0)
+            tma_store_wait_read_n<EB - 1>();
+        __syncwarp();
+        const uint32_t rowa = buf + lane * 64u;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            if (fp32) {
+                const uint64_t p0 = acc[8 * k + 2 * j], p1 = acc[8 * k + 2 * j + 1];
+                st_shared_v4(rowa + 16u * (j ^ sw), static_cast<uint32_t>(p0),
+                             static_cast<uint32_t>(p0 >> 32), static_cast<uint32_t>(p1),
+                             static_cast<uint32_t>(p1 >> 32));
+            } else if (k < 4) {
+                const int b = 16 * k + 4 * j;
+                st_shared_v4(rowa + 16u * (j ^ sw), pack_out2(acc[b], bf),
+                             pack_out2(acc[b + 1], bf), pack_out2(acc[b + 2], bf),
+                             pack_out2(acc[b + 3], bf));
             }
         }
-    } else {
-        uint16_t *dst = static_cast<uint16_t *>(C) + row_off + col0;
-        const bool bf = out_kind == OUT_BF16;
-#pragma unroll
-        for (int c = 0; c < 16; ++c) {
-            if (col0 + 8 * c < N) {
-                float a[8];
-#pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    unpack2f(acc[4 * c + i], a[2 * i], a[2 * i + 1]);
-                uint4 v;
-                v.x = bf ? pack_bf16x2(a[0], a[1]) : pack_f16x2(a[0], a[1]);
-                v.y = bf ? pack_bf16x2(a[2], a[3]) : pack_f16x2(a[2], a[3]);
-                v.z = bf ? pack_bf16x2(a[4], a[5]) : pack_f16x2(a[4], a[5]);
-                v.w = bf ? pack_bf16x2(a[6], a[7]) : pack_f16x2(a[6], a[7]);
-                *reinterpret_cast<uint4 *>(dst + 8 * c) = v;
-            }
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            tma_store_2d(tmC, buf, x, y);
+            tma_store_commit();
         }
     }
 }
@@ -93,15 +122,21 @@ template <int BN, int STAGES> struct TiledLayout {
     static constexpr int kBufs = 512 / BN;                  // TMEM partial buffers
     static constexpr uint32_t kTmemCols = 512;
     static constexpr size_t kStageBytes = STAGES * (kABytes + kBBytes);
+    // Epilogue buffers per promotion warp (2 KB each): with fewer pipeline
+    // stages there is room for four, so that stores never wait on each other.
+    static constexpr int kEpiBufs =
+        ((BN == 256 && STAGES <= 3) || (BN == 128 && STAGES <= 5)) ? 4 : 1;
+    static constexpr size_t kEpiBytes = 4 * kPromoWG * 2048 * kEpiBufs;
     static constexpr size_t kScaleBytes = kScaleSlots * kSlotFloats * 4;
     static constexpr int kBars = 2 * STAGES + 2 * kBufs + 2 * kScaleSlots + 1;
-    static constexpr size_t kSmem = 1024 + kStageBytes + kScaleBytes + kBars * 8 + 16;
+    static constexpr size_t kSmem =
+        1024 + kStageBytes + kEpiBytes + kScaleBytes + kBars * 8 + 16;
 };
 
 template <int BN, int STAGES>
 __global__ void __launch_bounds__(TiledLayout<BN, STAGES>::kThreads, 1)
     k_tiled(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-            const TiledParams p)
+            const __grid_constant__ CUtensorMap tmC, const TiledParams p)
 {
     using L = TiledLayout<BN, STAGES>;
     extern __shared__ uint8_t smem_raw[];
@@ -109,8 +144,10 @@ __global__ void __launch_bounds__(TiledLayout<BN, STAGES>::kThreads, 1)
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const uint32_t sA = smem_addr(smem);
     const uint32_t sB = sA + STAGES * L::kABytes;
-    float *scales = reinterpret_cast<float *>(smem + L::kStageBytes);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kStageBytes + L::kScaleBytes);
+    const uint32_t sEpi = sA + static_cast<uint32_t>(L::kStageBytes);
+    float *scales = reinterpret_cast<float *>(smem + L::kStageBytes + L::kEpiBytes);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kStageBytes + L::kEpiBytes +
+                                                  L::kScaleBytes);
     const uint32_t bar0 = smem_addr(bars);
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
     auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
@@ -146,6 +183,7 @@ __global__ void __launch_bounds__(TiledLayout<BN, STAGES>::kThreads, 1)
     if (warp == 0 && lane == 0) {
         tma_prefetch_map(&tmA);
         tma_prefetch_map(&tmB);
+        tma_prefetch_map(&tmC);
     }
     if (warp == 1) {
         tmem_alloc(smem_addr(tmem_slot), L::kTmemCols);
@@ -292,13 +330,13 @@ __global__ void __launch_bounds__(TiledLayout<BN, STAGES>::kThreads, 1)
         const int h = static_cast<int>(warp / 4) - 1;      // promotion warpgroup: column half
         const uint32_t q = warp & 3u;                      // TMEM lane quarter of this warp
         const int row = static_cast<int>(q * 32 + lane);
+        const uint32_t epi_buf = sEpi + (warp - 4u) * 2048u * L::kEpiBufs;
         uint32_t it = 0;
         int slot = 0;
         uint32_t sphase = 0;
         for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
             int mb, nb;
             tile_coords(t, p.num_m_tiles, p.num_n_tiles, mb, nb);
-            const int m = mb * 128 + row;
             const int col0 = nb * BN + h * 128;
             uint64_t acc[64];
 #pragma unroll
@@ -346,9 +384,16 @@ __global__ void __launch_bounds__(TiledLayout<BN, STAGES>::kThreads, 1)
             }
             if (!ok)
                 break;
-            if (m < p.M && col0 < p.N)
-                store_row128(acc, p.C, static_cast<size_t>(m) * p.N, col0, p.N, p.out_kind);
+            // Epilogue: this warp's 32 rows x 128 columns leave in chunks of 64
+            // bytes per row through a 2 KB shared-memory buffer (64-byte
+            // swizzle, conflict-free 16-byte writes) and asynchronous TMA stores,
+            // which write whole row segments and clip rows past M / columns past N.
+            const int y = mb * 128 + static_cast<int>(q * 32);
+            if (y < p.M && col0 < p.N)
+                store_tile_rows<L::kEpiBufs>(acc, &tmC, epi_buf, lane, col0, y, p.N, p.out_kind);
         }
+        if (lane == 0)
+            tma_store_wait_all();
     }
 
     tc_fence_before_sync();
@@ -360,8 +405,8 @@ __global__ void __launch_bounds__(TiledLayout<BN, STAGES>::kThreads, 1)
 }
 
 template <int BN, int STAGES>
-cudaError_t launch_tiled_t(const CUtensorMap &tmA, const CUtensorMap &tmB, const TiledParams &p,
-                           const LaunchCfg &cfg)
+cudaError_t launch_tiled_t(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmC,
+                           const TiledParams &p, const LaunchCfg &cfg)
 {
     using L = TiledLayout<BN, STAGES>;
     auto kernel = k_tiled<BN, STAGES>;
@@ -379,31 +424,40 @@ cudaError_t launch_tiled_t(const CUtensorMap &tmA, const CUtensorMap &tmB, const
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     lc.attrs = attr;
     lc.numAttrs = cfg.pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&lc, kernel, tmA, tmB, p);
+    return cudaLaunchKernelEx(&lc, kernel, tmA, tmB, tmC, p);
 }
 
 }  // namespace
 
+// Instantiated configurations: (BN, stages) = (256, 4), (256, 3), (128, 6), (128, 5), (128, 4).
 size_t tiled_smem_bytes(int bn, int stages)
 {
     if (bn == 256 && stages == 4)
         return TiledLayout<256, 4>::kSmem;
+    if (bn == 256 && stages == 3)
+        return TiledLayout<256, 3>::kSmem;
     if (bn == 128 && stages == 6)
         return TiledLayout<128, 6>::kSmem;
+    if (bn == 128 && stages == 5)
+        return TiledLayout<128, 5>::kSmem;
     if (bn == 128 && stages == 4)
         return TiledLayout<128, 4>::kSmem;
     return 0;
 }
 
-cudaError_t launch_tiled(const CUtensorMap &tmA, const CUtensorMap &tmB, const TiledParams &p,
-                         int bn, const LaunchCfg &cfg)
+cudaError_t launch_tiled(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmC,
+                         const TiledParams &p, int bn, const LaunchCfg &cfg)
 {
     if (bn == 256 && cfg.stages == 4)
-        return launch_tiled_t<256, 4>(tmA, tmB, p, cfg);
+        return launch_tiled_t<256, 4>(tmA, tmB, tmC, p, cfg);
+    if (bn == 256 && cfg.stages == 3)
+        return launch_tiled_t<256, 3>(tmA, tmB, tmC, p, cfg);
     if (bn == 128 && cfg.stages == 6)
-        return launch_tiled_t<128, 6>(tmA, tmB, p, cfg);
+        return launch_tiled_t<128, 6>(tmA, tmB, tmC, p, cfg);
+    if (bn == 128 && cfg.stages == 5)
+        return launch_tiled_t<128, 5>(tmA, tmB, tmC, p, cfg);
     if (bn == 128 && cfg.stages == 4)
-        return launch_tiled_t<128, 4>(tmA, tmB, p, cfg);
+        return launch_tiled_t<128, 4>(tmA, tmB, tmC, p, cfg);
     return cudaErrorInvalidValue;
 }
 

@@ -69,8 +69,10 @@ struct LaunchCfg {
 size_t tiled_smem_bytes(int bn, int stages);
 size_t swapab_smem_bytes(int mt, int stages, int groups_per_split, int out_bytes);
 
-cudaError_t launch_tiled(const CUtensorMap &tmA, const CUtensorMap &tmB, const TiledParams &p,
-                         int bn, const LaunchCfg &cfg);
+// tmC: C as a 2-D [M, N] tensor of the output type, box {64 bytes of columns,
+// 32 rows}, 64-byte swizzle (the tiled kernel's per-warp epilogue chunks).
+cudaError_t launch_tiled(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmC,
+                         const TiledParams &p, int bn, const LaunchCfg &cfg);
 // tmC: C as a 2-D [M, N] tensor of the output type, box {128 columns, mma_n rows},
 // no swizzle (used by the epilogue's TMA store when splits == 1).
 cudaError_t launch_swapab(const CUtensorMap &tmW, const CUtensorMap &tmX, const CUtensorMap &tmC,

@@ -179,6 +179,11 @@ __device__ __forceinline__ void tma_store_wait_read()
 {
     asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
+// Wait until at most N committed bulk stores are still reading shared memory.
+template <int N> __device__ __forceinline__ void tma_store_wait_read_n()
+{
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
 // Wait until every committed bulk store has completed its global writes.
 __device__ __forceinline__ void tma_store_wait_all()
 {
