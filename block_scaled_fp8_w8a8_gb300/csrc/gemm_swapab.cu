@@ -182,6 +182,8 @@ __global__ void __launch_bounds__(SwapLayout<MT>::kThreads, 1)
                     phase ^= 1u;
                 }
             }
+            const int next_stage = stage;       // ring position after the last issue
+            const uint32_t next_phase = phase;
             if (ok) {
                 // Tail: wait until the MMA has released every stage, so that no
                 // commit arrives on this CTA's shared memory after it exits.
@@ -192,13 +194,15 @@ __global__ void __launch_bounds__(SwapLayout<MT>::kThreads, 1)
                         phase ^= 1u;
                     }
                 }
-            } else {
-                // Drain: wait for the loads still landing in this CTA's shared memory.
+            }
+            if (!ok) {
+                // Drain: wait for the loads still landing in this CTA's shared memory
+                // (the last issue into each stage; stages never issued are skipped).
                 for (int s = 0; s < stages; ++s) {
-                    const bool this_round = s < stage;
+                    const bool this_round = s < next_stage;
                     if (!this_round && issued < stages && s >= issued)
                         continue;
-                    wait_drain(full_bar(s), this_round ? phase : (phase ^ 1u), p.status,
+                    wait_drain(full_bar(s), this_round ? next_phase : (next_phase ^ 1u), p.status,
                                p.wait_limit, (SITE_DRAIN << 8) | 4u);
                 }
             }
