@@ -11,10 +11,11 @@ Hopper" (FlagGems-vllm PR #693, Performance).
 
 Timing: every step reads a different input set out of a rotation whose total
 size exceeds twice the L2 cache, so each step streams its operands from HBM.
-Each step is one CUDA-graph replay of the workload's kernel launches; K steps
-are bracketed by a barrier and torch.cuda.synchronize() and timed with CUDA
-events; the K-step block is repeated until about a second has been timed and
-the median block is reported.  nvidia-smi samples the clocks meanwhile.
+The K timed steps are captured as one CUDA graph (kernels chained with
+programmatic dependent launch); each replay of it is bracketed by a barrier
+and torch.cuda.synchronize() and timed with CUDA events; replays are repeated
+until about a second has been timed and the median is reported.  nvidia-smi
+samples the clocks meanwhile.
 
 Under torchrun (N > 1) every rank runs the same workload on its own GPU as an
 independent replica (the operator has no exchange step); the reported time is
@@ -188,7 +189,7 @@ class ClockSampler:
 # ---------------------------------------------------------------------- our implementation
 
 class Workload:
-    """Device-resident rotating input sets and one CUDA graph per set."""
+    """Device-resident rotating input sets and the graphs that replay them."""
 
     def __init__(self, name, out_dtype, l2_bytes, shapes=None):
         import block_scaled_fp8_w8a8_gb300 as w8
@@ -220,7 +221,6 @@ class Workload:
                 nb = plan.workspace_bytes
                 row.append(torch.zeros(max(nb, 256), dtype=torch.uint8, device="cuda") if nb else None)
             self.ws.append(row)
-        self.graphs = []
 
     def launch(self, r, i, stream):
         (A, a_s, B, b_s), C = self.data[r][i]
@@ -240,18 +240,21 @@ class Workload:
         for i in range(len(self.shapes)):
             self.launch(r, i, stream)
 
-    def capture(self):
+    def capture(self, steps):
+        """One CUDA graph holding exactly `steps` consecutive steps (step k reads
+        input set k mod sets), so that kernels of successive steps follow each
+        other with programmatic dependent launch and no graph-launch gap."""
         stream = torch.cuda.Stream()
         torch.cuda.synchronize()
         for r in range(self.sets):          # warm every set once outside capture
             self.step_eager(r, stream)
         stream.synchronize()
-        for r in range(self.sets):
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=stream):
-                self.step_eager(r, torch.cuda.current_stream())
-            self.graphs.append(g)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for k in range(steps):
+                self.step_eager(k % self.sets, torch.cuda.current_stream())
         torch.cuda.synchronize()
+        return g
 
     def capture_single(self, i, count):
         """A graph of `count` launches of shape i, rotating over the sets."""
@@ -295,18 +298,19 @@ def run_ours(args, rank, world):
     if args.shapes:
         override = [tuple(int(v) for v in s.split("x")) for s in args.shapes.split(",")]
     wl = Workload(args.workload, args.out_dtype, l2, override)
-    wl.capture()
+    warm_graph = wl.capture(max(1, args.warmup))
+    timed_graph = wl.capture(args.steps)
     shapes = wl.shapes
     flops, nbytes = workload_units(shapes, wl.out_bytes)
     bound = bound_of(shapes)
 
-    for k in range(args.warmup):
-        wl.graphs[k % wl.sets].replay()
+    warm_graph.replay()                      # the W untimed warm-up steps
     torch.cuda.synchronize()
 
+    # Each timed block is one replay of the K-step graph, i.e. exactly K steps.
     with ClockSampler(dev) as clk:
-        t_step_blocks, nblocks = time_blocks(lambda k: wl.graphs[k % wl.sets].replay(),
-                                             args.steps, world, args.min_seconds)
+        t_step_blocks, nblocks = time_blocks(lambda k: timed_graph.replay(), 1, world,
+                                             args.min_seconds)
     clocks = clk.summary()
     t_step = t_step_blocks / args.steps
 
@@ -362,7 +366,7 @@ def run_ours(args, rank, world):
         "data": "synthetic (seeded N(0,1), block-quantised to E4M3 with amax/448 scales)",
         "config": {"workload": args.workload, "shapes": [list(s) for s in shapes],
                    "l2": f"rotating {wl.sets} input sets of {nbytes / 1e6:.2f} MB (> 2x L2 "
-                         f"{l2 / 1e6:.0f} MB); CUDA-graph replay per step",
+                         f"{l2 / 1e6:.0f} MB); the K timed steps are one CUDA graph",
                    "timed_blocks": nblocks, "parallelism": f"replicas x{world}",
                    "launch": "pdl=1, weights_static=1 (B streamed before the predecessor finishes)"},
         "gpu_launches": args.steps * len(shapes),

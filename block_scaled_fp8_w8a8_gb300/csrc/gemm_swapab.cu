@@ -139,8 +139,12 @@ __global__ void __launch_bounds__(SwapLayout<MT>::kThreads, 1)
     const WaitGuard guard{abort_flag, p.status, p.wait_limit};
 
     grid_launch_dependents();
-    if (!is_producer)
-        grid_dependency_wait();     // the producer waits after its weight prefetch
+    // Warp 0 holds the producer; its lane 0 waits for the previous grid only
+    // after issuing the weight prefetch.  The whole warp skips this wait (its
+    // other lanes touch no memory): were lanes 1..31 to wait here, the warp
+    // would reconverge behind them and the prefetch would wait too.
+    if (warp != 0)
+        grid_dependency_wait();
 
     if (warp < 4) {
         if constexpr (L::kPromoWG == 2)
