@@ -70,6 +70,30 @@ def parse():
     return ap.parse_args()
 
 
+def source_digest() -> str:
+    """sha256 over the CUDA sources (first 16 hex digits): identifies the kernel build
+    that a recorded ncu traffic figure belongs to."""
+    import hashlib
+    csrc = os.path.join(ROOT, "block_scaled_fp8_w8a8_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h", ".inc")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+# DRAM bytes (read + write) of one launch, from an ncu capture of the kernel build
+# with the given source digest: (digest, "MxNxK", output bytes) -> bytes.  A figure
+# whose kernel sources have changed since is not reported (the key no longer matches).
+MEASURED_TRAFFIC = {
+    # profiles/k_swapab_decode_m214.md: read 1.159 MB, write 0 (C stays in L2 within the launch)
+    ("977f9d0fc575f7b5", "214x4096x256", 2): 1159424,
+    # profiles/k_tiled_prefill_16384x4096x4096.md: read 97.27 MB + write 99.67 MB
+    ("977f9d0fc575f7b5", "16384x4096x4096", 2): 196937216,
+}
+
+
 def peaks():
     try:
         with open(PEAKS_FILE) as f:
@@ -346,8 +370,16 @@ def run_ours(args, rank, world):
         achieved = d["tflops"]
         peak = 2.0 * bf16          # dense FP8 = 2 x the measured bf16 rate (nominal ratio)
         unit = "TFLOP/s"
+    shape_key = f"{d['M']}x{d['N']}x{d['K']}"
+    traffic = MEASURED_TRAFFIC.get((source_digest(), shape_key, wl.out_bytes))
     roofline = {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
-                "frac": round(achieved / peak, 4), "traffic": None,
+                "frac": round(achieved / peak, 4),
+                "traffic": traffic,
+                "traffic_source": ("ncu dram__bytes_read.sum + dram__bytes_write.sum of one launch "
+                                   "(profiles/)" if traffic is not None else
+                                   "none for this kernel build"),
+                "algorithmic_bytes": synth.algorithmic_bytes(d["M"], d["N"], d["K"], wl.out_bytes)
+                if per_shape else nbytes,
                 "kernel": f"M={d['M']} N={d['N']} K={d['K']} ({d['variant']})",
                 "peak_source": f"{peak_kind}" + (" (bf16 x 2, nominal fp8/bf16 ratio)" if bound == "tensor" else "")}
 
