@@ -183,7 +183,7 @@ w8a8_status check_options(const w8a8_options *o)
 {
     if (!o)
         return W8A8_OK;
-    if (o->variant < W8A8_VARIANT_AUTO || o->variant > W8A8_VARIANT_SPLITK)
+    if (o->variant < W8A8_VARIANT_AUTO || o->variant > W8A8_VARIANT_SPLITK_CLUSTER)
         return fail(W8A8_ERR_INVALID_ARG, "unknown variant %d", o->variant);
     if (o->split_k < 0 || o->stages < 0 || o->stages > 8 || o->grid_limit < 0 || o->m_tile < 0 ||
         o->debug_skip_load < 0)
@@ -207,6 +207,7 @@ struct Plan {
     int stages;
     int grid;         // tiled: persistent CTAs
     int mma_n, mt, m_tiles, splits, gps;   // swap family
+    int tile_bytes;                        // swap family: bytes per staged C-tile element
     size_t smem;
 };
 
@@ -277,23 +278,28 @@ w8a8_status make_plan(int64_t M, int64_t N, int64_t K, int out_bytes, const w8a8
     mma_n = std::max(mma_n, 16);
     const int mt = mt_for(mma_n);
     int splits = 1;
-    if (variant == W8A8_VARIANT_SPLITK) {
+    const bool cluster = variant == W8A8_VARIANT_SPLITK_CLUSTER;
+    if (variant == W8A8_VARIANT_SPLITK || cluster) {
         if (split_hint) {
             splits = split_hint;
         } else {
             const int64_t ctas = static_cast<int64_t>(NB) * m_tiles;
             splits = static_cast<int>(std::max<int64_t>(2, dev.sm_count / std::max<int64_t>(ctas, 1)));
-            splits = std::min(splits, 16);
+            splits = std::min(splits, cluster ? 8 : 16);
         }
         splits = std::min(std::max(splits, 1), G);
+        if (cluster && splits > 16)
+            return fail(W8A8_ERR_UNSUPPORTED, "a cluster split-K holds at most 16 splits");
     }
     int gps = static_cast<int>(cdiv(G, splits));
     splits = static_cast<int>(cdiv(G, gps));       // every split non-empty
+    // The cluster reduction stages an fp32 partial tile in shared memory.
+    const int tile_bytes = (cluster && splits > 1) ? 4 : out_bytes;
     int max_stages = std::min(8, gps);
     int stages = stage_hint ? std::min(stage_hint, max_stages) : max_stages;
-    while (stages > 1 && swapab_smem_bytes(mt, stages, gps, out_bytes) > dev.smem_optin)
+    while (stages > 1 && swapab_smem_bytes(mt, stages, gps, tile_bytes) > dev.smem_optin)
         --stages;
-    if (stages < 2 && gps > 1 && swapab_smem_bytes(mt, 2, gps, out_bytes) > dev.smem_optin)
+    if (swapab_smem_bytes(mt, stages, gps, tile_bytes) > dev.smem_optin)
         return fail(W8A8_ERR_UNSUPPORTED,
                     "K=%lld is too long for one swap-AB CTA; use the split-K variant",
                     (long long)K);
@@ -303,7 +309,8 @@ w8a8_status make_plan(int64_t M, int64_t N, int64_t K, int out_bytes, const w8a8
     pl->splits = splits;
     pl->gps = gps;
     pl->stages = stages;
-    pl->smem = swapab_smem_bytes(mt, stages, gps, out_bytes);
+    pl->smem = swapab_smem_bytes(mt, stages, gps, tile_bytes);
+    pl->tile_bytes = tile_bytes;
     if (splits == 1)
         pl->variant = W8A8_VARIANT_SWAPAB;
     return W8A8_OK;
@@ -464,7 +471,8 @@ w8a8_status run(const void *A, const float *a_s, const void *B, const float *b_s
         p.splits = pl.splits;
         p.groups_per_split = pl.gps;
         p.out_kind = out;
-        p.out_bytes = out == W8A8_OUT_FP32 ? 4 : 2;
+        p.out_bytes = pl.tile_bytes;
+        p.cluster_reduce = (pl.variant == W8A8_VARIANT_SPLITK_CLUSTER && pl.splits > 1) ? 1 : 0;
         p.prefetch_weights = (o && o->pdl && o->weights_static) ? 1 : 0;
         p.debug_skip_tma = debug_skip;
         p.status = info.status;

@@ -35,6 +35,9 @@ template <int MT> struct SwapLayout {
     static constexpr int kPromoWG = MT > 128 ? 2 : 1;
     static constexpr int kCols = MT / kPromoWG;      // token columns per promotion thread
     static constexpr int kThreads = 128 + 128 * kPromoWG;
+    // Small token tiles run many CTAs per problem: keep two resident per SM
+    // (at most 128 registers per thread).
+    static constexpr int kMinBlocks = MT <= 64 ? 2 : 1;
     static constexpr uint32_t kWBytes = 128u * 128u;
     static constexpr uint32_t kXBytes = static_cast<uint32_t>(MT) * 128u;
     static constexpr uint32_t kTmemCols = 2 * MT < 32 ? 32 : 2 * MT;
@@ -78,7 +81,7 @@ __device__ __forceinline__ void add4(float4 &a, const float4 &b)
 }
 
 template <int MT>
-__global__ void __launch_bounds__(SwapLayout<MT>::kThreads, 1)
+__global__ void __launch_bounds__(SwapLayout<MT>::kThreads, SwapLayout<MT>::kMinBlocks)
     k_swapab(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
              const __grid_constant__ CUtensorMap tmC, const SwapParams p, const int stages)
 {
@@ -148,7 +151,7 @@ __global__ void __launch_bounds__(SwapLayout<MT>::kThreads, 1)
 
     if (warp < 4) {
         if constexpr (L::kPromoWG == 2)
-            regs_dealloc<40>();
+            regs_dealloc<56>();     // 128 x 56 + 256 x 224 = 384 x 168 (the launch's registers)
         if (is_producer) {
             // ---------------------------------------------------------- TMA producer
             const uint32_t tx = L::kWBytes + static_cast<uint32_t>(p.mma_n) * 128u;
@@ -247,7 +250,7 @@ __global__ void __launch_bounds__(SwapLayout<MT>::kThreads, 1)
     } else {
         // -------------------------------------------------------------- promotion + epilogue
         if constexpr (L::kPromoWG == 2)
-            regs_alloc<232>();
+            regs_alloc<224>();
         const int tid = static_cast<int>(threadIdx.x) - 128;
         constexpr int kPromoThreads = 128 * L::kPromoWG;
         const int h = tid / 128;                             // column half
@@ -340,6 +343,16 @@ __global__ void __launch_bounds__(SwapLayout<MT>::kThreads, 1)
                 tma_store_commit();
                 tma_store_wait_all();
             }
+        } else if (p.cluster_reduce) {
+            // Cluster split-K: this split's fp32 partial tile [mma_n rows][128]
+            // goes to this CTA's own (now idle) stage area; the reduction below
+            // reads it from the other CTAs of the cluster.  (After a timeout the
+            // tile is garbage and the status word already reports the failure.)
+            float *tile = reinterpret_cast<float *>(smem);
+#pragma unroll
+            for (int j = 0; j < L::kCols; ++j)
+                if (c0 + j < p.mma_n)
+                    tile[(c0 + j) * 128 + row] = acc[j];
         } else if (ok) {
             // Deterministic split-K: publish this split's partial tile, take a
             // ticket; the last arrival sums the splits in order 0..S-1.
@@ -393,6 +406,47 @@ __global__ void __launch_bounds__(SwapLayout<MT>::kThreads, 1)
         }
     }
 
+    if (p.cluster_reduce) {
+        // Every thread of every CTA of the cluster passes both barriers exactly once.
+        cluster_sync();                      // all partial tiles are in shared memory
+        if (warp >= 4) {
+            // This CTA (cluster rank r of S) reduces rows [r0, r1) of the tile:
+            // items of 4 consecutive columns, consecutive threads on consecutive
+            // items, the S partials summed in rank order 0..S-1 (the same order,
+            // and so the same bits, as the workspace reduction).
+            uint32_t rank;
+            asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(rank));
+            const int tid = static_cast<int>(threadIdx.x) - 128;
+            constexpr int kPromoThreads = 128 * L::kPromoWG;
+            const int rows = min(p.mma_n, p.M - m0);
+            const int r0 = rows * static_cast<int>(rank) / p.splits;
+            const int r1 = rows * (static_cast<int>(rank) + 1) / p.splits;
+            const int c4n = min(128, p.N - nb * 128) / 4;
+            const int items = (r1 - r0) * c4n;
+            const uint32_t tile = smem_addr(smem);
+            for (int it = tid; it < items; it += kPromoThreads) {
+                const int r = r0 + it / c4n, c4 = it % c4n;
+                const uint32_t local = tile + static_cast<uint32_t>(r * 128 + 4 * c4) * 4u;
+                float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
+                int s = 0;
+                for (; s + 8 <= p.splits; s += 8) {
+                    float4 v[8];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u)
+                        v[u] = ld_cluster_f4(cluster_map(local, static_cast<uint32_t>(s + u)));
+#pragma unroll
+                    for (int u = 0; u < 8; ++u)
+                        add4(sum, v[u]);
+                }
+                for (; s < p.splits; ++s)
+                    add4(sum, ld_cluster_f4(cluster_map(local, static_cast<uint32_t>(s))));
+                store4(p.C, static_cast<size_t>(m0 + r) * p.N + nb * 128 + 4 * c4, sum,
+                       p.out_kind);
+            }
+        }
+        cluster_sync();                      // no CTA leaves while its tile is being read
+    }
+
     tc_fence_before_sync();
     __syncthreads();
     if (warp == 1) {
@@ -417,11 +471,35 @@ cudaError_t launch_swapab_t(const CUtensorMap &tmW, const CUtensorMap &tmX, cons
     lc.blockDim = dim3(L::kThreads, 1, 1);
     lc.dynamicSmemBytes = smem;
     lc.stream = cfg.stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchAttribute attr[2];
+    unsigned n = 0;
+    if (cfg.pdl) {
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
+    if (p.cluster_reduce) {
+        // The splits of one tile form a cluster along grid.y.
+        if (p.splits > 8) {
+            static volatile int wide_set[kMaxDeviceFlags] = {};
+            int dev = 0;
+            if ((e = cudaGetDevice(&dev)) != cudaSuccess)
+                return e;
+            if (dev >= 0 && dev < kMaxDeviceFlags && !wide_set[dev]) {
+                e = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+                if (e != cudaSuccess)
+                    return e;
+                wide_set[dev] = 1;
+            }
+        }
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = 1;
+        attr[n].val.clusterDim.y = static_cast<unsigned>(p.splits);
+        attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
     lc.attrs = attr;
-    lc.numAttrs = cfg.pdl ? 1 : 0;
+    lc.numAttrs = n;
     return cudaLaunchKernelEx(&lc, kernel, tmW, tmX, tmC, p, cfg.stages);
 }
 

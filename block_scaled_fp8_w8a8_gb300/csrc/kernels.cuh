@@ -51,8 +51,11 @@ struct SwapParams {
     int splits;
     int groups_per_split;
     int out_kind;
-    int out_bytes;         // 2 (bf16, fp16) or 4 (fp32)
+    int out_bytes;         // bytes per element of the C tile staged in shared memory:
+                           // the output's (2 or 4), or 4 for the cluster reduction
     int prefetch_weights;  // start the B loads before waiting on the previous grid
+    int cluster_reduce;    // splits > 1: the grid.y CTAs of a tile form one cluster and
+                           // reduce their partial tiles through distributed shared memory
     int debug_skip_tma;
     unsigned *status;
     unsigned long long wait_limit;

@@ -319,6 +319,36 @@ __device__ __forceinline__ void tmem_load_64cols(uint32_t taddr, uint32_t (&r)[6
                  : "memory");
 }
 
+// ------------------------------------------------------------------ thread-block clusters
+
+// Cluster-wide barrier; every thread of every CTA of the cluster must call it
+// (warp-uniformly).  Release/acquire order shared-memory writes before it with
+// reads of them by other CTAs after it.
+__device__ __forceinline__ void cluster_sync()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Address, in the cluster's shared window, of the same shared-memory location
+// in the CTA of cluster rank `rank`.
+__device__ __forceinline__ uint32_t cluster_map(uint32_t saddr, uint32_t rank)
+{
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ float4 ld_cluster_f4(uint32_t caddr)
+{
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(caddr)
+                 : "memory");
+    return v;
+}
+
 // ------------------------------------------------------------------ paired fp32 arithmetic
 
 __device__ __forceinline__ uint64_t pack2(uint32_t lo, uint32_t hi)

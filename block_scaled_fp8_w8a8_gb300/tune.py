@@ -51,6 +51,9 @@ def candidates(M, N, K):
             for s in (2, 3, 4, 6, 8, 12, 16, 32):
                 if s <= G and -(-G // -(-G // s)) == s:
                     out.append(dict(variant=b.W8A8_VARIANT_SPLITK, m_tile=mt, split_k=s))
+                    if s <= 16:
+                        out.append(dict(variant=b.W8A8_VARIANT_SPLITK_CLUSTER, m_tile=mt,
+                                        split_k=s))
     return out
 
 
@@ -125,7 +128,11 @@ def main():
         bench = Bench(M, N, K, l2)
         rows = []
         for cfg in candidates(M, N, K):
-            us, plan = bench.time(cfg)
+            try:
+                us, plan = bench.time(cfg)
+            except b.W8A8Error as e:        # e.g. a cluster that cannot be scheduled
+                print(f"  skip {cfg}: {e}", flush=True)
+                continue
             if us is None:
                 continue
             rows.append({"cfg": cfg, "us": us, "variant": plan.variant, "split_k": plan.split_k,

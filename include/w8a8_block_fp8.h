@@ -71,7 +71,12 @@ typedef enum {
     W8A8_VARIANT_AUTO = 0,
     W8A8_VARIANT_TILED = 1,   /* tokens on the MMA M side: 128 x BN tiles, for large M       */
     W8A8_VARIANT_SWAPAB = 2,  /* C^T = B A^T: 128 weight rows per MMA, tokens on MMA N       */
-    W8A8_VARIANT_SPLITK = 3   /* swap-AB with the K groups split over CTAs + ordered reduce */
+    W8A8_VARIANT_SPLITK = 3,  /* swap-AB with the K groups split over CTAs + ordered reduce
+                                 through a global workspace                                 */
+    W8A8_VARIANT_SPLITK_CLUSTER = 4  /* swap-AB split-K whose splits of a tile form one
+                                        thread-block cluster (2..16 CTAs) and reduce their
+                                        partials in rank order through distributed shared
+                                        memory: no workspace; same bits as SPLITK          */
 } w8a8_variant;
 
 /*

@@ -196,3 +196,30 @@ def test_splitk_workspace_reused_across_shapes():
                 workspace_dev=ws.data_ptr(), workspace_bytes=nbytes)
         assert_close(C, ref, what=f"reuse {M}x{N}x{K}")
     assert torch.count_nonzero(ws[:65536 * 4]) == 0
+
+
+@pytest.mark.parametrize("M,N,K,splits", [(16, 512, 4096, 8), (64, 512, 4096, 4), (158, 512, 4096, 8),
+                                          (7, 144, 384, 3), (300, 256, 2048, 2), (1, 8192, 1024, 2),
+                                          (70, 512, 4096, 16)])
+def test_cluster_splitk_matches_oracle_and_workspace_variant(M, N, K, splits):
+    """The cluster split-K (partials reduced through distributed shared memory)
+    agrees with the oracle, and bit for bit with the workspace split-K of the same
+    split count (both sum the splits in order 0..S-1)."""
+    x = synth.make_inputs(M, N, K, seed=M * 7 + splits, outlier_p=1e-3)
+    ref = oracle.reference_c(x.A, x.a_s, x.B, x.b_s)
+    for out in ("fp32", "bf16"):
+        Cc = run(x, out, variant=w8.W8A8_VARIANT_SPLITK_CLUSTER, split_k=splits)
+        Cw = run(x, out, variant=w8.W8A8_VARIANT_SPLITK, split_k=splits)
+        assert_close(Cc, ref, what=f"cluster {M}x{N}x{K} S={splits} {out}")
+        assert torch.equal(Cc.view(torch.int16 if out == "bf16" else torch.int32),
+                           Cw.view(torch.int16 if out == "bf16" else torch.int32))
+
+
+def test_cluster_splitk_deterministic():
+    x = synth.make_inputs(158, 512, 4096, seed=0, outlier_p=1e-3)
+    A, a_s, B, b_s = to_device(x)
+    outs = [w8.matmul(A, a_s, B, b_s, out_dtype="fp32", variant=w8.W8A8_VARIANT_SPLITK_CLUSTER,
+                      split_k=8) for _ in range(5)]
+    torch.cuda.synchronize()
+    for o in outs[1:]:
+        assert torch.equal(o.view(torch.int32), outs[0].view(torch.int32))
