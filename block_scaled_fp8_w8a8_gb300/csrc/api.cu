@@ -167,13 +167,17 @@ w8a8_status check_problem(int64_t M, int64_t N, int64_t K, int block_n, int bloc
     if (block_n != 128 || block_k != 128)
         return fail(W8A8_ERR_UNSUPPORTED, "block_n=%d block_k=%d: only [128, 128] scale blocks",
                     block_n, block_k);
-    if (N < 1 || K < 128)
-        return fail(W8A8_ERR_UNSUPPORTED, "N=%lld K=%lld: need N >= 1 and K >= 128",
+    if (N < 1 || K < 16)
+        return fail(W8A8_ERR_UNSUPPORTED, "N=%lld K=%lld: need N >= 1 and K >= 16",
                     (long long)N, (long long)K);
-    if (K % 128 != 0)
-        return fail(W8A8_ERR_UNSUPPORTED, "K=%lld is not a multiple of 128", (long long)K);
-    if (N % 16 != 0)
-        return fail(W8A8_ERR_UNSUPPORTED, "N=%lld is not a multiple of 16", (long long)N);
+    // Rows of A and B, and of C, must start on 16-byte boundaries (TMA strides).
+    // A last K group shorter than 128 is read zero-padded by the TMA.
+    if (K % 16 != 0)
+        return fail(W8A8_ERR_UNSUPPORTED, "K=%lld is not a multiple of 16", (long long)K);
+    const int n_align = out == W8A8_OUT_FP32 ? 4 : 8;
+    if (N % n_align != 0)
+        return fail(W8A8_ERR_UNSUPPORTED, "N=%lld is not a multiple of %d for this output type",
+                    (long long)N, n_align);
     if (M > (1ll << 31) - 1 || N > (1ll << 31) - 1 || K > (1ll << 31) - 1)
         return fail(W8A8_ERR_UNSUPPORTED, "sizes must be below 2^31");
     return W8A8_OK;
@@ -188,8 +192,9 @@ w8a8_status check_options(const w8a8_options *o)
     if (o->split_k < 0 || o->stages < 0 || o->stages > 8 || o->grid_limit < 0 || o->m_tile < 0 ||
         o->debug_skip_load < 0)
         return fail(W8A8_ERR_INVALID_ARG, "negative or out-of-range option");
-    if (o->block_n_tile != 0 && o->block_n_tile != 128 && o->block_n_tile != 256)
-        return fail(W8A8_ERR_INVALID_ARG, "block_n_tile must be 0, 128 or 256");
+    if (o->block_n_tile != 0 && o->block_n_tile != 128 && o->block_n_tile != 192 &&
+        o->block_n_tile != 256)
+        return fail(W8A8_ERR_INVALID_ARG, "block_n_tile must be 0, 128, 192 or 256");
     if (o->m_tile != 0 && (o->m_tile % 16 != 0 || o->m_tile > 256))
         return fail(W8A8_ERR_INVALID_ARG, "m_tile must be a multiple of 16 up to 256");
     return W8A8_OK;
@@ -214,7 +219,7 @@ struct Plan {
 w8a8_status make_plan(int64_t M, int64_t N, int64_t K, int out_bytes, const w8a8_options *o,
                       const DeviceInfo &dev, Plan *pl)
 {
-    const int G = static_cast<int>(K / 128);
+    const int G = static_cast<int>(cdiv(K, 128));
     const int NB = static_cast<int>(cdiv(N, 128));
     std::memset(pl, 0, sizeof(*pl));
     int variant = o ? o->variant : W8A8_VARIANT_AUTO;
@@ -237,8 +242,8 @@ w8a8_status make_plan(int64_t M, int64_t N, int64_t K, int out_bytes, const w8a8
             // tiles alone cannot fill half the SMs.
             variant = W8A8_VARIANT_SWAPAB;
             const int64_t ctas = NB * cdiv(M, M <= 16 ? 16 : 32);
-            if (ctas * 2 <= dev.sm_count && G >= 16)
-                variant = W8A8_VARIANT_SPLITK;
+            if (ctas * 2 <= dev.sm_count && G >= 4)
+                variant = W8A8_VARIANT_SPLITK_CLUSTER;
         } else {
             variant = W8A8_VARIANT_TILED;
         }
@@ -247,8 +252,9 @@ w8a8_status make_plan(int64_t M, int64_t N, int64_t K, int out_bytes, const w8a8
 
     if (variant == W8A8_VARIANT_TILED) {
         int bn = bn_hint ? bn_hint : (N % 256 == 0 ? 256 : 128);
-        int stages = bn == 256 ? (stage_hint == 3 ? 3 : 4)
-                               : ((stage_hint == 4 || stage_hint == 5) ? stage_hint : 6);
+        int stages = bn == 256   ? (stage_hint == 3 ? 3 : 4)
+                     : bn == 192 ? 4
+                                 : ((stage_hint == 4 || stage_hint == 5) ? stage_hint : 6);
         const int64_t tiles = cdiv(M, 128) * cdiv(N, bn);
         int64_t grid = std::min<int64_t>(tiles, dev.sm_count);
         if (o && o->grid_limit)
@@ -394,7 +400,7 @@ w8a8_status run(const void *A, const float *a_s, const void *B, const float *b_s
     if ((st = make_plan(M, N, K, out == W8A8_OUT_FP32 ? 4 : 2, o, info, &pl)) != W8A8_OK)
         return st;
 
-    const int G = static_cast<int>(K / 128);
+    const int G = static_cast<int>(cdiv(K, 128));
     const int NB = static_cast<int>(cdiv(N, 128));
     const unsigned long long limit =
         (o && o->wait_limit_cycles) ? o->wait_limit_cycles : kDefaultWaitLimit;
@@ -520,7 +526,7 @@ size_t w8a8_block_fp8_host_staging_size(int64_t M, int64_t N, int64_t K, w8a8_ou
 {
     if (check_problem(M, N, K, 128, 128, out) != W8A8_OK)
         return 0;
-    const int64_t G = K / 128;
+    const int64_t G = cdiv(K, 128);
     auto up = [](size_t x) { return (x + 255) / 256 * 256; };
     const size_t ob = out == W8A8_OUT_FP32 ? 4 : 2;
     return up(M * K) + up(M * G * 4) + up(N * K) + up(cdiv(N, 128) * G * 4) + up(M * N * ob);
@@ -545,7 +551,7 @@ w8a8_status w8a8_block_fp8_matmul_host(const void *A_host, const float *a_s_host
     if (staging_bytes < need || !aligned(staging_dev, 256))
         return fail(W8A8_ERR_WORKSPACE, "staging of %zu bytes: need %zu, 256-byte aligned",
                     staging_bytes, need);
-    const int64_t G = K / 128;
+    const int64_t G = cdiv(K, 128);
     auto up = [](size_t x) { return (x + 255) / 256 * 256; };
     const size_t ob = out_dtype == W8A8_OUT_FP32 ? 4 : 2;
     char *p = static_cast<char *>(staging_dev);

@@ -341,7 +341,7 @@ __global__ void __launch_bounds__(SwapLayout<MT>::kThreads, SwapLayout<MT>::kMin
             if (tid == 0) {
                 tma_store_2d(&tmC, sW, nb * 128, m0);
                 tma_store_commit();
-                tma_store_wait_all();
+                tma_store_wait_read();      // the tile's shared memory may be released
             }
         } else if (p.cluster_reduce) {
             // Cluster split-K: this split's fp32 partial tile [mma_n rows][128]

@@ -63,26 +63,26 @@ __device__ __forceinline__ uint32_t pack_out2(uint64_t pair, bool bf)
     return bf ? pack_bf16x2(lo, hi) : pack_f16x2(lo, hi);
 }
 
-// Epilogue of one warp: its 32 rows (lane = row) x 128 accumulator columns
-// (64 fp32 pairs) go out in chunks of 64 bytes per row.  Each chunk is written
+// Epilogue of one warp: its 32 rows (lane = row) x 2*NP accumulator columns
+// (NP fp32 pairs) go out in chunks of 64 bytes per row.  Each chunk is written
 // to one of the warp's EB buffers of 2 KB in the layout a TMA store with the
 // 64-byte swizzle reads (16-byte piece j of row r at r*64 + 16*(j ^ ((r >> 1) & 3)),
 // which also spreads a quarter-warp's 16-byte writes over all banks), then one
 // lane issues the store of the box {64 bytes of columns, 32 rows} at (x, y).
 // A buffer is rewritten only once the store that last used it (EB stores
 // earlier, possibly in the previous tile) has finished reading it.
-template <int EB>
-__device__ __forceinline__ void store_tile_rows(const uint64_t (&acc)[64], const CUtensorMap *tmC,
+template <int NP, int EB>
+__device__ __forceinline__ void store_tile_rows(const uint64_t (&acc)[NP], const CUtensorMap *tmC,
                                                 uint32_t buf0, uint32_t lane, int col0, int y,
                                                 int N, int out_kind)
 {
     const uint32_t sw = (lane >> 1) & 3u;
     const bool fp32 = out_kind == OUT_FP32;
     const bool bf = out_kind == OUT_BF16;
-    const int chunks = fp32 ? 8 : 4;
+    const int chunks = fp32 ? NP / 8 : NP / 16;
     const int ccols = fp32 ? 16 : 32;
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
+    for (int k = 0; k < NP / 8; ++k) {
         const int x = col0 + ccols * k;
         if (k >= chunks || x >= N)
             break;
@@ -98,7 +98,7 @@ __device__ __forceinline__ void store_tile_rows(const uint64_t (&acc)[64], const
                 st_shared_v4(rowa + 16u * (j ^ sw), static_cast<uint32_t>(p0),
                              static_cast<uint32_t>(p0 >> 32), static_cast<uint32_t>(p1),
                              static_cast<uint32_t>(p1 >> 32));
-            } else if (k < 4) {
+            } else if (k < NP / 16) {
                 const int b = 16 * k + 4 * j;
                 st_shared_v4(rowa + 16u * (j ^ sw), pack_out2(acc[b], bf),
                              pack_out2(acc[b + 1], bf), pack_out2(acc[b + 2], bf),
@@ -114,31 +114,38 @@ __device__ __forceinline__ void store_tile_rows(const uint64_t (&acc)[64], const
     }
 }
 
-template <int BN, int STAGES> struct TiledLayout {
-    static constexpr int kPromoWG = BN / 128;
+// BN output columns per tile, STAGES shared-memory stages, CPW columns per
+// promotion warpgroup (64 or 128: 64 needs one TMEM load round trip per group
+// and thread, 128 two), EB epilogue buffers of 2 KB per promotion warp.
+template <int BN, int STAGES, int CPW, int EB> struct TiledLayout {
+    static constexpr int kPromoWG = BN / CPW;
+    static constexpr int kPairs = CPW / 2;                  // fp32 accumulator pairs per thread
     static constexpr int kThreads = 128 + 128 * kPromoWG;
     static constexpr uint32_t kABytes = 128u * 128u;
     static constexpr uint32_t kBBytes = static_cast<uint32_t>(BN) * 128u;
     static constexpr int kBufs = 512 / BN;                  // TMEM partial buffers
     static constexpr uint32_t kTmemCols = 512;
     static constexpr size_t kStageBytes = STAGES * (kABytes + kBBytes);
-    // Epilogue buffers per promotion warp (2 KB each): with fewer pipeline
-    // stages there is room for four, so that stores never wait on each other.
-    static constexpr int kEpiBufs =
-        ((BN == 256 && STAGES <= 3) || (BN == 128 && STAGES <= 5)) ? 4 : 1;
+    static constexpr int kEpiBufs = EB;
     static constexpr size_t kEpiBytes = 4 * kPromoWG * 2048 * kEpiBufs;
+    // setmaxnreg split (registers per thread) between the first warpgroup
+    // (producer, MMA issuer, scale loader) and the promotion warpgroups; the
+    // sum over all threads equals the launch's registers (kThreads x 65536/kThreads,
+    // rounded down to a multiple of 8): 384 threads x 168, 512 threads x 128.
+    static constexpr int kRegsLow = 56;
+    static constexpr int kRegsHigh = kThreads == 384 ? 224 : 152;
     static constexpr size_t kScaleBytes = kScaleSlots * kSlotFloats * 4;
     static constexpr int kBars = 2 * STAGES + 2 * kBufs + 2 * kScaleSlots + 1;
     static constexpr size_t kSmem =
         1024 + kStageBytes + kEpiBytes + kScaleBytes + kBars * 8 + 16;
 };
 
-template <int BN, int STAGES>
-__global__ void __launch_bounds__(TiledLayout<BN, STAGES>::kThreads, 1)
+template <int BN, int STAGES, int CPW, int EB>
+__global__ void __launch_bounds__(TiledLayout<BN, STAGES, CPW, EB>::kThreads, 1)
     k_tiled(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
             const __grid_constant__ CUtensorMap tmC, const TiledParams p)
 {
-    using L = TiledLayout<BN, STAGES>;
+    using L = TiledLayout<BN, STAGES, CPW, EB>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -199,8 +206,8 @@ __global__ void __launch_bounds__(TiledLayout<BN, STAGES>::kThreads, 1)
     grid_dependency_wait();
 
     if (warp < 4) {
-        if constexpr (L::kPromoWG == 2)
-            regs_dealloc<56>();
+        if constexpr (L::kThreads > 256)
+            regs_dealloc<L::kRegsLow>();
         if (warp == 0 && lane == 0) {
             // ---------------------------------------------------------- TMA producer
             int stage = 0;
@@ -310,7 +317,7 @@ __global__ void __launch_bounds__(TiledLayout<BN, STAGES>::kThreads, 1)
                                    in ? 4u : 0u);
                     }
                     if (lane < static_cast<uint32_t>(L::kPromoWG)) {
-                        const int col0 = nb * BN + static_cast<int>(lane) * 128;
+                        const int col0 = nb * BN + static_cast<int>(lane) * CPW;
                         const bool in = col0 < p.N;
                         cp_async_4(dst + 4u * (128 + lane),
                                    p.b_s + static_cast<size_t>(in ? col0 / 128 : 0) * p.G + g,
@@ -329,8 +336,8 @@ __global__ void __launch_bounds__(TiledLayout<BN, STAGES>::kThreads, 1)
         __syncwarp();
     } else {
         // -------------------------------------------------------------- promotion + epilogue
-        if constexpr (L::kPromoWG == 2)
-            regs_alloc<224>();
+        if constexpr (L::kThreads > 256)
+            regs_alloc<L::kRegsHigh>();
         const int h = static_cast<int>(warp / 4) - 1;      // promotion warpgroup: column half
         const uint32_t q = warp & 3u;                      // TMEM lane quarter of this warp
         const int row = static_cast<int>(q * 32 + lane);
@@ -341,10 +348,10 @@ __global__ void __launch_bounds__(TiledLayout<BN, STAGES>::kThreads, 1)
         for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
             int mb, nb;
             tile_coords(t, p.num_m_tiles, p.num_n_tiles, mb, nb);
-            const int col0 = nb * BN + h * 128;
-            uint64_t acc[64];
+            const int col0 = nb * BN + h * CPW;
+            uint64_t acc[L::kPairs];
 #pragma unroll
-            for (int j = 0; j < 64; ++j)
+            for (int j = 0; j < L::kPairs; ++j)
                 acc[j] = 0ull;
             bool ok = true;
             for (int g = 0; g < p.G; ++g) {
@@ -369,11 +376,11 @@ __global__ void __launch_bounds__(TiledLayout<BN, STAGES>::kThreads, 1)
                     sphase ^= 1u;
                 }
                 tc_fence_after_sync();
-                const uint32_t taddr = tmem_base + ((q * 32u) << 16) + buf * BN + h * 128;
-                // Two 64-column loads: TMEM load round trips, not FMA issue,
-                // bound this loop, so fewer and larger loads are faster.
+                const uint32_t taddr = tmem_base + ((q * 32u) << 16) + buf * BN + h * CPW;
+                // 64-column loads: TMEM load round trips, not FMA issue, bound
+                // this loop, so fewer and larger loads are faster.
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {
+                for (int c = 0; c < CPW / 64; ++c) {
                     uint32_t v[64];
                     tmem_load_64cols(taddr + 64u * c, v);
 #pragma unroll
@@ -388,16 +395,17 @@ __global__ void __launch_bounds__(TiledLayout<BN, STAGES>::kThreads, 1)
             }
             if (!ok)
                 break;
-            // Epilogue: this warp's 32 rows x 128 columns leave in chunks of 64
-            // bytes per row through a 2 KB shared-memory buffer (64-byte
+            // Epilogue: this warp's 32 rows x CPW columns leave in chunks of 64
+            // bytes per row through 2 KB shared-memory buffers (64-byte
             // swizzle, conflict-free 16-byte writes) and asynchronous TMA stores,
             // which write whole row segments and clip rows past M / columns past N.
             const int y = mb * 128 + static_cast<int>(q * 32);
             if (y < p.M && col0 < p.N)
-                store_tile_rows<L::kEpiBufs>(acc, &tmC, epi_buf, lane, col0, y, p.N, p.out_kind);
+                store_tile_rows<L::kPairs, L::kEpiBufs>(acc, &tmC, epi_buf, lane, col0, y, p.N,
+                                                        p.out_kind);
         }
         if (lane == 0)
-            tma_store_wait_all();
+            tma_store_wait_read();          // the epilogue buffers may be released
     }
 
     tc_fence_before_sync();
@@ -408,12 +416,12 @@ __global__ void __launch_bounds__(TiledLayout<BN, STAGES>::kThreads, 1)
     }
 }
 
-template <int BN, int STAGES>
+template <int BN, int STAGES, int CPW, int EB>
 cudaError_t launch_tiled_t(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmC,
                            const TiledParams &p, const LaunchCfg &cfg)
 {
-    using L = TiledLayout<BN, STAGES>;
-    auto kernel = k_tiled<BN, STAGES>;
+    using L = TiledLayout<BN, STAGES, CPW, EB>;
+    auto kernel = k_tiled<BN, STAGES, CPW, EB>;
     static volatile int smem_set[kMaxDeviceFlags] = {};
     cudaError_t e = ensure_smem_limit(kernel, smem_set);
     if (e != cudaSuccess)
@@ -433,35 +441,36 @@ cudaError_t launch_tiled_t(const CUtensorMap &tmA, const CUtensorMap &tmB, const
 
 }  // namespace
 
-// Instantiated configurations: (BN, stages) = (256, 4), (256, 3), (128, 6), (128, 5), (128, 4).
+// Instantiated configurations, selected by (BN, stages):
+//   BN 256: 4 stages (1 epilogue buffer) or 3 stages (4), two warpgroups of 128 columns;
+//   BN 192: 4 stages (2), three warpgroups of 64 columns;
+//   BN 128: 6 (1), 5 (2) or 4 (4) stages, two warpgroups of 64 columns.
+#define W8A8_TILED_CONFIGS(X) \
+    X(256, 4, 128, 1)         \
+    X(256, 3, 128, 4)         \
+    X(192, 4, 64, 2)          \
+    X(128, 6, 64, 1)          \
+    X(128, 5, 64, 2)          \
+    X(128, 4, 64, 4)
+
 size_t tiled_smem_bytes(int bn, int stages)
 {
-    if (bn == 256 && stages == 4)
-        return TiledLayout<256, 4>::kSmem;
-    if (bn == 256 && stages == 3)
-        return TiledLayout<256, 3>::kSmem;
-    if (bn == 128 && stages == 6)
-        return TiledLayout<128, 6>::kSmem;
-    if (bn == 128 && stages == 5)
-        return TiledLayout<128, 5>::kSmem;
-    if (bn == 128 && stages == 4)
-        return TiledLayout<128, 4>::kSmem;
+#define W8A8_SMEM_CASE(B, S, C, E)                   \
+    if (bn == B && stages == S)                      \
+        return TiledLayout<B, S, C, E>::kSmem;
+    W8A8_TILED_CONFIGS(W8A8_SMEM_CASE)
+#undef W8A8_SMEM_CASE
     return 0;
 }
 
 cudaError_t launch_tiled(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmC,
                          const TiledParams &p, int bn, const LaunchCfg &cfg)
 {
-    if (bn == 256 && cfg.stages == 4)
-        return launch_tiled_t<256, 4>(tmA, tmB, tmC, p, cfg);
-    if (bn == 256 && cfg.stages == 3)
-        return launch_tiled_t<256, 3>(tmA, tmB, tmC, p, cfg);
-    if (bn == 128 && cfg.stages == 6)
-        return launch_tiled_t<128, 6>(tmA, tmB, tmC, p, cfg);
-    if (bn == 128 && cfg.stages == 5)
-        return launch_tiled_t<128, 5>(tmA, tmB, tmC, p, cfg);
-    if (bn == 128 && cfg.stages == 4)
-        return launch_tiled_t<128, 4>(tmA, tmB, tmC, p, cfg);
+#define W8A8_LAUNCH_CASE(B, S, C, E)                 \
+    if (bn == B && cfg.stages == S)                  \
+        return launch_tiled_t<B, S, C, E>(tmA, tmB, tmC, p, cfg);
+    W8A8_TILED_CONFIGS(W8A8_LAUNCH_CASE)
+#undef W8A8_LAUNCH_CASE
     return cudaErrorInvalidValue;
 }
 

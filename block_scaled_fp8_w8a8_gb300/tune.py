@@ -34,7 +34,7 @@ def candidates(M, N, K):
     G = K // 128
     out = []
     if M >= 64:
-        for bn, stages in ((256, 4), (256, 3), (128, 6), (128, 5)):
+        for bn, stages in ((256, 4), (256, 3), (192, 4), (128, 6), (128, 5), (128, 4)):
             out.append(dict(variant=b.W8A8_VARIANT_TILED, block_n_tile=bn, stages=stages))
     if M <= 1024:
         r16 = lambda v: max(16, -(-v // 16) * 16)

@@ -8,10 +8,10 @@
  *
  *   A    FP8 E4M3 (OCP "FN" encoding) activations, [M, K] row-major (row stride K bytes)
  *   a_s  fp32 de-quantisation scales, one per token per 128-wide K group,
- *        [M, K/128] row-major
+ *        [M, ceil(K/128)] row-major (the last group may be shorter than 128)
  *   B    FP8 E4M3 weights, [N, K] row-major (row stride K bytes): C = A * B^T
  *   b_s  fp32 de-quantisation scales, one per [128, 128] weight block,
- *        [ceil(N/128), K/128] row-major
+ *        [ceil(N/128), ceil(K/128)] row-major
  *   C    [M, N] row-major in bf16, fp16 or fp32 (round to nearest even)
  *
  * The group products are accumulated in fp32 on the tensor cores, promoted
@@ -27,9 +27,11 @@
  *    the call.  C is fully overwritten; it need not be initialised.
  *  - Supported problems (anything else returns W8A8_ERR_UNSUPPORTED before any
  *    CUDA call; the shape guards of the page's Numerical safety section):
- *    block_n == block_k == 128, K % 128 == 0, N % 16 == 0, M >= 0, N >= 1,
- *    K >= 128, A/B/C 16-byte aligned, a_s/b_s 4-byte aligned, dense
- *    row-major tensors.  M == 0 returns W8A8_OK and launches nothing.
+ *    block_n == block_k == 128; K >= 16 and K % 16 == 0 (16-byte rows of A
+ *    and B); N >= 1 with N % 8 == 0 for bf16/fp16 output and N % 4 == 0 for
+ *    fp32 output (16-byte rows of C); M >= 0; A/B/C 16-byte aligned, a_s/b_s
+ *    4-byte aligned, dense row-major tensors.  M == 0 returns W8A8_OK and
+ *    launches nothing.
  *  - Errors are returned synchronously as w8a8_status; a human-readable detail
  *    string for the calling thread's last error is available from
  *    w8a8_last_error().  A device-side wait that gives up (a bounded wait that
@@ -84,7 +86,7 @@ typedef enum {
  * what you need; every zero field means "library default".
  *   variant            force a kernel variant (w8a8_variant); AUTO = dispatcher
  *   split_k            number of K splits for W8A8_VARIANT_SPLITK (0 = choose)
- *   block_n_tile       TILED only: 128 or 256 output columns per tile (0 = choose)
+ *   block_n_tile       TILED only: 128, 192 or 256 output columns per tile (0 = choose)
  *   m_tile             SWAPAB/SPLITK only: tokens per tile, multiple of 16, <= 256 (0 = choose)
  *   stages             shared-memory pipeline depth 1..8 (0 = choose)
  *   grid_limit         TILED only: cap on the number of persistent CTAs (0 = one per SM)

@@ -19,6 +19,11 @@ pytestmark = pytest.mark.gpu
 VARIANTS = {
     "tiled256": dict(variant=w8.W8A8_VARIANT_TILED, block_n_tile=256),
     "tiled128": dict(variant=w8.W8A8_VARIANT_TILED, block_n_tile=128),
+    "tiled192": dict(variant=w8.W8A8_VARIANT_TILED, block_n_tile=192),
+    "tiled256s3": dict(variant=w8.W8A8_VARIANT_TILED, block_n_tile=256, stages=3),
+    "tiled128s5": dict(variant=w8.W8A8_VARIANT_TILED, block_n_tile=128, stages=5),
+    "tiled128s4": dict(variant=w8.W8A8_VARIANT_TILED, block_n_tile=128, stages=4),
+    "cluster": dict(variant=w8.W8A8_VARIANT_SPLITK_CLUSTER),
     "swapab": dict(variant=w8.W8A8_VARIANT_SWAPAB),
     "splitk": dict(variant=w8.W8A8_VARIANT_SPLITK),
     "auto": dict(),
@@ -54,7 +59,8 @@ EDGE = [(1, 128, 128), (2, 16, 128), (7, 144, 384), (16, 400, 256), (127, 256, 5
 
 
 @pytest.mark.parametrize("M,N,K", EDGE)
-@pytest.mark.parametrize("variant", ["tiled256", "tiled128", "swapab", "splitk"])
+@pytest.mark.parametrize("variant", ["tiled256", "tiled128", "tiled192", "tiled256s3",
+                                     "tiled128s5", "tiled128s4", "swapab", "splitk", "cluster"])
 def test_edge_shapes(M, N, K, variant):
     """Ragged M and N tails, single-group K, N not a multiple of 128 or 256."""
     x = synth.make_inputs(M, N, K, seed=M + N + K)
@@ -126,7 +132,7 @@ def test_unit_scale_cast_is_round_to_nearest_even():
     assert np.abs(ref).max() < 2 ** 11
     for out in ("bf16", "fp16"):
         want = oracle.cast_out(ref, out)
-        for variant in ("tiled128", "tiled256", "swapab"):
+        for variant in ("tiled128", "tiled192", "tiled256", "swapab"):
             C = run(x, out, **VARIANTS[variant]).cpu()
             assert torch.equal(C.view(torch.int16), want.view(torch.int16)), (out, variant)
 
@@ -223,3 +229,19 @@ def test_cluster_splitk_deterministic():
     torch.cuda.synchronize()
     for o in outs[1:]:
         assert torch.equal(o.view(torch.int32), outs[0].view(torch.int32))
+
+
+RAGGED = [(5, 136, 208, "bf16"), (33, 200, 336, "bf16"), (130, 264, 144, "fp16"),
+          (1, 8, 16, "bf16"), (7, 12, 48, "fp32"), (300, 392, 1040, "bf16"), (64, 1000, 4000, "fp32")]
+
+
+@pytest.mark.parametrize("M,N,K,out", RAGGED)
+@pytest.mark.parametrize("variant", ["auto", "tiled256", "tiled192", "tiled128", "swapab",
+                                     "splitk", "cluster"])
+def test_ragged_k_and_n(M, N, K, out, variant):
+    """K not a multiple of 128 (the last scale group is short and read zero-padded)
+    and N not a multiple of 16: the oracle's partial-group reading of the definition."""
+    x = synth.make_inputs(M, N, K, seed=M + N + K)
+    ref = oracle.reference_c(x.A, x.a_s, x.B, x.b_s)
+    C = run(x, out, **VARIANTS[variant])
+    assert_close(C, ref, what=f"{variant} {M}x{N}x{K} {out}")
