@@ -200,3 +200,58 @@ def cast_out(C: np.ndarray, dtype: str):
 
 if __name__ == "__main__":  # pragma: no cover - manual build helper
     print(build(force="--force" in sys.argv))
+
+
+# --------------------------------------------------------------------------- quantiser
+#
+# The operator's activation input is FP8 E4M3 with one fp32 scale per token per
+# 128-wide K group ("feat: optimize w8a8 block fp8 matmul for Hopper", FlagGems-vllm
+# PR #693, Description); the workloads fix the scale as amax / 448.  Reading of the
+# steps (the page gives only "scale = amax/448"): in fp32, scale = amax / 448 (1 for
+# an all-zero group), then each code is the E4M3FN value nearest to x / scale (true
+# fp32 division), ties to the even code, after clamping to +-448.
+
+_POS_VALUES = _TABLE[:127]          # codes 0x00..0x7E, increasing, 0 .. 448
+
+
+def e4m3fn_encode(v: np.ndarray) -> np.ndarray:
+    """Round float64 values (already within [-448, 448], no NaN) to the nearest
+    E4M3FN code, ties to the code with an even mantissa; returns uint8 codes.
+    Written from the format: search the 127 non-negative codes for the nearest
+    value, then attach the sign."""
+    v = np.asarray(v, dtype=np.float64)
+    a = np.abs(v)
+    hi = np.clip(np.searchsorted(_POS_VALUES, a, side="left"), 0, 126)   # first value >= a
+    lo = np.clip(hi - 1, 0, 126)
+    d_hi = _POS_VALUES[hi] - a
+    d_lo = a - _POS_VALUES[lo]
+    pick_hi = (d_hi < d_lo) | ((d_hi == d_lo) & (hi % 2 == 0))
+    code = np.where(pick_hi, hi, lo).astype(np.uint8)
+    neg = np.signbit(v)
+    return np.where(neg, code | 0x80, code).astype(np.uint8)
+
+
+def quantize_per_token_group(X, group: int = 128):
+    """Per-token-group quantisation of a [M, K] activation matrix.
+
+    Returns (codes uint8 [M, K], scales float32 [M, ceil(K/group)]).  All
+    arithmetic that decides a code is fp32, as on the GPU: amax is exact, the
+    scale is the fp32 quotient amax / 448, each element is divided by the scale
+    in fp32 and then rounded to E4M3FN."""
+    X = _np(X)
+    X = X.astype(np.float32)
+    M, K = X.shape
+    G = -(-K // group) if K else 0
+    codes = np.zeros((M, K), dtype=np.uint8)
+    scales = np.ones((M, G), dtype=np.float32)
+    for g in range(G):
+        k0, k1 = g * group, min((g + 1) * group, K)
+        blk = X[:, k0:k1]
+        amax = np.max(np.abs(blk), axis=1)
+        s = (amax / np.float32(448.0)).astype(np.float32)
+        s = np.where(amax == 0, np.float32(1.0), s).astype(np.float32)
+        q = (blk / s[:, None]).astype(np.float32)
+        q = np.clip(q, np.float32(-448.0), np.float32(448.0))
+        codes[:, k0:k1] = e4m3fn_encode(q.astype(np.float64))
+        scales[:, g] = s
+    return codes, scales
