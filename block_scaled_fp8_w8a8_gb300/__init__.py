@@ -20,6 +20,7 @@ from ._binding import (  # noqa: F401
     w8a8_block_fp8_host_staging_size, w8a8_block_fp8_matmul, w8a8_block_fp8_matmul_ex,
     w8a8_block_fp8_matmul_host, w8a8_block_fp8_plan, w8a8_block_fp8_workspace_size,
     w8a8_block_fp8_matmul_splitk_noalloc, W8A8_NOALLOC_SCRATCH_BYTES,
+    w8a8_quantize_fp8_per_token_group, W8A8_IN_BF16, W8A8_IN_FP16, W8A8_IN_FP32,
     w8a8_get_device_status, w8a8_last_error, w8a8_options, w8a8_shutdown, w8a8_status_string,
 )
 
@@ -66,3 +67,26 @@ def matmul(A, a_s, B, b_s, out_dtype="bf16", out=None, stream=None, **opts):
                                   options(**opts) if opts else None)
     check(st)
     return out
+
+
+def quantize_fp8_per_token_group(X, group_size=128, A=None, a_s=None, stream=None):
+    """Per-token-group E4M3 quantisation of a CUDA tensor X [M, K] (bf16, fp16
+    or fp32): returns (A uint8 [M, K], a_s float32 [M, ceil(K/128)]), the
+    matmul's activation operand and its scales.  ``A`` / ``a_s`` may be
+    preallocated.  Raises W8A8Error on a non-zero status."""
+    import torch
+    M, K = X.shape
+    code = {torch.bfloat16: W8A8_IN_BF16, torch.float16: W8A8_IN_FP16,
+            torch.float32: W8A8_IN_FP32}.get(X.dtype)
+    if code is None:
+        raise W8A8Error(W8A8_ERR_INVALID_ARG, f"unsupported input dtype {X.dtype}")
+    if A is None:
+        A = torch.empty((M, K), dtype=torch.uint8, device=X.device)
+    if a_s is None:
+        a_s = torch.empty((M, (K + group_size - 1) // group_size), dtype=torch.float32,
+                          device=X.device)
+    for t in (X, A, a_s):
+        if not t.is_contiguous():
+            raise W8A8Error(W8A8_ERR_UNSUPPORTED, "tensors must be contiguous row-major")
+    check(w8a8_quantize_fp8_per_token_group(X, code, A, a_s, M, K, group_size, stream))
+    return A, a_s

@@ -31,6 +31,7 @@ EXPORTED = (
     "w8a8_block_fp8_matmul_ex",
     "w8a8_block_fp8_matmul_host",
     "w8a8_block_fp8_matmul_splitk_noalloc",
+    "w8a8_quantize_fp8_per_token_group",
     "w8a8_block_fp8_host_staging_size",
     "w8a8_block_fp8_workspace_size",
     "w8a8_block_fp8_plan",
@@ -94,6 +95,8 @@ def load_library():
     lib.w8a8_block_fp8_matmul_splitk_noalloc.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i32,
                                                          i32, i32, i32, vp]
     lib.w8a8_block_fp8_matmul_splitk_noalloc.restype = ctypes.c_int
+    lib.w8a8_quantize_fp8_per_token_group.argtypes = [vp, i32, vp, vp, i64, i64, i32, vp]
+    lib.w8a8_quantize_fp8_per_token_group.restype = ctypes.c_int
     lib.w8a8_block_fp8_host_staging_size.argtypes = [i64, i64, i64, i32]
     lib.w8a8_block_fp8_host_staging_size.restype = sz
     lib.w8a8_block_fp8_workspace_size.argtypes = [i64, i64, i64, opt_p]
@@ -175,6 +178,15 @@ def w8a8_block_fp8_matmul_splitk_noalloc(A, a_s, B, b_s, C, M, N, K, block_n=128
     return load_library().w8a8_block_fp8_matmul_splitk_noalloc(
         _ptr(A), _ptr(a_s), _ptr(B), _ptr(b_s), _ptr(C), M, N, K, block_n, block_k, out_dtype,
         split_k, _stream(stream))
+
+
+W8A8_IN_BF16, W8A8_IN_FP16, W8A8_IN_FP32 = 0, 1, 2
+
+
+def w8a8_quantize_fp8_per_token_group(X, x_dtype, A, a_s, M, K, group_size=128,
+                                      stream=None) -> int:
+    return load_library().w8a8_quantize_fp8_per_token_group(
+        _ptr(X), x_dtype, _ptr(A), _ptr(a_s), M, K, group_size, _stream(stream))
 
 
 def w8a8_block_fp8_host_staging_size(M, N, K, out_dtype=W8A8_OUT_BF16) -> int:

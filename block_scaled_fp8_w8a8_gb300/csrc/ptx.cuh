@@ -372,6 +372,14 @@ __device__ __forceinline__ void fma2(uint64_t &acc, uint64_t a, uint64_t b)
     asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(a), "l"(b));
 }
 
+// a * b + c on two fp32 lanes at once (each lane rounded like a scalar fmaf).
+__device__ __forceinline__ uint64_t fma2_rn(uint64_t a, uint64_t b, uint64_t c)
+{
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+
 // ------------------------------------------------------------------ cp.async (4-byte gathers)
 
 // Copy 4 bytes global -> shared; src_bytes = 0 writes zeros and reads nothing.

@@ -5,8 +5,8 @@ path's tests and benchmark.  It holds none of the matmul's arithmetic: it only
 draws Gaussian data and block-quantises it to FP8 E4M3 (OCP "FN" variant,
 max finite 448) with fp32 de-quantisation scales, which is how the operator's
 inputs are described in "feat: optimize w8a8 block fp8 matmul for Hopper"
-(FlagGems-vllm PR #693, Description: per-token/per-block FP8 E4M3 inputs with
-[block_n, block_k] de-quant scales).
+(FlagGems-vllm PR #693, Description: E4M3 activations scaled per token and K
+block, E4M3 weights scaled per [block_n, block_k] block).
 
 Recipe (the plainest reading of the workload descriptions; every choice is
 stated so that the two sides of a parity test see identical bytes):
@@ -94,6 +94,17 @@ def make_inputs(M: int, N: int, K: int, *, seed: int = 0, block_n: int = 128,
     Aq, a_s = quantize_blocks(A, 1, block_k)        # per token, per K group
     Bq, b_s = quantize_blocks(B, block_n, block_k)  # per [block_n, block_k] block
     return W8A8Inputs(Aq, a_s, Bq, b_s, block_n, block_k)
+
+
+def activations(M: int, K: int, *, seed: int = 0, dtype: torch.dtype = torch.float32,
+                outlier_p: float = 0.0, outlier_scale: float = 20.0) -> torch.Tensor:
+    """Seeded unquantised activations [M, K]: N(0,1) fp32 draws (a fraction
+    ``outlier_p`` of them times ``outlier_scale``), rounded once to ``dtype``."""
+    g = torch.Generator(device="cpu").manual_seed(seed)
+    X = torch.randn(M, K, generator=g, dtype=torch.float32)
+    if outlier_p > 0.0:
+        X = torch.where(torch.rand(M, K, generator=g) < outlier_p, X * outlier_scale, X)
+    return X.to(dtype)
 
 
 def random_codes(rows: int, cols: int, *, seed: int, allow_nan: bool = False) -> torch.Tensor:

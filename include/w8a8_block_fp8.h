@@ -195,6 +195,35 @@ w8a8_status w8a8_block_fp8_matmul_splitk_noalloc(const void *A_dev, const float 
                                                  w8a8_out_dtype out_dtype, int split_k,
                                                  w8a8_stream_t stream);
 
+/*
+ * Per-token-group FP8 quantiser: makes the matmul's activation operand A and
+ * its scales a_s from a higher-precision activation X ("feat: optimize w8a8
+ * block fp8 matmul for Hopper", FlagGems-vllm PR #693, Description: the
+ * activations are E4M3 with one fp32 scale per token and 128-wide K group).
+ * The pages leave the choice of scale open; this takes the plainest reading:
+ *
+ *   a_s[m,g] = max_{k in g} |X[m,k]| / 448      (fp32 quotient; 1 where it is 0: an
+ *                                                all-zero group or an underflowing max)
+ *   A[m,k]   = E4M3FN(clamp(X[m,k] / a_s[m,g], -448, 448))
+ *              (fp32 division rounded to nearest, then round to nearest even)
+ *
+ *   X_dev    device, row-major [M, K] of x_dtype (bf16, fp16 or fp32), 16-byte aligned
+ *   A_dev    device, row-major [M, K] E4M3 codes (written), 16-byte aligned
+ *   a_s_dev  device, row-major [M, ceil(K/128)] fp32 (written), 4-byte aligned
+ *   group_size must be 128 (the matmul's block_k); K >= 16 and K % 16 == 0, the
+ *   last group may be shorter than 128.  M == 0 is a no-op.
+ *
+ * The caller owns every buffer; nothing is allocated.  One kernel launch on
+ * `stream`, asynchronous; X must not overlap A or a_s.  X must be finite: a
+ * NaN or infinity gives unspecified codes and scale for its group.  Errors: W8A8_ERR_INVALID_ARG (null pointer,
+ * negative size, unknown dtype), W8A8_ERR_UNSUPPORTED (group_size, K or
+ * alignment outside the above), W8A8_ERR_CUDA (launch failed).
+ */
+typedef enum { W8A8_IN_BF16 = 0, W8A8_IN_FP16 = 1, W8A8_IN_FP32 = 2 } w8a8_in_dtype;
+w8a8_status w8a8_quantize_fp8_per_token_group(const void *X_dev, w8a8_in_dtype x_dtype,
+                                              void *A_dev, float *a_s_dev, int64_t M, int64_t K,
+                                              int group_size, w8a8_stream_t stream);
+
 /* Bytes of device staging that w8a8_block_fp8_matmul_host needs (0 for bad sizes). */
 size_t w8a8_block_fp8_host_staging_size(int64_t M, int64_t N, int64_t K, w8a8_out_dtype out_dtype);
 

@@ -7,9 +7,9 @@ besides the seeded input generator ``block_scaled_fp8_w8a8_gb300.synth``, which
 holds none of the matmul's arithmetic.
 
 The operator ("feat: optimize w8a8 block fp8 matmul for Hopper", FlagGems-vllm
-PR #693, Description: per-token/per-block FP8 E4M3 inputs with
-[block_n, block_k] de-quant scales; Numerical safety: FP32 accumulation, cast
-to bf16 / fp16 / fp32):
+PR #693, Description: E4M3 activations scaled per token and K block, E4M3
+weights scaled per [block_n, block_k] block; Numerical safety: the sums are
+kept in fp32 and the result is cast to bf16, fp16 or fp32):
 
     C[m,n] = cast_out( sum_g a_s[m,g] * b_s[n // block_n, g] * sum_{k in g} A[m,k] * B[n,k] )
 
@@ -207,9 +207,11 @@ if __name__ == "__main__":  # pragma: no cover - manual build helper
 # The operator's activation input is FP8 E4M3 with one fp32 scale per token per
 # 128-wide K group ("feat: optimize w8a8 block fp8 matmul for Hopper", FlagGems-vllm
 # PR #693, Description); the workloads fix the scale as amax / 448.  Reading of the
-# steps (the page gives only "scale = amax/448"): in fp32, scale = amax / 448 (1 for
-# an all-zero group), then each code is the E4M3FN value nearest to x / scale (true
-# fp32 division), ties to the even code, after clamping to +-448.
+# steps (the page gives only "scale = amax/448"): in fp32, scale = amax / 448, set
+# to 1 where that quotient is 0 (an all-zero group, or a max below 448 times the
+# smallest fp32 subnormal, whose quotient underflows), then each code is the E4M3FN
+# value nearest to x / scale (true fp32 division), ties to the even code, after
+# clamping to +-448.
 
 _POS_VALUES = _TABLE[:127]          # codes 0x00..0x7E, increasing, 0 .. 448
 
@@ -249,7 +251,7 @@ def quantize_per_token_group(X, group: int = 128):
         blk = X[:, k0:k1]
         amax = np.max(np.abs(blk), axis=1)
         s = (amax / np.float32(448.0)).astype(np.float32)
-        s = np.where(amax == 0, np.float32(1.0), s).astype(np.float32)
+        s = np.where(s == 0, np.float32(1.0), s).astype(np.float32)
         q = (blk / s[:, None]).astype(np.float32)
         q = np.clip(q, np.float32(-448.0), np.float32(448.0))
         codes[:, k0:k1] = e4m3fn_encode(q.astype(np.float64))

@@ -1,9 +1,9 @@
 """Pins of the CPU oracle against facts that do not come from the oracle itself.
 
 Operator: "feat: optimize w8a8 block fp8 matmul for Hopper" (FlagGems-vllm
-PR #693), Description (per-token/per-block FP8 E4M3 inputs with
-[block_n, block_k] de-quant scales) and Numerical safety (FP32 accumulation,
-cast to bf16 / fp16 / fp32).  Each test names the mistake it would catch.
+PR #693), Description (E4M3 activations scaled per token and K block, E4M3
+weights scaled per [block_n, block_k] block) and Numerical safety (sums kept in
+fp32, result cast to bf16, fp16 or fp32).  Each test names the mistake it would catch.
 """
 import itertools
 import json

@@ -71,3 +71,23 @@ def test_matches_independent_library_formulation(dtype):
     q = (pad / sc[:, :, None]).clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8)
     assert np.array_equal(s, sc.numpy())
     assert np.array_equal(codes, q.reshape(33, 1024)[:, :1000].numpy())
+
+
+def test_signed_zeros_and_underflowing_scale():
+    """-0 keeps its sign (code 0x80); a group whose max / 448 underflows to 0 in
+    fp32 takes scale 1 (not a division by zero), and its tiny values become
+    signed zeros; a group just above that limit keeps its own subnormal scale.
+    There 1e-42 is 714 * 2^-149 in fp32 and 714/448 * 2^-149 rounds to the
+    scale 2 * 2^-149, so the quotient is exactly 357 and codes as 352 (0x7B)."""
+    X = np.zeros((3, 256), dtype=np.float32)
+    X[0, :] = -0.0
+    X[1, :128] = np.linspace(-1e-44, 1e-44, 128, dtype=np.float64).astype(np.float32)
+    X[2, :128] = np.float32(1e-42) * np.sign(np.arange(128) - 63.5).astype(np.float32)
+    codes, s = oracle.quantize_per_token_group(X)
+    assert np.all(codes[0] == 0x80) and np.all(s[0] == 1.0)
+    assert s[1, 0] == 1.0
+    assert np.all((codes[1, :128] & 0x7F) == 0)
+    assert np.all((codes[1, :128] >> 7) == np.signbit(X[1, :128]))
+    assert s[2, 0] == np.float32(2 * 2.0 ** -149)
+    assert np.all((codes[2, :128] & 0x7F) == 0x7B)
+    assert np.all((codes[2, :128] >> 7) == np.signbit(X[2, :128]))
