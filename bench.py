@@ -64,33 +64,47 @@ def parse():
                          "(for profiling one kernel)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-quant", action="store_true",
+                    help="skip the activation quantiser's own measurement")
     ap.add_argument("--no-per-shape", action="store_true",
                     help="skip the per-shape launch timing (keeps an ncu launch list short)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     return ap.parse_args()
 
 
-def source_digest() -> str:
-    """sha256 over the CUDA sources (first 16 hex digits): identifies the kernel build
-    that a recorded ncu traffic figure belongs to."""
+# The sources each kernel's launches depend on (its own file, the shared PTX
+# helpers and launch declarations, and for the matmul the host planner and the
+# measured dispatch table).
+KERNEL_SOURCES = {
+    "matmul": ("api.cu", "gemm_swapab.cu", "gemm_tiled.cu", "kernels.cuh", "ptx.cuh",
+               "dispatch_table.h", "tuning_table.inc"),
+    "quant": ("quant.cu", "kernels.cuh", "ptx.cuh"),
+}
+
+
+def source_digest(kernel: str = "matmul") -> str:
+    """sha256 over the CUDA sources of one kernel family (first 16 hex digits):
+    identifies the build that a recorded ncu traffic figure belongs to."""
     import hashlib
     csrc = os.path.join(ROOT, "block_scaled_fp8_w8a8_gb300", "csrc")
     h = hashlib.sha256()
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h", ".inc")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode() + b"\0" + f.read())
+    for name in sorted(KERNEL_SOURCES[kernel]):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
     return h.hexdigest()[:16]
 
 
 # DRAM bytes (read + write) of one launch, from an ncu capture of the kernel build
-# with the given source digest: (digest, "MxNxK", output bytes) -> bytes.  A figure
-# whose kernel sources have changed since is not reported (the key no longer matches).
+# with the given source digest: (digest, shape key, output bytes) -> bytes.  A
+# figure whose kernel sources have changed since is not reported (the key no
+# longer matches).
 MEASURED_TRAFFIC = {
-    # profiles/k_swapab_decode_m214.md: read 1.159 MB, write 0 (C stays in L2 within the launch)
-    ("977f9d0fc575f7b5", "214x4096x256", 2): 1159424,
-    # profiles/k_tiled_prefill_16384x4096x4096.md: read 97.27 MB + write 99.67 MB
-    ("977f9d0fc575f7b5", "16384x4096x4096", 2): 196937216,
+    # profiles/k_swapab_decode_m214.md: read 1.172 MB, write 0 (C stays in L2 within the launch)
+    ("53eeccc5d6e05ef3", "214x4096x256", 2): 1172224,
+    # profiles/k_tiled_prefill_16384x4096x4096.md: read 95.61 MB + write 99.11 MB
+    ("53eeccc5d6e05ef3", "16384x4096x4096", 2): 194723072,
+    # profiles/k_quant_group128_16384x4096_bf16.md: read 134.28 MB + write 37.95 MB
+    ("ce940a1728174b49", "quant_16384x4096", 1): 172228352,
 }
 
 
@@ -415,10 +429,63 @@ def run_ours(args, rank, world):
         result["value"], result["unit"] = result["tflops"], "TFLOP/s"
     if e2e is not None:
         result["e2e"] = e2e
+    if not args.no_quant:
+        result["quantizer"] = measure_quantizer(hbm, l2)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(shapes, wl.host, args.out_dtype, bound,
                                               args.cpu_seconds)
     return result
+
+
+# Activations the quantiser turns into the matmul's A operand: the prefill
+# (16384 x 4096), a mid-size and the largest decode row count of the sweep.
+QUANT_SHAPES = [(16384, 4096), (4096, 4096), (214, 4096)]
+
+
+def quant_bytes(M, K, in_bytes=2):
+    """Algorithmic HBM bytes of one quantiser call: read X, write codes and scales."""
+    return M * K * in_bytes + M * K + M * (-(-K // 128)) * 4
+
+
+def measure_quantizer(hbm, l2):
+    """Launch duration of the per-token-group quantiser on bf16 activations,
+    from a CUDA graph of L launches over rotating inputs larger than L2."""
+    import block_scaled_fp8_w8a8_gb300 as w8
+    out = []
+    for (M, K) in QUANT_SHAPES:
+        per = quant_bytes(M, K)
+        sets = max(2, int(-(-2 * l2 // per)) + 1)
+        X = [synth.activations(M, K, seed=r, dtype=torch.bfloat16).to("cuda") for r in range(sets)]
+        A = [torch.empty((M, K), dtype=torch.uint8, device="cuda") for _ in range(sets)]
+        S = [torch.empty((M, -(-K // 128)), dtype=torch.float32, device="cuda") for _ in range(sets)]
+        L = max(sets, 64)
+        stream = torch.cuda.Stream()
+        for r in range(sets):
+            w8.check(w8.w8a8_quantize_fp8_per_token_group(X[r], w8.W8A8_IN_BF16, A[r], S[r], M, K,
+                                                          128, stream))
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for j in range(L):
+                r = j % sets
+                w8.check(w8.w8a8_quantize_fp8_per_token_group(
+                    X[r], w8.W8A8_IN_BF16, A[r], S[r], M, K, 128, torch.cuda.current_stream()))
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        t_blk, _ = time_blocks(lambda k: g.replay(), 5, 1, 0.2)
+        t = t_blk / (5 * L)
+        out.append({"M": M, "K": K, "us": round(t * 1e6, 3),
+                    "gbs": round(quant_bytes(M, K) / t / 1e9, 1)})
+        del X, A, S, g
+    d = out[0]
+    traffic = MEASURED_TRAFFIC.get((source_digest("quant"), f"quant_{d['M']}x{d['K']}", 1))
+    return {"op": "per-token-group E4M3 quantiser, bf16 activations -> codes + fp32 scales",
+            "per_shape": out,
+            "roofline": {"bound": "hbm", "achieved": d["gbs"], "peak": hbm, "unit": "GB/s",
+                         "frac": round(d["gbs"] / hbm, 4), "traffic": traffic,
+                         "algorithmic_bytes": quant_bytes(d["M"], d["K"]),
+                         "kernel": f"k_quant_group128 M={d['M']} K={d['K']}"}}
 
 
 def run_e2e(wl, args, world):
