@@ -257,3 +257,50 @@ def quantize_per_token_group(X, group: int = 128):
         codes[:, k0:k1] = e4m3fn_encode(q.astype(np.float64))
         scales[:, g] = s
     return codes, scales
+
+
+# --------------------------------------------------------------------------- grouped (MoE)
+#
+# The grouped form of the same matmul: E experts, each with its own weights B[e]
+# [N, K] and block scales b_s[e] [ceil(N/128), ceil(K/128)]; every token row is
+# multiplied by the weights of the expert it is routed to.  The MoE pages run
+# this per-expert GEMM with the decode swap-AB mapping ("[SM90] Optimize FP8
+# MegaMoE across L2 epilogue, 4WG launch heuristic and decode swap-AB",
+# sgl-project/DeepGEMM PR #69, Summary).  Reading: two layouts, both with the
+# definition above applied per expert and nothing else changed.
+#  * masked: A [E, max_m, K], a_s [E, max_m, G]; expert e owns rows
+#    0 .. masked_m[e]-1 of its slab; C [E, max_m, N]; rows at or past
+#    masked_m[e] are unspecified (NaN here).
+#  * contiguous: A [M, K], a_s [M, G]; m_indices[m] is row m's expert, -1 for a
+#    padding row; C [M, N]; padding rows are unspecified (NaN here).
+# Each expert's rows go through reference_c with that expert's B and b_s.
+
+def reference_grouped_masked(A, a_s, B, b_s, masked_m, block_n: int = 128, block_k: int = 128):
+    A, a_s, B, b_s = _np(A), _np(a_s), _np(B), _np(b_s)
+    masked_m = np.asarray(_np(masked_m), dtype=np.int64)
+    E, max_m, _ = A.shape
+    N = B.shape[1]
+    C = np.full((E, max_m, N), np.nan, dtype=np.float64)
+    for e in range(E):
+        m = int(masked_m[e])
+        if not 0 <= m <= max_m:
+            raise ValueError("masked_m out of range")
+        if m:
+            C[e, :m] = reference_c(A[e, :m], a_s[e, :m], B[e], b_s[e], block_n, block_k)
+    return C
+
+
+def reference_grouped_contiguous(A, a_s, B, b_s, m_indices, block_n: int = 128,
+                                 block_k: int = 128):
+    A, a_s, B, b_s = _np(A), _np(a_s), _np(B), _np(b_s)
+    idx = np.asarray(_np(m_indices), dtype=np.int64)
+    M = A.shape[0]
+    E, N = B.shape[0], B.shape[1]
+    C = np.full((M, N), np.nan, dtype=np.float64)
+    for e in range(E):
+        rows = np.flatnonzero(idx == e)
+        if rows.size:
+            C[rows] = reference_c(A[rows], a_s[rows], B[e], b_s[e], block_n, block_k)
+    if np.any((idx < -1) | (idx >= E)):
+        raise ValueError("m_indices out of range")
+    return C
