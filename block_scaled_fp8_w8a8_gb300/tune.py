@@ -29,9 +29,46 @@ TABLE = os.path.join(HERE, "csrc", "tuning_table.inc")
 # K in {256,1024,4096}) at the workloads' M values.
 DEFAULT_SHAPES = sorted({s for w in synth.WORKLOADS.values() for s in w["shapes"]})
 
+# The full trace grid: every (N, K) pair of the grid, M from 1 to 16384 at
+# these points plus the workloads' own M values for that pair.  Each tuned
+# point covers the M range from the previous point (exclusive) to itself; the
+# last covers everything above.
+GRID_N = (512, 1536, 4096, 8192)
+GRID_K = (256, 1024, 4096)
+GRID_M = (1, 2, 4, 8, 16, 24, 32, 48, 64, 80, 96, 112, 128, 160, 192, 224, 256, 320, 384,
+          448, 512, 640, 768, 1024, 1536, 2048, 3072, 4096, 6144, 8192, 12288, 16384)
+M_OPEN_END = 1 << 40
 
-def candidates(M, N, K):
-    G = K // 128
+
+def grid_shapes():
+    extra = {}
+    for (M, N, K) in DEFAULT_SHAPES:
+        extra.setdefault((N, K), set()).add(M)
+    return [(M, N, K) for N in GRID_N for K in GRID_K
+            for M in sorted(set(GRID_M) | extra.get((N, K), set()))]
+
+
+def table_lines(best_by_shape, ranges):
+    """Table rows from {(M, N, K): best row}.  With ranges, each (N, K) pair's
+    points cover (previous M, M], the last one up to M_OPEN_END."""
+    lines = []
+    by_nk = {}
+    for (M, N, K) in best_by_shape:
+        by_nk.setdefault((N, K), []).append(M)
+    for (N, K) in sorted(by_nk):
+        ms = sorted(by_nk[(N, K)])
+        for i, M in enumerate(ms):
+            best = best_by_shape[(M, N, K)]
+            lo, hi = (M, M) if not ranges else (ms[i - 1] + 1 if i else 1,
+                                                M if i + 1 < len(ms) else M_OPEN_END)
+            lines.append(f"{{{lo}, {hi}, {N}, {K}, {best['variant']}, {best['split_k']}, "
+                         f"{best['m_tile']}, {best['block_n_tile']}, {best['stages']}}},"
+                         f"  // M={M}: {best['us']:.2f} us")
+    return lines
+
+
+def candidates(M, N, K, sms=152):
+    G = -(-K // 128)
     out = []
     if M >= 64:
         for bn, stages in ((256, 4), (256, 3), (192, 4), (128, 6), (128, 5), (128, 4)):
@@ -48,8 +85,10 @@ def candidates(M, N, K):
                 tiles.add(mt)
         for mt in sorted(tiles):
             out.append(dict(variant=b.W8A8_VARIANT_SWAPAB, m_tile=mt))
+            ctas = -(-N // 128) * -(-M // mt)
             for s in (2, 3, 4, 6, 8, 12, 16, 32):
-                if s <= G and -(-G // -(-G // s)) == s:
+                # splits that leave more than four waves of CTAs are not tried
+                if s <= G and -(-G // -(-G // s)) == s and ctas * s <= 4 * sms:
                     out.append(dict(variant=b.W8A8_VARIANT_SPLITK, m_tile=mt, split_k=s))
                     if s <= 16:
                         out.append(dict(variant=b.W8A8_VARIANT_SPLITK_CLUSTER, m_tile=mt,
@@ -70,6 +109,7 @@ class Bench:
 
     def time(self, cfg, launches=64, reps=5):
         M, N, K = self.shape
+        launches = max(launches, self.sets)   # every launch reads a set not in L2
         o = b.w8a8_options()
         for k, v in cfg.items():
             setattr(o, k, v)
@@ -113,17 +153,42 @@ class Bench:
         return best, plan
 
 
+def write_table(path, lines):
+    with open(path, "w") as f:
+        f.write("// m_lo, m_hi, n, k, variant, split_k, m_tile, block_n_tile, stages\n")
+        f.write("// Written by block_scaled_fp8_w8a8_gb300/tune.py from timed runs on a GB300.\n")
+        f.write("\n".join(lines) + "\n")
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--out", default=TABLE)
     ap.add_argument("--report", default=None)
     ap.add_argument("--shapes", default=None)
+    ap.add_argument("--grid", action="store_true",
+                    help="tune the full trace grid and write M ranges")
+    ap.add_argument("--grid-n", type=int, default=None,
+                    help="with --grid: only the shapes with this N")
+    ap.add_argument("--jsonl", default=None,
+                    help="append each shape's best configuration to this file as it is found")
+    ap.add_argument("--table-from", default=None,
+                    help="write the table from a --jsonl file instead of measuring")
     args = ap.parse_args()
-    shapes = DEFAULT_SHAPES
+    if args.table_from:
+        best_by_shape = {}
+        with open(args.table_from) as f:
+            for line in f:
+                r = json.loads(line)
+                best_by_shape[tuple(r["shape"])] = r["best"]
+        write_table(args.out, table_lines(best_by_shape, ranges=args.grid))
+        return
+    shapes = grid_shapes() if args.grid else DEFAULT_SHAPES
+    if args.grid and args.grid_n:
+        shapes = [s for s in shapes if s[1] == args.grid_n]
     if args.shapes:
         shapes = [tuple(int(v) for v in s.split("x")) for s in args.shapes.split(",")]
     l2 = torch.cuda.get_device_properties(0).L2_cache_size
-    report, lines = [], []
+    report, best_by_shape = [], {}
     for (M, N, K) in shapes:
         bench = Bench(M, N, K, l2)
         rows = []
@@ -145,14 +210,12 @@ def main():
             continue
         best = rows[0]
         report.append({"shape": [M, N, K], "best": best, "all": rows})
-        lines.append(f"{{{M}, {M}, {N}, {K}, {best['variant']}, {best['split_k']}, "
-                     f"{best['m_tile']}, {best['block_n_tile']}, {best['stages']}}},"
-                     f"  // {best['us']:.2f} us")
+        best_by_shape[(M, N, K)] = best
+        if args.jsonl:
+            with open(args.jsonl, "a") as f:
+                f.write(json.dumps({"shape": [M, N, K], "best": best}) + "\n")
         print(f"{M}x{N}x{K}: best {best['us']:.2f} us {best['cfg']}", flush=True)
-    with open(args.out, "w") as f:
-        f.write("// m_lo, m_hi, n, k, variant, split_k, m_tile, block_n_tile, stages\n")
-        f.write("// Written by block_scaled_fp8_w8a8_gb300/tune.py from timed runs on a GB300.\n")
-        f.write("\n".join(lines) + "\n")
+    write_table(args.out, table_lines(best_by_shape, ranges=args.grid))
     if args.report:
         with open(args.report, "w") as f:
             json.dump(report, f, indent=1)
