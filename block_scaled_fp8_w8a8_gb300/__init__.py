@@ -21,6 +21,7 @@ from ._binding import (  # noqa: F401
     w8a8_block_fp8_matmul_host, w8a8_block_fp8_plan, w8a8_block_fp8_workspace_size,
     w8a8_block_fp8_matmul_splitk_noalloc, W8A8_NOALLOC_SCRATCH_BYTES,
     w8a8_quantize_fp8_per_token_group, W8A8_IN_BF16, W8A8_IN_FP16, W8A8_IN_FP32,
+    w8a8_block_fp8_grouped_matmul_masked, w8a8_block_fp8_grouped_matmul_contiguous,
     w8a8_get_device_status, w8a8_last_error, w8a8_options, w8a8_shutdown, w8a8_status_string,
 )
 
@@ -90,3 +91,49 @@ def quantize_fp8_per_token_group(X, group_size=128, A=None, a_s=None, stream=Non
             raise W8A8Error(W8A8_ERR_UNSUPPORTED, "tensors must be contiguous row-major")
     check(w8a8_quantize_fp8_per_token_group(X, code, A, a_s, M, K, group_size, stream))
     return A, a_s
+
+
+def _out_tensor(shape, code, device):
+    import torch
+    tdt = {W8A8_OUT_BF16: torch.bfloat16, W8A8_OUT_FP16: torch.float16,
+           W8A8_OUT_FP32: torch.float32}[code]
+    return torch.empty(shape, dtype=tdt, device=device)
+
+
+def grouped_matmul_masked(A, a_s, B, b_s, masked_m, out_dtype="bf16", out=None, stream=None,
+                          **opts):
+    """Grouped matmul, masked layout, on CUDA tensors: A [E, max_m, K], a_s
+    [E, max_m, K/128], B [E, N, K], b_s [E, ceil(N/128), K/128], masked_m int32
+    [E].  Returns C [E, max_m, N]; rows at or past masked_m[e] are unspecified."""
+    E, max_m, K = A.shape
+    N = B.shape[1]
+    code = out_code(out_dtype)
+    if out is None:
+        out = _out_tensor((E, max_m, N), code, A.device)
+    for t in (A, a_s, B, b_s, out, masked_m):
+        if not t.is_contiguous():
+            raise W8A8Error(W8A8_ERR_UNSUPPORTED, "tensors must be contiguous row-major")
+    check(w8a8_block_fp8_grouped_matmul_masked(A, a_s, B, b_s, out, masked_m, E, max_m, N, K,
+                                               128, 128, code, stream,
+                                               options(**opts) if opts else None))
+    return out
+
+
+def grouped_matmul_contiguous(A, a_s, B, b_s, m_indices, out_dtype="bf16", out=None,
+                              stream=None, **opts):
+    """Grouped matmul, contiguous layout, on CUDA tensors: A [M, K], a_s [M,
+    K/128], B [E, N, K], b_s [E, ceil(N/128), K/128], m_indices int32 [M] (the
+    expert of each row, -1 = padding; each aligned 128-row block holds one
+    expert).  Returns C [M, N]; padding rows are unspecified."""
+    M, K = A.shape
+    E, N = B.shape[0], B.shape[1]
+    code = out_code(out_dtype)
+    if out is None:
+        out = _out_tensor((M, N), code, A.device)
+    for t in (A, a_s, B, b_s, out, m_indices):
+        if not t.is_contiguous():
+            raise W8A8Error(W8A8_ERR_UNSUPPORTED, "tensors must be contiguous row-major")
+    check(w8a8_block_fp8_grouped_matmul_contiguous(A, a_s, B, b_s, out, m_indices, M, E, N, K,
+                                                   128, 128, code, stream,
+                                                   options(**opts) if opts else None))
+    return out

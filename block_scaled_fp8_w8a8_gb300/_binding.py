@@ -31,6 +31,8 @@ EXPORTED = (
     "w8a8_block_fp8_matmul_ex",
     "w8a8_block_fp8_matmul_host",
     "w8a8_block_fp8_matmul_splitk_noalloc",
+    "w8a8_block_fp8_grouped_matmul_masked",
+    "w8a8_block_fp8_grouped_matmul_contiguous",
     "w8a8_quantize_fp8_per_token_group",
     "w8a8_block_fp8_host_staging_size",
     "w8a8_block_fp8_workspace_size",
@@ -95,6 +97,12 @@ def load_library():
     lib.w8a8_block_fp8_matmul_splitk_noalloc.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i32,
                                                          i32, i32, i32, vp]
     lib.w8a8_block_fp8_matmul_splitk_noalloc.restype = ctypes.c_int
+    lib.w8a8_block_fp8_grouped_matmul_masked.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64,
+                                                         i64, i32, i32, i32, vp, opt_p]
+    lib.w8a8_block_fp8_grouped_matmul_masked.restype = ctypes.c_int
+    lib.w8a8_block_fp8_grouped_matmul_contiguous.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64,
+                                                             i64, i64, i32, i32, i32, vp, opt_p]
+    lib.w8a8_block_fp8_grouped_matmul_contiguous.restype = ctypes.c_int
     lib.w8a8_quantize_fp8_per_token_group.argtypes = [vp, i32, vp, vp, i64, i64, i32, vp]
     lib.w8a8_quantize_fp8_per_token_group.restype = ctypes.c_int
     lib.w8a8_block_fp8_host_staging_size.argtypes = [i64, i64, i64, i32]
@@ -178,6 +186,22 @@ def w8a8_block_fp8_matmul_splitk_noalloc(A, a_s, B, b_s, C, M, N, K, block_n=128
     return load_library().w8a8_block_fp8_matmul_splitk_noalloc(
         _ptr(A), _ptr(a_s), _ptr(B), _ptr(b_s), _ptr(C), M, N, K, block_n, block_k, out_dtype,
         split_k, _stream(stream))
+
+
+def w8a8_block_fp8_grouped_matmul_masked(A, a_s, B, b_s, C, masked_m, E, max_m, N, K,
+                                         block_n=128, block_k=128, out_dtype=W8A8_OUT_BF16,
+                                         stream=None, opts=None) -> int:
+    return load_library().w8a8_block_fp8_grouped_matmul_masked(
+        _ptr(A), _ptr(a_s), _ptr(B), _ptr(b_s), _ptr(C), _ptr(masked_m), E, max_m, N, K,
+        block_n, block_k, out_dtype, _stream(stream), _opts(opts))
+
+
+def w8a8_block_fp8_grouped_matmul_contiguous(A, a_s, B, b_s, C, m_indices, M, E, N, K,
+                                             block_n=128, block_k=128, out_dtype=W8A8_OUT_BF16,
+                                             stream=None, opts=None) -> int:
+    return load_library().w8a8_block_fp8_grouped_matmul_contiguous(
+        _ptr(A), _ptr(a_s), _ptr(B), _ptr(b_s), _ptr(C), _ptr(m_indices), M, E, N, K,
+        block_n, block_k, out_dtype, _stream(stream), _opts(opts))
 
 
 W8A8_IN_BF16, W8A8_IN_FP16, W8A8_IN_FP32 = 0, 1, 2

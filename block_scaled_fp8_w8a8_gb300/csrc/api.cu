@@ -114,13 +114,17 @@ w8a8_status current_device(int *dev_out, DeviceInfo *info_out)
 // 128 columns (one K group, 128 bytes) by box_rows rows, 128-byte swizzle,
 // out-of-range elements read as zero.
 w8a8_status encode_u8_map(CUtensorMap *map, const void *base, int64_t rows, int64_t cols,
-                          int box_rows)
+                          int box_rows, int64_t slabs = 0)
 {
-    cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
-    cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols)};
-    cuuint32_t box[2] = {128u, static_cast<cuuint32_t>(box_rows)};
-    cuuint32_t elem[2] = {1u, 1u};
-    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims,
+    // slabs > 0: a 3-D map over [slabs, rows, cols] (one expert per slab), boxes
+    // of one slab; rows past `rows` inside a slab read as zeros.
+    const cuuint32_t rank = slabs > 0 ? 3u : 2u;
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows),
+                          static_cast<cuuint64_t>(slabs)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(cols * rows)};
+    cuuint32_t box[3] = {128u, static_cast<cuuint32_t>(box_rows), 1u};
+    cuuint32_t elem[3] = {1u, 1u, 1u};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, rank, const_cast<void *>(base), dims,
                           strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -134,17 +138,22 @@ w8a8_status encode_u8_map(CUtensorMap *map, const void *base, int64_t rows, int6
 // 2-D tensor map over the row-major [rows, cols] output C in its dtype; boxes
 // of box_cols columns by box_rows rows with the given shared-memory swizzle.
 w8a8_status encode_out_map(CUtensorMap *map, void *base, int64_t rows, int64_t cols, int out,
-                           int box_cols, int box_rows, CUtensorMapSwizzle swizzle)
+                           int box_cols, int box_rows, CUtensorMapSwizzle swizzle,
+                           int64_t slabs = 0)
 {
     const int eb = out == W8A8_OUT_FP32 ? 4 : 2;
     const CUtensorMapDataType dt = out == W8A8_OUT_FP32   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
                                    : out == W8A8_OUT_FP16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
                                                           : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-    cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
-    cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * eb};
-    cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
-    cuuint32_t elem[2] = {1u, 1u};
-    CUresult r = g_encode(map, dt, 2, base, dims, strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
+    // slabs > 0: 3-D over [slabs, rows, cols]; stores clip at each slab's last row.
+    const cuuint32_t rank = slabs > 0 ? 3u : 2u;
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows),
+                          static_cast<cuuint64_t>(slabs)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(cols) * eb,
+                             static_cast<cuuint64_t>(cols) * eb * static_cast<cuuint64_t>(rows)};
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows), 1u};
+    cuuint32_t elem[3] = {1u, 1u, 1u};
+    CUresult r = g_encode(map, dt, rank, base, dims, strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
                           swizzle, CU_TENSOR_MAP_L2_PROMOTION_NONE,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS)
@@ -373,9 +382,18 @@ w8a8_status library_workspace(int dev, cudaStream_t stream, size_t bytes, void *
     return W8A8_OK;
 }
 
+// Grouped (MoE) calls: which layout, the device array of per-expert counts
+// (masked) or per-row expert ids (contiguous), and the number of experts.  In
+// the masked layout M is the rows of one expert's slab.
+struct Grouping {
+    enum Mode { NONE, MASKED, CONTIGUOUS } mode = NONE;
+    const int32_t *ids = nullptr;
+    int64_t experts = 0;
+};
+
 w8a8_status run(const void *A, const float *a_s, const void *B, const float *b_s, void *C,
                 int64_t M, int64_t N, int64_t K, int block_n, int block_k, int out,
-                cudaStream_t stream, const w8a8_options *o)
+                cudaStream_t stream, const w8a8_options *o, const Grouping &gr = Grouping())
 {
     g_last_error[0] = '\0';
     w8a8_status st = check_problem(M, N, K, block_n, block_k, out);
@@ -383,9 +401,29 @@ w8a8_status run(const void *A, const float *a_s, const void *B, const float *b_s
         return st;
     if ((st = check_options(o)) != W8A8_OK)
         return st;
+    const bool masked = gr.mode == Grouping::MASKED, contiguous = gr.mode == Grouping::CONTIGUOUS;
+    if (gr.mode != Grouping::NONE) {
+        if (gr.experts < 0)
+            return fail(W8A8_ERR_INVALID_ARG, "negative number of experts");
+        if (gr.experts * std::max<int64_t>(M, 1) > (1ll << 31) - 1 || gr.experts > 65535)
+            return fail(W8A8_ERR_UNSUPPORTED, "%lld experts of %lld rows: too many",
+                        static_cast<long long>(gr.experts), static_cast<long long>(M));
+        const int v = o ? o->variant : W8A8_VARIANT_AUTO;
+        if (masked && v != W8A8_VARIANT_AUTO && v != W8A8_VARIANT_SWAPAB &&
+            v != W8A8_VARIANT_SPLITK_CLUSTER)
+            return fail(W8A8_ERR_UNSUPPORTED, "the masked layout runs the swap-AB kernel "
+                                              "(variant AUTO, SWAPAB or SPLITK_CLUSTER)");
+        if (contiguous && v != W8A8_VARIANT_AUTO && v != W8A8_VARIANT_TILED)
+            return fail(W8A8_ERR_UNSUPPORTED, "the contiguous layout runs the tiled kernel "
+                                              "(variant AUTO or TILED)");
+        if (gr.experts == 0 && masked)
+            return W8A8_OK;
+    }
     if (M == 0)
         return W8A8_OK;
-    if (!A || !a_s || !B || !b_s || !C)
+    if (gr.mode != Grouping::NONE && gr.experts == 0)
+        return fail(W8A8_ERR_INVALID_ARG, "rows routed to no expert (experts == 0)");
+    if (!A || !a_s || !B || !b_s || !C || (gr.mode != Grouping::NONE && !gr.ids))
         return fail(W8A8_ERR_INVALID_ARG, "null pointer argument");
     if (!aligned(A, 16) || !aligned(B, 16) || !aligned(C, 16))
         return fail(W8A8_ERR_UNSUPPORTED, "A, B and C must be 16-byte aligned");
@@ -397,8 +435,29 @@ w8a8_status run(const void *A, const float *a_s, const void *B, const float *b_s
     if ((st = current_device(&dev, &info)) != W8A8_OK)
         return st;
     Plan pl;
-    if ((st = make_plan(M, N, K, out == W8A8_OUT_FP32 ? 4 : 2, o, info, &pl)) != W8A8_OK)
+    w8a8_options forced = {};
+    if (o)
+        forced = *o;
+    if (masked) {
+        // One token tile per expert by default (most experts' counts fit), no split.
+        if (forced.variant == W8A8_VARIANT_AUTO)
+            forced.variant = W8A8_VARIANT_SWAPAB;
+        if (!forced.m_tile)
+            forced.m_tile = static_cast<int>(std::min<int64_t>(256, cdiv(M, 16) * 16));
+    } else if (contiguous && forced.variant == W8A8_VARIANT_AUTO) {
+        forced.variant = W8A8_VARIANT_TILED;
+        const TableEntry *t = lookup_tuned(M, N, K);
+        if (t && t->variant == W8A8_VARIANT_TILED) {
+            if (!forced.block_n_tile) forced.block_n_tile = t->block_n_tile;
+            if (!forced.stages) forced.stages = t->stages;
+        }
+    }
+    if ((st = make_plan(M, N, K, out == W8A8_OUT_FP32 ? 4 : 2,
+                        gr.mode != Grouping::NONE ? &forced : o, info, &pl)) != W8A8_OK)
         return st;
+    if (masked && static_cast<int64_t>(pl.m_tiles) * gr.experts > 65535)
+        return fail(W8A8_ERR_UNSUPPORTED, "%lld experts x %d token tiles exceed the grid",
+                    static_cast<long long>(gr.experts), pl.m_tiles);
 
     const int G = static_cast<int>(cdiv(K, 128));
     const int NB = static_cast<int>(cdiv(N, 128));
@@ -416,11 +475,11 @@ w8a8_status run(const void *A, const float *a_s, const void *B, const float *b_s
         CUtensorMap mA, mB, mC;
         const int chunk_cols = out == W8A8_OUT_FP32 ? 16 : 32;   // 64 bytes of a row
         if ((st = encode_u8_map(&mA, A, M, K, 128)) != W8A8_OK ||
-            (st = encode_u8_map(&mB, B, N, K, pl.bn)) != W8A8_OK ||
+            (st = encode_u8_map(&mB, B, N, K, pl.bn, contiguous ? gr.experts : 0)) != W8A8_OK ||
             (st = encode_out_map(&mC, C, M, N, out, chunk_cols, 32, CU_TENSOR_MAP_SWIZZLE_64B)) !=
                 W8A8_OK)
             return st;
-        TiledParams p;
+        TiledParams p = {};
         p.a_s = a_s;
         p.b_s = b_s;
         p.C = C;
@@ -436,21 +495,26 @@ w8a8_status run(const void *A, const float *a_s, const void *B, const float *b_s
         p.debug_skip_tma = debug_skip;
         p.status = info.status;
         p.wait_limit = limit;
+        p.m_indices = contiguous ? gr.ids : nullptr;
+        p.experts = contiguous ? static_cast<int>(gr.experts) : 1;
         e = launch_tiled(mA, mB, mC, p, pl.bn, cfg);
     } else {
         CUtensorMap mW, mX, mC;
-        if ((st = encode_u8_map(&mW, B, N, K, 128)) != W8A8_OK ||
-            (st = encode_u8_map(&mX, A, M, K, pl.mma_n)) != W8A8_OK ||
-            (st = encode_out_map(&mC, C, M, N, out, 128, pl.mma_n, CU_TENSOR_MAP_SWIZZLE_NONE)) !=
-                W8A8_OK)
+        const int64_t slabs = masked ? gr.experts : 0;
+        if ((st = encode_u8_map(&mW, B, N, K, 128, slabs)) != W8A8_OK ||
+            (st = encode_u8_map(&mX, A, M, K, pl.mma_n, slabs)) != W8A8_OK ||
+            (st = encode_out_map(&mC, C, M, N, out, 128, pl.mma_n, CU_TENSOR_MAP_SWIZZLE_NONE,
+                                 slabs)) != W8A8_OK)
             return st;
-        SwapParams p;
+        SwapParams p = {};
         p.a_s = a_s;
         p.b_s = b_s;
         p.C = C;
         p.ws = nullptr;
         p.counters = nullptr;
         const size_t ws_bytes = splitk_workspace_bytes(M, N, pl);
+        if (ws_bytes && masked)
+            return fail(W8A8_ERR_UNSUPPORTED, "the masked layout splits K only in clusters");
         if (ws_bytes) {
             if (static_cast<size_t>(pl.m_tiles) * NB > kCounterWords)
                 return fail(W8A8_ERR_UNSUPPORTED, "split-K over %lld output tiles (max %zu)",
@@ -473,13 +537,18 @@ w8a8_status run(const void *A, const float *a_s, const void *B, const float *b_s
         p.G = G;
         p.NB = NB;
         p.mma_n = pl.mma_n;
-        p.num_m_tiles = pl.m_tiles;
+        p.num_m_tiles = masked ? static_cast<int>(pl.m_tiles * gr.experts) : pl.m_tiles;
+        p.masked_m = masked ? gr.ids : nullptr;
+        p.experts = masked ? static_cast<int>(gr.experts) : 1;
+        p.tiles_per_expert = pl.m_tiles;
         p.splits = pl.splits;
         p.groups_per_split = pl.gps;
         p.out_kind = out;
         p.out_bytes = pl.tile_bytes;
         p.cluster_reduce = (pl.variant == W8A8_VARIANT_SPLITK_CLUSTER && pl.splits > 1) ? 1 : 0;
-        p.prefetch_weights = (o && o->pdl && o->weights_static) ? 1 : 0;
+        // A masked call learns which experts have tokens only after the wait,
+        // so it streams no weights before it (most of them may be unused).
+        p.prefetch_weights = (o && o->pdl && o->weights_static && !masked) ? 1 : 0;
         p.debug_skip_tma = debug_skip;
         p.status = info.status;
         p.wait_limit = limit;
@@ -520,6 +589,39 @@ w8a8_status w8a8_block_fp8_matmul_ex(const void *A_dev, const float *a_s_dev, co
 {
     return run(A_dev, a_s_dev, B_dev, b_s_dev, C_dev, M, N, K, block_n, block_k, out_dtype,
                reinterpret_cast<cudaStream_t>(stream), opts);
+}
+
+w8a8_status w8a8_block_fp8_grouped_matmul_masked(const void *A_dev, const float *a_s_dev,
+                                                 const void *B_dev, const float *b_s_dev,
+                                                 void *C_dev, const int32_t *masked_m_dev,
+                                                 int64_t E, int64_t max_m, int64_t N, int64_t K,
+                                                 int block_n, int block_k,
+                                                 w8a8_out_dtype out_dtype, w8a8_stream_t stream,
+                                                 const w8a8_options *opts)
+{
+    Grouping gr;
+    gr.mode = Grouping::MASKED;
+    gr.ids = masked_m_dev;
+    gr.experts = E;
+    return run(A_dev, a_s_dev, B_dev, b_s_dev, C_dev, max_m, N, K, block_n, block_k, out_dtype,
+               reinterpret_cast<cudaStream_t>(stream), opts, gr);
+}
+
+w8a8_status w8a8_block_fp8_grouped_matmul_contiguous(const void *A_dev, const float *a_s_dev,
+                                                     const void *B_dev, const float *b_s_dev,
+                                                     void *C_dev, const int32_t *m_indices_dev,
+                                                     int64_t M, int64_t E, int64_t N, int64_t K,
+                                                     int block_n, int block_k,
+                                                     w8a8_out_dtype out_dtype,
+                                                     w8a8_stream_t stream,
+                                                     const w8a8_options *opts)
+{
+    Grouping gr;
+    gr.mode = Grouping::CONTIGUOUS;
+    gr.ids = m_indices_dev;
+    gr.experts = E;
+    return run(A_dev, a_s_dev, B_dev, b_s_dev, C_dev, M, N, K, block_n, block_k, out_dtype,
+               reinterpret_cast<cudaStream_t>(stream), opts, gr);
 }
 
 size_t w8a8_block_fp8_host_staging_size(int64_t M, int64_t N, int64_t K, w8a8_out_dtype out)

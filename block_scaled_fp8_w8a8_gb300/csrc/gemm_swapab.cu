@@ -80,7 +80,10 @@ __device__ __forceinline__ void add4(float4 &a, const float4 &b)
     a.w += b.w;
 }
 
-template <int MT>
+// GROUPED selects the masked MoE layout at compile time, so that the plain
+// kernel carries none of its bookkeeping (the largest token tile's promotion
+// loop uses every register the launch allows).
+template <int MT, bool GROUPED>
 __global__ void __launch_bounds__(SwapLayout<MT>::kThreads, SwapLayout<MT>::kMinBlocks)
     k_swapab(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
              const __grid_constant__ CUtensorMap tmC, const SwapParams p, const int stages)
@@ -102,14 +105,19 @@ __global__ void __launch_bounds__(SwapLayout<MT>::kThreads, SwapLayout<MT>::kMin
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + L::kBars);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     volatile int *last_flag = reinterpret_cast<volatile int *>(tmem_slot + 2);
+    volatile int *rows_slot = reinterpret_cast<volatile int *>(tmem_slot + 3);
 
     const uint32_t warp = warp_index(), lane = lane_index();
     const int nb = blockIdx.x;                 // 128-row block of B (and of C's columns)
     const int split = blockIdx.y;
-    const int m0 = blockIdx.z * p.mma_n;
+    // Grouped (masked layout): grid.z enumerates (expert, token tile) and every
+    // operand is addressed inside the expert's slab.
+    constexpr bool grouped = GROUPED;
+    const int expert = grouped ? static_cast<int>(blockIdx.z) / p.tiles_per_expert : 0;
+    const int m0 = grouped ? (static_cast<int>(blockIdx.z) - expert * p.tiles_per_expert) * p.mma_n
+                           : static_cast<int>(blockIdx.z) * p.mma_n;
     const int g_begin = split * p.groups_per_split;
     const int g_end = min(p.G, g_begin + p.groups_per_split);
-    const int ng = g_end - g_begin;
     const bool is_producer = warp == 0 && lane == 0;
 
     if (threadIdx.x == 0) {
@@ -142,6 +150,26 @@ __global__ void __launch_bounds__(SwapLayout<MT>::kThreads, SwapLayout<MT>::kMin
     const WaitGuard guard{abort_flag, p.status, p.wait_limit};
 
     grid_launch_dependents();
+    // A grouped tile learns its expert's token count only after the dependency
+    // wait (the routing that writes masked_m runs before this launch); the
+    // rows of the tile that carry results go to *rows_slot, and an empty tile
+    // releases its tensor memory and leaves.  The CTAs of a cluster share one
+    // tile, so they all leave together and none waits at a cluster barrier.
+    if constexpr (grouped) {
+        if (threadIdx.x == 0) {
+            grid_dependency_wait();
+            const int count = min(max(p.masked_m[expert], 0), p.M);
+            *rows_slot = max(0, min(count - m0, p.mma_n));
+        }
+        __syncthreads();
+        if (*rows_slot == 0) {
+            if (warp == 1)
+                tmem_dealloc(tmem_base, L::kTmemCols);
+            return;
+        }
+    }
+    const int ng = g_end - g_begin;
+
     // Warp 0 holds the producer; its lane 0 waits for the previous grid only
     // after issuing the weight prefetch.  The whole warp skips this wait (its
     // other lanes touch no memory): were lanes 1..31 to wait here, the warp
@@ -161,7 +189,12 @@ __global__ void __launch_bounds__(SwapLayout<MT>::kThreads, SwapLayout<MT>::kMin
             for (int i = 0; i < pre; ++i) {
                 if (i != p.debug_skip_tma) {
                     mbar_arrive_expect_tx(full_bar(i), tx);
-                    tma_load_2d(sW + i * L::kWBytes, &tmW, full_bar(i), (g_begin + i) * 128, nb * 128);
+                    if constexpr (grouped)
+                        tma_load_3d(sW + i * L::kWBytes, &tmW, full_bar(i), (g_begin + i) * 128,
+                                    nb * 128, expert);
+                    else
+                        tma_load_2d(sW + i * L::kWBytes, &tmW, full_bar(i), (g_begin + i) * 128,
+                                    nb * 128);
                 }
             }
             grid_dependency_wait();
@@ -178,11 +211,21 @@ __global__ void __launch_bounds__(SwapLayout<MT>::kThreads, SwapLayout<MT>::kMin
                     }
                     if (i != p.debug_skip_tma) {
                         mbar_arrive_expect_tx(full_bar(stage), tx);
-                        tma_load_2d(sW + stage * L::kWBytes, &tmW, full_bar(stage), g * 128, nb * 128);
+                        if constexpr (grouped)
+                            tma_load_3d(sW + stage * L::kWBytes, &tmW, full_bar(stage), g * 128,
+                                        nb * 128, expert);
+                        else
+                            tma_load_2d(sW + stage * L::kWBytes, &tmW, full_bar(stage), g * 128,
+                                        nb * 128);
                     }
                 }
-                if (i != p.debug_skip_tma)
-                    tma_load_2d(sX + stage * L::kXBytes, &tmX, full_bar(stage), g * 128, m0);
+                if (i != p.debug_skip_tma) {
+                    if constexpr (grouped)
+                        tma_load_3d(sX + stage * L::kXBytes, &tmX, full_bar(stage), g * 128, m0,
+                                    expert);
+                    else
+                        tma_load_2d(sX + stage * L::kXBytes, &tmX, full_bar(stage), g * 128, m0);
+                }
                 ++issued;
                 if (++stage == stages) {
                     stage = 0;
@@ -259,17 +302,33 @@ __global__ void __launch_bounds__(SwapLayout<MT>::kThreads, SwapLayout<MT>::kMin
         const int n = nb * 128 + row;
         const int c0 = h * L::kCols;                         // first token column of this thread
 
-        // Folded scales s[g][j] = a_s[m0+j, g] * b_s[nb, g] (zero past M and mma_n).
-        for (int idx = tid; idx < ng * MT; idx += kPromoThreads) {
-            const int gl = idx / MT, j = idx - gl * MT;
-            const int m = m0 + j;
-            float v = 0.f;
-            if (j < p.mma_n && m < p.M) {
-                const int g = g_begin + gl;
-                v = __ldg(p.a_s + static_cast<size_t>(m) * p.G + g) *
-                    __ldg(p.b_s + static_cast<size_t>(nb) * p.G + g);
+        // Folded scales s[g][j] = a_s[m0+j, g] * b_s[nb, g] (zero past the
+        // tile's valid rows; a grouped tile reads its expert's slabs).
+        if constexpr (grouped) {
+            const size_t a_row0 = static_cast<size_t>(expert) * p.M + m0;
+            const size_t b_row = static_cast<size_t>(expert) * p.NB + nb;
+            const int tile_rows = *rows_slot;
+            for (int idx = tid; idx < ng * MT; idx += kPromoThreads) {
+                const int gl = idx / MT, j = idx - gl * MT;
+                float v = 0.f;
+                if (j < tile_rows) {
+                    const int g = g_begin + gl;
+                    v = __ldg(p.a_s + (a_row0 + j) * p.G + g) * __ldg(p.b_s + b_row * p.G + g);
+                }
+                sscale[idx] = v;
             }
-            sscale[idx] = v;
+        } else {
+            for (int idx = tid; idx < ng * MT; idx += kPromoThreads) {
+                const int gl = idx / MT, j = idx - gl * MT;
+                const int m = m0 + j;
+                float v = 0.f;
+                if (j < p.mma_n && m < p.M) {
+                    const int g = g_begin + gl;
+                    v = __ldg(p.a_s + static_cast<size_t>(m) * p.G + g) *
+                        __ldg(p.b_s + static_cast<size_t>(nb) * p.G + g);
+                }
+                sscale[idx] = v;
+            }
         }
         named_barrier(1, kPromoThreads);
 
@@ -339,7 +398,10 @@ __global__ void __launch_bounds__(SwapLayout<MT>::kThreads, SwapLayout<MT>::kMin
             fence_async_smem();
             named_barrier(1, kPromoThreads);
             if (tid == 0) {
-                tma_store_2d(&tmC, sW, nb * 128, m0);
+                if constexpr (grouped)
+                    tma_store_3d(&tmC, sW, nb * 128, m0, expert);
+                else
+                    tma_store_2d(&tmC, sW, nb * 128, m0);
                 tma_store_commit();
                 tma_store_wait_read();      // the tile's shared memory may be released
             }
@@ -418,7 +480,8 @@ __global__ void __launch_bounds__(SwapLayout<MT>::kThreads, SwapLayout<MT>::kMin
             asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(rank));
             const int tid = static_cast<int>(threadIdx.x) - 128;
             constexpr int kPromoThreads = 128 * L::kPromoWG;
-            const int rows = min(p.mma_n, p.M - m0);
+            const int rows = grouped ? *rows_slot : min(p.mma_n, p.M - m0);
+            const size_t c_row0 = static_cast<size_t>(expert) * p.M + m0;
             const int r0 = rows * static_cast<int>(rank) / p.splits;
             const int r1 = rows * (static_cast<int>(rank) + 1) / p.splits;
             const int c4n = min(128, p.N - nb * 128) / 4;
@@ -440,8 +503,7 @@ __global__ void __launch_bounds__(SwapLayout<MT>::kThreads, SwapLayout<MT>::kMin
                 }
                 for (; s < p.splits; ++s)
                     add4(sum, ld_cluster_f4(cluster_map(local, static_cast<uint32_t>(s))));
-                store4(p.C, static_cast<size_t>(m0 + r) * p.N + nb * 128 + 4 * c4, sum,
-                       p.out_kind);
+                store4(p.C, (c_row0 + r) * p.N + nb * 128 + 4 * c4, sum, p.out_kind);
             }
         }
         cluster_sync();                      // no CTA leaves while its tile is being read
@@ -455,12 +517,12 @@ __global__ void __launch_bounds__(SwapLayout<MT>::kThreads, SwapLayout<MT>::kMin
     }
 }
 
-template <int MT>
+template <int MT, bool GROUPED>
 cudaError_t launch_swapab_t(const CUtensorMap &tmW, const CUtensorMap &tmX, const CUtensorMap &tmC,
                             const SwapParams &p, const LaunchCfg &cfg)
 {
     using L = SwapLayout<MT>;
-    auto kernel = k_swapab<MT>;
+    auto kernel = k_swapab<MT, GROUPED>;
     const size_t smem = L::smem(cfg.stages, p.groups_per_split, p.out_bytes);
     static volatile int smem_set[kMaxDeviceFlags] = {};
     cudaError_t e = ensure_smem_limit(kernel, smem_set);
@@ -523,11 +585,16 @@ cudaError_t launch_swapab(const CUtensorMap &tmW, const CUtensorMap &tmX, const 
 {
     if (cfg.stages < 1 || cfg.stages > kMaxStages)
         return cudaErrorInvalidValue;
+    const bool grouped = p.masked_m != nullptr;
     switch (mt) {
-    case 32: return launch_swapab_t<32>(tmW, tmX, tmC, p, cfg);
-    case 64: return launch_swapab_t<64>(tmW, tmX, tmC, p, cfg);
-    case 128: return launch_swapab_t<128>(tmW, tmX, tmC, p, cfg);
-    case 256: return launch_swapab_t<256>(tmW, tmX, tmC, p, cfg);
+    case 32: return grouped ? launch_swapab_t<32, true>(tmW, tmX, tmC, p, cfg)
+                            : launch_swapab_t<32, false>(tmW, tmX, tmC, p, cfg);
+    case 64: return grouped ? launch_swapab_t<64, true>(tmW, tmX, tmC, p, cfg)
+                            : launch_swapab_t<64, false>(tmW, tmX, tmC, p, cfg);
+    case 128: return grouped ? launch_swapab_t<128, true>(tmW, tmX, tmC, p, cfg)
+                             : launch_swapab_t<128, false>(tmW, tmX, tmC, p, cfg);
+    case 256: return grouped ? launch_swapab_t<256, true>(tmW, tmX, tmC, p, cfg)
+                             : launch_swapab_t<256, false>(tmW, tmX, tmC, p, cfg);
     default: return cudaErrorInvalidValue;
     }
 }

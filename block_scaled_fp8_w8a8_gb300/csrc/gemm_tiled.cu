@@ -48,6 +48,20 @@ __device__ __forceinline__ void tile_coords(int t, int num_m, int num_n, int &mb
     nb = r / gm;
 }
 
+// Expert of tile t in the grouped (contiguous) layout: the id of the first row
+// of its 128-row block, padding blocks (-1) mapped to expert 0 and ids past the
+// last expert to the last one (so no scale read leaves b_s); 0 past the last
+// tile or without grouping.  Plain loads: the ids are written by the work
+// before this launch and are read after the dependency wait.
+__device__ __forceinline__ int tile_expert(const TiledParams &p, int t)
+{
+    if (p.m_indices == nullptr || t >= p.num_tiles)
+        return 0;
+    int mb, nb;
+    tile_coords(t, p.num_m_tiles, p.num_n_tiles, mb, nb);
+    return min(max(p.m_indices[mb * 128], 0), p.experts - 1);
+}
+
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
                                              uint32_t d)
 {
@@ -214,9 +228,12 @@ __global__ void __launch_bounds__(TiledLayout<BN, STAGES, CPW, EB>::kThreads, 1)
             uint32_t phase = 0;
             long long issued = 0;
             bool ok = true;
+            int e_next = tile_expert(p, blockIdx.x);
             for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
                 int mb, nb;
                 tile_coords(t, p.num_m_tiles, p.num_n_tiles, mb, nb);
+                const int e = e_next;
+                e_next = tile_expert(p, t + gridDim.x);   // in flight during this tile
                 for (int g = 0; g < p.G; ++g) {
                     if (!wait_bounded(empty_bar(stage), phase ^ 1u, guard, SITE_TILED_PRODUCER)) {
                         ok = false;
@@ -225,7 +242,12 @@ __global__ void __launch_bounds__(TiledLayout<BN, STAGES, CPW, EB>::kThreads, 1)
                     if (issued != p.debug_skip_tma) {
                         mbar_arrive_expect_tx(full_bar(stage), L::kABytes + L::kBBytes);
                         tma_load_2d(sA + stage * L::kABytes, &tmA, full_bar(stage), g * 128, mb * 128);
-                        tma_load_2d(sB + stage * L::kBBytes, &tmB, full_bar(stage), g * 128, nb * BN);
+                        if (p.m_indices)
+                            tma_load_3d(sB + stage * L::kBBytes, &tmB, full_bar(stage), g * 128,
+                                        nb * BN, e);
+                        else
+                            tma_load_2d(sB + stage * L::kBBytes, &tmB, full_bar(stage), g * 128,
+                                        nb * BN);
                     }
                     ++issued;
                     if (++stage == STAGES) {
@@ -299,9 +321,12 @@ __global__ void __launch_bounds__(TiledLayout<BN, STAGES, CPW, EB>::kThreads, 1)
             int slot = 0;
             uint32_t sphase = 0;
             bool ok = true;
+            int e_next = tile_expert(p, blockIdx.x);
             for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
                 int mb, nb;
                 tile_coords(t, p.num_m_tiles, p.num_n_tiles, mb, nb);
+                const size_t b_row0 = static_cast<size_t>(e_next) * p.NB;
+                e_next = tile_expert(p, t + gridDim.x);
                 for (int g = 0; g < p.G; ++g) {
                     ok = __all_sync(0xffffffffu, wait_bounded(sempty_bar(slot), sphase ^ 1u, guard,
                                                               SITE_TILED_SCALES));
@@ -320,7 +345,7 @@ __global__ void __launch_bounds__(TiledLayout<BN, STAGES, CPW, EB>::kThreads, 1)
                         const int col0 = nb * BN + static_cast<int>(lane) * CPW;
                         const bool in = col0 < p.N;
                         cp_async_4(dst + 4u * (128 + lane),
-                                   p.b_s + static_cast<size_t>(in ? col0 / 128 : 0) * p.G + g,
+                                   p.b_s + (b_row0 + (in ? col0 / 128 : 0)) * p.G + g,
                                    in ? 4u : 0u);
                     }
                     cp_async_arrive(sfull_bar(slot));

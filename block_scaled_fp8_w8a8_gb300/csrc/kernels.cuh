@@ -34,6 +34,11 @@ struct TiledParams {
     int debug_skip_tma;    // test hook: >= 0 makes the producer skip that many-th load (no TMA issued)
     unsigned *status;
     unsigned long long wait_limit;
+    // Grouped (contiguous layout): B is [experts, N, K] behind a 3-D tensor map,
+    // b_s is [experts, NB, G]; the expert of 128-row block mb is m_indices[128 mb]
+    // (-1: a padding block, computed with expert 0's weights).  nullptr: one B.
+    const int *m_indices;
+    int experts;
 };
 
 // Swap-AB: weights on the MMA M side (128 rows of B = one b_s row block),
@@ -59,6 +64,13 @@ struct SwapParams {
     int debug_skip_tma;
     unsigned *status;
     unsigned long long wait_limit;
+    // Grouped (masked layout): A, C and a_s hold `experts` slabs of M rows
+    // (3-D tensor maps for A, B and C; b_s is [experts, NB, G]); expert e's
+    // valid rows are 0 .. masked_m[e]-1, read on the device after the
+    // dependency wait; grid.z = e * tiles_per_expert + token tile.  nullptr: one problem.
+    const int *masked_m;
+    int experts;
+    int tiles_per_expert;
 };
 
 struct LaunchCfg {

@@ -107,6 +107,45 @@ def activations(M: int, K: int, *, seed: int = 0, dtype: torch.dtype = torch.flo
     return X.to(dtype)
 
 
+def make_grouped_masked(E: int, max_m: int, N: int, K: int, *, seed: int = 0, counts=None,
+                        outlier_p: float = 0.0):
+    """Masked-layout MoE inputs: per expert, N(0,1) activations [max_m, K] and
+    weights [N, K] block-quantised as in make_inputs, and a token count (drawn
+    uniformly from 0..max_m unless ``counts`` is given).  Returns (A [E,max_m,K],
+    a_s [E,max_m,G], B [E,N,K], b_s [E,NB,G], masked_m int32 [E])."""
+    parts = [make_inputs(max_m, N, K, seed=seed * 1000 + e, outlier_p=outlier_p) for e in range(E)]
+    if counts is None:
+        g = torch.Generator(device="cpu").manual_seed(seed)
+        counts = torch.randint(0, max_m + 1, (E,), generator=g)
+    masked_m = torch.as_tensor(counts, dtype=torch.int32)
+    return (torch.stack([x.A for x in parts]), torch.stack([x.a_s for x in parts]),
+            torch.stack([x.B for x in parts]), torch.stack([x.b_s for x in parts]), masked_m)
+
+
+def make_grouped_contiguous(counts, N: int, K: int, *, seed: int = 0, align: int = 128):
+    """Contiguous-layout MoE inputs: expert e's ``counts[e]`` token rows form one
+    segment padded with -1 rows to a multiple of ``align``; padding rows hold
+    zero codes and unit scales.  Returns (A [M,K], a_s [M,G], B [E,N,K],
+    b_s [E,NB,G], m_indices int32 [M])."""
+    E = len(counts)
+    rows, idx = [], []
+    for e, c in enumerate(counts):
+        c = int(c)
+        padded = _cdiv(c, align) * align
+        x = make_inputs(max(c, 1), 8, K, seed=seed * 1000 + e)
+        if c:
+            rows.append((x.A[:c], x.a_s[:c]))
+        if padded > c:
+            rows.append((torch.zeros(padded - c, K, dtype=torch.uint8),
+                         torch.ones(padded - c, _cdiv(K, 128), dtype=torch.float32)))
+        idx += [e] * c + [-1] * (padded - c)
+    A = torch.cat([r[0] for r in rows]) if rows else torch.zeros(0, K, dtype=torch.uint8)
+    a_s = torch.cat([r[1] for r in rows]) if rows else torch.zeros(0, _cdiv(K, 128))
+    w = [make_inputs(1, N, K, seed=seed * 1000 + 500 + e) for e in range(E)]
+    return (A.contiguous(), a_s.contiguous(), torch.stack([x.B for x in w]),
+            torch.stack([x.b_s for x in w]), torch.tensor(idx, dtype=torch.int32))
+
+
 def random_codes(rows: int, cols: int, *, seed: int, allow_nan: bool = False) -> torch.Tensor:
     """Uniformly random E4M3FN bytes (all codes, including subnormals and -0).
 

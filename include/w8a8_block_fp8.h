@@ -196,6 +196,62 @@ w8a8_status w8a8_block_fp8_matmul_splitk_noalloc(const void *A_dev, const float 
                                                  w8a8_stream_t stream);
 
 /*
+ * Grouped (mixture-of-experts) forms of the same matmul: E experts, each with
+ * its own weights B[e] [N, K] and block scales b_s[e] [ceil(N/128), ceil(K/128)];
+ * every token row is multiplied by the weights of the expert it is routed to,
+ * with the definition at the top of this file unchanged.  The MoE pages run
+ * this per-expert GEMM with the decode swap-AB mapping ("[SM90] Optimize FP8
+ * MegaMoE across L2 epilogue, 4WG launch heuristic and decode swap-AB",
+ * sgl-project/DeepGEMM PR #69, Summary).  The expert routing is a DEVICE array
+ * written by earlier work on the stream; the host never reads it, so a call
+ * can be captured in a CUDA graph and replayed with new routing.
+ *
+ * Masked layout (decode; swap-AB kernel, one CTA per expert x 128 weight rows x
+ * token tile; empty tiles leave at once):
+ *   A_dev        E4M3 [E, max_m, K], a_s_dev fp32 [E, max_m, ceil(K/128)]
+ *   B_dev        E4M3 [E, N, K],     b_s_dev fp32 [E, ceil(N/128), ceil(K/128)]
+ *   C_dev        [E, max_m, N] in out_dtype
+ *   masked_m_dev int32 [E]: expert e's rows 0 .. masked_m[e]-1 are valid
+ *                (values are clamped to [0, max_m]).
+ *   Rows of C at or past masked_m[e] are unspecified (they may be written).
+ *   opts: variant AUTO/SWAPAB (default: one token tile of min(256, max_m
+ *   rounded up to 16) rows per expert; m_tile and stages may be set) or
+ *   SPLITK_CLUSTER with split_k; other variants are W8A8_ERR_UNSUPPORTED.
+ *   With pdl = 1 the kernel overlaps the previous one's tail but streams no
+ *   weights before the dependency wait (weights_static has no effect here).
+ *
+ * Contiguous layout (prefill; tiled kernel):
+ *   A_dev [M, K], a_s_dev [M, ceil(K/128)], C_dev [M, N] as in the plain call;
+ *   B_dev [E, N, K], b_s_dev [E, ceil(N/128), ceil(K/128)];
+ *   m_indices_dev int32 [M]: the expert of each row, -1 for a padding row.
+ *   Every aligned block of 128 rows (rows 128i .. 128i+127) must hold rows of
+ *   one expert only, optionally followed by padding; the expert of a block is
+ *   read from its first row (a block starting with -1 is padding).  Padding
+ *   rows of C are unspecified.  Ids outside [-1, E) give unspecified results
+ *   but never an out-of-bounds access.  opts: variant AUTO or TILED.
+ *
+ * Shape rules are those of the plain call (K % 16, N % 8 or 4, alignment),
+ * plus E * rows < 2^31 and E <= 65535 (masked: E x token tiles <= 65535).
+ * E == 0 (masked) or max_m == 0 or M == 0 is a no-op.  Errors as for
+ * w8a8_block_fp8_matmul_ex; a null id array is W8A8_ERR_INVALID_ARG.
+ */
+w8a8_status w8a8_block_fp8_grouped_matmul_masked(const void *A_dev, const float *a_s_dev,
+                                                 const void *B_dev, const float *b_s_dev,
+                                                 void *C_dev, const int32_t *masked_m_dev,
+                                                 int64_t E, int64_t max_m, int64_t N, int64_t K,
+                                                 int block_n, int block_k,
+                                                 w8a8_out_dtype out_dtype, w8a8_stream_t stream,
+                                                 const w8a8_options *opts);
+w8a8_status w8a8_block_fp8_grouped_matmul_contiguous(const void *A_dev, const float *a_s_dev,
+                                                     const void *B_dev, const float *b_s_dev,
+                                                     void *C_dev, const int32_t *m_indices_dev,
+                                                     int64_t M, int64_t E, int64_t N, int64_t K,
+                                                     int block_n, int block_k,
+                                                     w8a8_out_dtype out_dtype,
+                                                     w8a8_stream_t stream,
+                                                     const w8a8_options *opts);
+
+/*
  * Per-token-group FP8 quantiser: makes the matmul's activation operand A and
  * its scales a_s from a higher-precision activation X ("feat: optimize w8a8
  * block fp8 matmul for Hopper", FlagGems-vllm PR #693, Description: the
