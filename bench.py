@@ -66,6 +66,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-quant", action="store_true",
                     help="skip the activation quantiser's own measurement")
+    ap.add_argument("--no-grouped", action="store_true",
+                    help="skip the grouped (MoE) matmul measurements")
     ap.add_argument("--no-per-shape", action="store_true",
                     help="skip the per-shape launch timing (keeps an ncu launch list short)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
@@ -105,6 +107,8 @@ MEASURED_TRAFFIC = {
     ("53eeccc5d6e05ef3", "16384x4096x4096", 2): 194723072,
     # profiles/k_quant_group128_16384x4096_bf16.md: read 134.28 MB + write 37.95 MB
     ("ce940a1728174b49", "quant_16384x4096", 1): 172228352,
+    # profiles/k_swapab_grouped_moe_decode_256x1536x4096.md: read 1.645 GB + write 25.95 MB
+    ("8e787da19f26f0df", "grouped_decode_masked", 2): 1671156976,
 }
 
 
@@ -431,6 +435,8 @@ def run_ours(args, rank, world):
         result["e2e"] = e2e
     if not args.no_quant:
         result["quantizer"] = measure_quantizer(hbm, l2)
+    if not args.no_grouped:
+        result["grouped"] = measure_grouped(hbm, 2.0 * bf16)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(shapes, wl.host, args.out_dtype, bound,
                                               args.cpu_seconds)
@@ -486,6 +492,102 @@ def measure_quantizer(hbm, l2):
                          "frac": round(d["gbs"] / hbm, 4), "traffic": traffic,
                          "algorithmic_bytes": quant_bytes(d["M"], d["K"]),
                          "kernel": f"k_quant_group128 M={d['M']} K={d['K']}"}}
+
+
+# Grouped (MoE) workloads, each a layer slice of one expert projection
+# (N = 1536, K = 4096, a shape of the trace grid):
+#  * decode, masked layout: 256 experts, 256 tokens routed to 8 experts each
+#    (multinomial over the experts), at most 32 token slots per expert; every
+#    expert with a token streams its weights, 1.6 GB in all.
+#  * prefill, contiguous layout: 16384 rows routed to 16 experts in segments of
+#    1024 rows (aligned to 128).
+GROUPED_DECODE = dict(E=256, tokens=256, topk=8, max_m=32, N=1536, K=4096)
+GROUPED_PREFILL = dict(E=16, rows_per_expert=1024, N=1536, K=4096)
+
+
+def _device_quantized(rows, cols, gen, block_rows):
+    """Seeded N(0,1) values drawn on the GPU and block-quantised with the
+    same recipe as synth (amax/448 scales), for operands too large to draw on
+    the host in a benchmark's set-up time."""
+    x = torch.randn(rows, cols, device="cuda", generator=gen)
+    return synth.quantize_blocks(x, block_rows, 128)
+
+
+def measure_grouped(hbm, fp8_peak):
+    import block_scaled_fp8_w8a8_gb300 as w8
+    out = {}
+    gen = torch.Generator(device="cuda").manual_seed(0)
+
+    def time_launches(launch, L=20):
+        stream = torch.cuda.Stream()
+        with torch.cuda.stream(stream):
+            launch(stream)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for _ in range(L):
+                launch(torch.cuda.current_stream())
+        g.replay()
+        torch.cuda.synchronize()
+        t_blk, _ = time_blocks(lambda k: g.replay(), 3, 1, 0.2)
+        return t_blk / (3 * L)
+
+    # decode, masked layout
+    c = GROUPED_DECODE
+    E, max_m, N, K = c["E"], c["max_m"], c["N"], c["K"]
+    G, NB = -(-K // 128), -(-N // 128)
+    cg = torch.Generator(device="cpu").manual_seed(0)
+    choice = torch.stack([torch.randperm(E, generator=cg)[:c["topk"]] for _ in range(c["tokens"])])
+    counts = torch.bincount(choice.flatten(), minlength=E).clamp(max=max_m).to(torch.int32)
+    B = torch.empty(E, N, K, dtype=torch.uint8, device="cuda")
+    b_s = torch.empty(E, NB, G, dtype=torch.float32, device="cuda")
+    for e in range(E):
+        B[e], b_s[e] = _device_quantized(N, K, gen, 128)
+    A, a_s = _device_quantized(E * max_m, K, gen, 1)
+    A, a_s = A.view(E, max_m, K), a_s.view(E, max_m, G)
+    C = torch.empty(E, max_m, N, dtype=torch.bfloat16, device="cuda")
+    dm = counts.cuda()
+    t = time_launches(lambda st: w8.check(w8.w8a8_block_fp8_grouped_matmul_masked(
+        A, a_s, B, b_s, C, dm, E, max_m, N, K, 128, 128, w8.W8A8_OUT_BF16, st,
+        w8.options(pdl=1))))
+    used = int((counts > 0).sum())
+    rows = int(counts.sum())
+    nbytes = used * (N * K + NB * G * 4) + rows * (K + G * 4 + 2 * N)
+    flops = 2 * rows * N * K
+    out["decode_masked"] = {
+        "config": dict(c, experts_with_tokens=used, routed_rows=rows),
+        "us": round(t * 1e6, 2), "gbs": round(nbytes / t / 1e9, 1),
+        "tflops": round(flops / t / 1e12, 2),
+        "roofline": {"bound": "hbm", "achieved": round(nbytes / t / 1e9, 1), "peak": hbm,
+                     "unit": "GB/s", "frac": round(nbytes / t / 1e9 / hbm, 4),
+                     "algorithmic_bytes": nbytes,
+                     "traffic": MEASURED_TRAFFIC.get((source_digest("matmul"),
+                                                      "grouped_decode_masked", 2))}}
+    del A, a_s, B, b_s, C
+    torch.cuda.empty_cache()
+
+    # prefill, contiguous layout
+    c = GROUPED_PREFILL
+    E, rpe, N, K = c["E"], c["rows_per_expert"], c["N"], c["K"]
+    M = E * rpe
+    B = torch.empty(E, N, K, dtype=torch.uint8, device="cuda")
+    b_s = torch.empty(E, NB, G, dtype=torch.float32, device="cuda")
+    for e in range(E):
+        B[e], b_s[e] = _device_quantized(N, K, gen, 128)
+    A, a_s = _device_quantized(M, K, gen, 1)
+    idx = torch.arange(E, dtype=torch.int32, device="cuda").repeat_interleave(rpe)
+    C = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    t = time_launches(lambda st: w8.check(w8.w8a8_block_fp8_grouped_matmul_contiguous(
+        A, a_s, B, b_s, C, idx, M, E, N, K, 128, 128, w8.W8A8_OUT_BF16, st,
+        w8.options(pdl=1))))
+    flops = 2 * M * N * K
+    out["prefill_contiguous"] = {
+        "config": c, "us": round(t * 1e6, 2), "tflops": round(flops / t / 1e12, 1),
+        "roofline": {"bound": "tensor", "achieved": round(flops / t / 1e12, 1), "peak": fp8_peak,
+                     "unit": "TFLOP/s", "frac": round(flops / t / 1e12 / fp8_peak, 4)}}
+    del A, a_s, B, b_s, C
+    torch.cuda.empty_cache()
+    return out
 
 
 def run_e2e(wl, args, world):

@@ -215,7 +215,8 @@ w8a8_status w8a8_block_fp8_matmul_splitk_noalloc(const void *A_dev, const float 
  *                (values are clamped to [0, max_m]).
  *   Rows of C at or past masked_m[e] are unspecified (they may be written).
  *   opts: variant AUTO/SWAPAB (default: one token tile of min(256, max_m
- *   rounded up to 16) rows per expert; m_tile and stages may be set) or
+ *   rounded up to 16) rows per expert, 4 pipeline stages; m_tile and stages
+ *   may be set) or
  *   SPLITK_CLUSTER with split_k; other variants are W8A8_ERR_UNSUPPORTED.
  *   With pdl = 1 the kernel overlaps the previous one's tail but streams no
  *   weights before the dependency wait (weights_static has no effect here).
