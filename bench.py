@@ -433,6 +433,7 @@ def run_ours(args, rank, world):
         result["value"], result["unit"] = result["tflops"], "TFLOP/s"
     if e2e is not None:
         result["e2e"] = e2e
+    result["launch_floor"] = measure_floor()
     if not args.no_quant:
         result["quantizer"] = measure_quantizer(hbm, l2)
     if not args.no_grouped:
@@ -511,6 +512,39 @@ def _device_quantized(rows, cols, gen, block_rows):
     the host in a benchmark's set-up time."""
     x = torch.randn(rows, cols, device="cuda", generator=gen)
     return synth.quantize_blocks(x, block_rows, 128)
+
+
+def measure_floor():
+    """Per-launch device time of the shortest links of a dependent kernel chain
+    (graphs of back-to-back launches with programmatic dependent launch): the
+    library's empty kernel, and the smallest matmul (M=1, N=8, K=16) -- the
+    floor under the decode shapes' launch durations."""
+    import block_scaled_fp8_w8a8_gb300 as w8
+
+    def per_launch(launch, L=64):
+        stream = torch.cuda.Stream()
+        with torch.cuda.stream(stream):
+            launch(stream)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for _ in range(L):
+                launch(torch.cuda.current_stream())
+        g.replay()
+        torch.cuda.synchronize()
+        t_blk, _ = time_blocks(lambda k: g.replay(), 5, 1, 0.1)
+        return round(t_blk / (5 * L) * 1e6, 3)
+
+    x = synth.make_inputs(1, 8, 16, seed=0)
+    A, a_s, B, b_s = (t.cuda() for t in (x.A, x.a_s, x.B, x.b_s))
+    C = torch.empty(1, 8, dtype=torch.bfloat16, device="cuda")
+    o = w8.options(pdl=1, weights_static=1)
+    return {
+        "empty_kernel_us": per_launch(lambda st: w8.check(w8.w8a8_launch_floor_kernel(1, st))),
+        "smallest_matmul_us": per_launch(lambda st: w8.check(w8.w8a8_block_fp8_matmul_ex(
+            A, a_s, B, b_s, C, 1, 8, 16, 128, 128, w8.W8A8_OUT_BF16, st, o))),
+        "note": "graphs of 64 back-to-back launches with programmatic dependent launch, "
+                "operands resident in L2"}
 
 
 def measure_grouped(hbm, fp8_peak):
@@ -600,22 +634,28 @@ def run_e2e(wl, args, world):
     for (M, N, K) in shapes:
         nb = w8.w8a8_block_fp8_host_staging_size(M, N, K, wl.out_code)
         stage.append(torch.empty(nb, dtype=torch.uint8, device="cuda"))
-    stream = torch.cuda.current_stream()
+    # The shapes of a step are independent problems: each goes on its own
+    # stream, so that their host<->device copies overlap on the copy engines.
+    streams = [torch.cuda.Stream() for _ in shapes]
     h2d = sum(sum(t.numel() * t.element_size() for t in p) for p in pinned)
     d2h = sum(o.numel() * o.element_size() for o in outs)
+    opts = []
+    for i in range(len(shapes)):
+        o = w8.options()
+        if wl.plans[i].workspace_bytes:
+            ws = wl.ws[0][i]
+            o.workspace_dev = ws.data_ptr()
+            o.workspace_bytes = ws.numel()
+        opts.append(o)
 
     def step(_k):
         for i, (M, N, K) in enumerate(shapes):
-            o = w8.options()
-            if wl.plans[i].workspace_bytes:
-                ws = wl.ws[0][i]
-                o.workspace_dev = ws.data_ptr()
-                o.workspace_bytes = ws.numel()
             st = w8.w8a8_block_fp8_matmul_host(*pinned[i], outs[i], M, N, K, 128, 128,
                                                wl.out_code, stage[i], stage[i].numel(),
-                                               stream, o)
+                                               streams[i], opts[i])
             w8.check(st)
-        stream.synchronize()    # the step's result is on the host
+        for s_ in streams:
+            s_.synchronize()    # the step's results are on the host
 
     for k in range(max(1, args.warmup)):
         step(k)
@@ -626,7 +666,9 @@ def run_e2e(wl, args, world):
     value = nbytes * world / t / 1e9 if bound == "hbm" else flops * world / t / 1e12
     return {"value": round(value, 3), "unit": "GB/s" if bound == "hbm" else "TFLOP/s",
             "ms_per_step": round(t * 1e3, 4), "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "path": "w8a8_block_fp8_matmul_host (C ABI, pinned host buffers)"}
+            "d2h_bytes_per_step": d2h,
+            "path": "w8a8_block_fp8_matmul_host (C ABI, pinned host buffers), one stream per "
+                    "shape of the step"}
 
 
 # ---------------------------------------------------------------------- CPU oracle

@@ -22,6 +22,7 @@ from ._binding import (  # noqa: F401
     w8a8_block_fp8_matmul_splitk_noalloc, W8A8_NOALLOC_SCRATCH_BYTES,
     w8a8_quantize_fp8_per_token_group, W8A8_IN_BF16, W8A8_IN_FP16, W8A8_IN_FP32,
     w8a8_block_fp8_grouped_matmul_masked, w8a8_block_fp8_grouped_matmul_contiguous,
+    w8a8_launch_floor_kernel,
     w8a8_get_device_status, w8a8_last_error, w8a8_options, w8a8_shutdown, w8a8_status_string,
 )
 

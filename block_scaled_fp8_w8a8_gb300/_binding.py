@@ -34,6 +34,7 @@ EXPORTED = (
     "w8a8_block_fp8_grouped_matmul_masked",
     "w8a8_block_fp8_grouped_matmul_contiguous",
     "w8a8_quantize_fp8_per_token_group",
+    "w8a8_launch_floor_kernel",
     "w8a8_block_fp8_host_staging_size",
     "w8a8_block_fp8_workspace_size",
     "w8a8_block_fp8_plan",
@@ -103,6 +104,8 @@ def load_library():
     lib.w8a8_block_fp8_grouped_matmul_contiguous.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64,
                                                              i64, i64, i32, i32, i32, vp, opt_p]
     lib.w8a8_block_fp8_grouped_matmul_contiguous.restype = ctypes.c_int
+    lib.w8a8_launch_floor_kernel.argtypes = [i32, vp]
+    lib.w8a8_launch_floor_kernel.restype = ctypes.c_int
     lib.w8a8_quantize_fp8_per_token_group.argtypes = [vp, i32, vp, vp, i64, i64, i32, vp]
     lib.w8a8_quantize_fp8_per_token_group.restype = ctypes.c_int
     lib.w8a8_block_fp8_host_staging_size.argtypes = [i64, i64, i64, i32]
@@ -202,6 +205,10 @@ def w8a8_block_fp8_grouped_matmul_contiguous(A, a_s, B, b_s, C, m_indices, M, E,
     return load_library().w8a8_block_fp8_grouped_matmul_contiguous(
         _ptr(A), _ptr(a_s), _ptr(B), _ptr(b_s), _ptr(C), _ptr(m_indices), M, E, N, K,
         block_n, block_k, out_dtype, _stream(stream), _opts(opts))
+
+
+def w8a8_launch_floor_kernel(pdl=1, stream=None) -> int:
+    return load_library().w8a8_launch_floor_kernel(pdl, _stream(stream))
 
 
 W8A8_IN_BF16, W8A8_IN_FP16, W8A8_IN_FP32 = 0, 1, 2

@@ -677,10 +677,39 @@ w8a8_status w8a8_block_fp8_matmul_host(const void *A_host, const float *a_s_host
                    {das, a_s_host, static_cast<size_t>(M * G * 4)},
                    {dB, B_host, static_cast<size_t>(N * K)},
                    {dbs, b_s_host, static_cast<size_t>(cdiv(N, 128) * G * 4)}};
-    for (const auto &c : copies) {
-        cudaError_t e = cudaMemcpyAsync(c.dst, c.src, c.n, cudaMemcpyHostToDevice, s);
+    // Page-locked host inputs that the device can address are gathered by one
+    // kernel (one launch instead of four copies, each with its own latency);
+    // anything else (pageable memory) goes through ordinary copies.
+    GatherSegs segs = {};
+    bool mapped = true;
+    for (int i = 0; i < 4 && mapped; ++i) {
+        cudaPointerAttributes attr;
+        if (cudaPointerGetAttributes(&attr, copies[i].src) != cudaSuccess ||
+            attr.type != cudaMemoryTypeHost || attr.devicePointer == nullptr) {
+            cudaGetLastError();     // a pageable pointer is not an error here
+            mapped = false;
+            break;
+        }
+        segs.src[i] = static_cast<const uint8_t *>(attr.devicePointer);
+        segs.dst[i] = static_cast<uint8_t *>(copies[i].dst);
+        segs.bytes[i] = copies[i].n;
+    }
+    if (mapped) {
+        segs.count = 4;
+        int dev = 0, sms = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e == cudaSuccess)
+            e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e == cudaSuccess)
+            e = launch_gather(segs, 2 * sms, s);
         if (e != cudaSuccess)
-            return cuda_fail(e, "cudaMemcpyAsync(host to device)");
+            return cuda_fail(e, "gather of the host inputs");
+    } else {
+        for (const auto &c : copies) {
+            cudaError_t e = cudaMemcpyAsync(c.dst, c.src, c.n, cudaMemcpyHostToDevice, s);
+            if (e != cudaSuccess)
+                return cuda_fail(e, "cudaMemcpyAsync(host to device)");
+        }
     }
     st = run(dA, reinterpret_cast<const float *>(das), dB, reinterpret_cast<const float *>(dbs),
              dC, M, N, K, block_n, block_k, out_dtype, s, opts);

@@ -73,6 +73,15 @@ struct SwapParams {
     int tiles_per_expert;
 };
 
+// Up to four byte ranges copied by one gather kernel (host-mapped sources).
+struct GatherSegs {
+    const uint8_t *src[4];
+    uint8_t *dst[4];
+    size_t bytes[4];
+    int count;
+};
+cudaError_t launch_gather(const GatherSegs &segs, int grid, cudaStream_t stream);
+
 struct LaunchCfg {
     int stages;
     int grid;        // persistent kernels: number of CTAs

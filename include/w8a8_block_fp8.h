@@ -144,9 +144,12 @@ w8a8_status w8a8_block_fp8_matmul_ex(const void *A_dev, const float *a_s_dev,
                                      const w8a8_options *opts);
 
 /*
- * End-to-end call on HOST buffers: copies A, a_s, B and b_s from host memory
- * (pinned memory gives asynchronous copies) into `staging_dev`, runs the
- * matmul, and copies C back into host memory, all in order on `stream`.  The
+ * End-to-end call on HOST buffers: brings A, a_s, B and b_s from host memory
+ * into `staging_dev`, runs the matmul, and copies C back into host memory, all
+ * in order on `stream`.  When all four inputs are page-locked host memory the
+ * device can address (e.g. cudaHostAlloc / torch pin_memory), one gather
+ * kernel reads them over the CPU-GPU link; otherwise they are copied with
+ * cudaMemcpyAsync (synchronous for pageable memory).  The
  * call returns once the work is enqueued; synchronise `stream` before reading
  * C_host.  staging_dev is caller-owned device memory of at least
  * w8a8_block_fp8_host_staging_size(M, N, K, out_dtype) bytes, 256-byte aligned.
@@ -280,6 +283,16 @@ typedef enum { W8A8_IN_BF16 = 0, W8A8_IN_FP16 = 1, W8A8_IN_FP32 = 2 } w8a8_in_dt
 w8a8_status w8a8_quantize_fp8_per_token_group(const void *X_dev, w8a8_in_dtype x_dtype,
                                               void *A_dev, float *a_s_dev, int64_t M, int64_t K,
                                               int group_size, w8a8_stream_t stream);
+
+/*
+ * Diagnostic: launches one empty CTA on `stream` that signals its dependents
+ * and waits for its predecessor (programmatic dependent launch when pdl = 1)
+ * and does nothing else.  A chain of these measures the shortest time one
+ * dependent kernel can take on the device, the floor under which no decode-size
+ * matmul launch can go; bench.py reports it beside the decode shapes.  The
+ * pages have no counterpart.  Errors: W8A8_ERR_CUDA (launch failed).
+ */
+w8a8_status w8a8_launch_floor_kernel(int pdl, w8a8_stream_t stream);
 
 /* Bytes of device staging that w8a8_block_fp8_matmul_host needs (0 for bad sizes). */
 size_t w8a8_block_fp8_host_staging_size(int64_t M, int64_t N, int64_t K, w8a8_out_dtype out_dtype);

@@ -172,6 +172,34 @@ def test_host_buffer_call_matches_device_call():
     assert torch.equal(C_host.view(torch.int16), dev.cpu().view(torch.int16))
 
 
+@pytest.mark.parametrize("kind", ["pageable", "pinned_misaligned"])
+def test_host_buffer_call_other_host_memory(kind):
+    """Pageable inputs take the copy path; pinned inputs at odd addresses take
+    the gather kernel's byte path.  Both give the device call's bits."""
+    M, N, K = 37, 264, 528
+    x = synth.make_inputs(M, N, K, seed=2)
+    dev = run(x, "bf16")
+    if kind == "pageable":
+        ins = [t.clone() for t in (x.A, x.a_s, x.B, x.b_s)]
+        ptrs = [t.data_ptr() for t in ins]
+    else:
+        ins, ptrs = [], []
+        for t in (x.A, x.a_s, x.B, x.b_s):
+            raw = t.contiguous().view(torch.uint8).flatten()
+            big = torch.empty(raw.numel() + 16, dtype=torch.uint8).pin_memory()
+            big[3:3 + raw.numel()] = raw
+            ins.append(big)
+            ptrs.append(big.data_ptr() + 3)
+    C_host = torch.empty((M, N), dtype=torch.bfloat16).pin_memory()
+    nbytes = w8.w8a8_block_fp8_host_staging_size(M, N, K, w8.W8A8_OUT_BF16)
+    staging = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    w8.check(w8.w8a8_block_fp8_matmul_host(*ptrs, C_host, M, N, K, staging_dev=staging,
+                                           staging_bytes=nbytes, stream=stream))
+    stream.synchronize()
+    assert torch.equal(C_host.view(torch.int16), dev.cpu().view(torch.int16))
+
+
 def test_invalid_calls_do_not_launch():
     x = synth.make_inputs(8, 128, 256, seed=0)
     A, a_s, B, b_s = to_device(x)
