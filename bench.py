@@ -372,7 +372,7 @@ def run_ours(args, rank, world):
         per_shape.append({"M": M, "N": N, "K": K, "us": round(t * 1e6, 3),
                           "tflops": round(fl / t / 1e12, 3), "gbs": round(by / t / 1e9, 1),
                           "variant": {1: "tiled", 2: "swapab", 3: "splitk",
-                                      4: "splitk_cluster"}.get(plan.variant, "?"),
+                                      4: "splitk_cluster", 5: "smallm"}.get(plan.variant, "?"),
                           "split_k": plan.split_k, "m_tile": plan.m_tile,
                           "block_n_tile": plan.block_n_tile})
     if per_shape:

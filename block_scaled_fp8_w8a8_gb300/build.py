@@ -15,7 +15,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 SRC = os.path.join(HERE, "csrc")
 OUT = os.path.join(HERE, "_build")
 LIB_NAME = "libw8a8_gb300.so"
-UNITS = ["api.cu", "status.cu", "gemm_tiled.cu", "gemm_swapab.cu", "noalloc.cu", "quant.cu", "hostio.cu"]
+UNITS = ["api.cu", "status.cu", "gemm_tiled.cu", "gemm_swapab.cu", "noalloc.cu", "quant.cu", "hostio.cu",
+         "gemm_smallm.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 HEADERS = ["ptx.cuh", "kernels.cuh", "dispatch_table.h", "tuning_table.inc"]
 

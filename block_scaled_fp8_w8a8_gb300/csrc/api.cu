@@ -196,7 +196,7 @@ w8a8_status check_options(const w8a8_options *o)
 {
     if (!o)
         return W8A8_OK;
-    if (o->variant < W8A8_VARIANT_AUTO || o->variant > W8A8_VARIANT_SPLITK_CLUSTER)
+    if (o->variant < W8A8_VARIANT_AUTO || o->variant > W8A8_VARIANT_SMALLM)
         return fail(W8A8_ERR_INVALID_ARG, "unknown variant %d", o->variant);
     if (o->split_k < 0 || o->stages < 0 || o->stages > 8 || o->grid_limit < 0 || o->m_tile < 0 ||
         o->debug_skip_load < 0)
@@ -258,6 +258,20 @@ w8a8_status make_plan(int64_t M, int64_t N, int64_t K, int out_bytes, const w8a8
         }
     }
     pl->variant = variant;
+
+    if (variant == W8A8_VARIANT_SMALLM) {
+        pl->smem = smallm_smem_bytes(static_cast<int>(std::min<int64_t>(M, 1 << 20)),
+                                     static_cast<int>(K));
+        if (pl->smem == 0)
+            return fail(W8A8_ERR_UNSUPPORTED, "the small-M variant takes M <= %d (M=%lld)",
+                        kSmallMaxM, static_cast<long long>(M));
+        if (pl->smem > dev.smem_optin)
+            return fail(W8A8_ERR_UNSUPPORTED,
+                        "the small-M variant needs %zu B of shared memory for M=%lld, K=%lld",
+                        pl->smem, static_cast<long long>(M), static_cast<long long>(K));
+        pl->grid = static_cast<int>(cdiv(N, 32));
+        return W8A8_OK;
+    }
 
     if (variant == W8A8_VARIANT_TILED) {
         int bn = bn_hint ? bn_hint : (N % 256 == 0 ? 256 : 128);
@@ -477,7 +491,26 @@ w8a8_status run(const void *A, const float *a_s, const void *B, const float *b_s
     cfg.stream = stream;
 
     cudaError_t e;
-    if (pl.variant == W8A8_VARIANT_TILED) {
+    if (pl.variant == W8A8_VARIANT_SMALLM) {
+        CUtensorMap mB;
+        if ((st = encode_u8_map(&mB, B, N, K, 32)) != W8A8_OK)
+            return st;
+        SmallParams p = {};
+        p.A = static_cast<const uint8_t *>(A);
+        p.a_s = a_s;
+        p.b_s = b_s;
+        p.C = C;
+        p.M = static_cast<int>(M);
+        p.N = static_cast<int>(N);
+        p.K = static_cast<int>(K);
+        p.G = G;
+        p.out_kind = out;
+        p.prefetch_weights = (o && o->pdl && o->weights_static) ? 1 : 0;
+        p.debug_skip_tma = debug_skip;
+        p.status = info.status;
+        p.wait_limit = limit;
+        e = launch_smallm(mB, p, cfg);
+    } else if (pl.variant == W8A8_VARIANT_TILED) {
         CUtensorMap mA, mB, mC;
         const int chunk_cols = out == W8A8_OUT_FP32 ? 16 : 32;   // 64 bytes of a row
         if ((st = encode_u8_map(&mA, A, M, K, 128)) != W8A8_OK ||

@@ -21,6 +21,7 @@ enum WaitSite : uint32_t {
     SITE_SWAP_PROMOTE = 8,
     SITE_DRAIN = 9,
     SITE_TILED_SCALES = 10,
+    SITE_SMALL_WEIGHTS = 11,
 };
 
 // Tokens on the MMA M side: one CTA per SM walks 128 x BN output tiles.
@@ -88,6 +89,23 @@ struct LaunchCfg {
     int pdl;
     cudaStream_t stream;
 };
+
+// Small M (at most kSmallMaxM tokens) on the CUDA cores: 32 weight rows per CTA.
+constexpr int kSmallMaxM = 16;
+struct SmallParams {
+    const uint8_t *A;      // [M, K]
+    const float *a_s;      // [M, G]
+    const float *b_s;      // [NB, G]
+    void *C;               // [M, N]
+    int M, N, K, G;
+    int out_kind;
+    int prefetch_weights;  // issue the weight loads before waiting on the previous grid
+    int debug_skip_tma;    // test hook: >= 0 skips the weight load of that K group
+    unsigned *status;
+    unsigned long long wait_limit;
+};
+size_t smallm_smem_bytes(int M, int K);     // 0: M outside 1..kSmallMaxM
+cudaError_t launch_smallm(const CUtensorMap &tmB, const SmallParams &p, const LaunchCfg &cfg);
 
 // Shared memory bytes each kernel configuration needs (0 = unsupported configuration).
 size_t tiled_smem_bytes(int bn, int stages);

@@ -73,6 +73,8 @@ def candidates(M, N, K, sms=152):
     if M >= 64:
         for bn, stages in ((256, 4), (256, 3), (192, 4), (128, 6), (128, 5), (128, 4)):
             out.append(dict(variant=b.W8A8_VARIANT_TILED, block_n_tile=bn, stages=stages))
+    if M <= 4:
+        out.append(dict(variant=b.W8A8_VARIANT_SMALLM))   # rejected where it does not fit
     if M <= 1024:
         r16 = lambda v: max(16, -(-v // 16) * 16)
         tiles = set()

@@ -75,10 +75,13 @@ typedef enum {
     W8A8_VARIANT_SWAPAB = 2,  /* C^T = B A^T: 128 weight rows per MMA, tokens on MMA N       */
     W8A8_VARIANT_SPLITK = 3,  /* swap-AB with the K groups split over CTAs + ordered reduce
                                  through a global workspace                                 */
-    W8A8_VARIANT_SPLITK_CLUSTER = 4  /* swap-AB split-K whose splits of a tile form one
+    W8A8_VARIANT_SPLITK_CLUSTER = 4, /* swap-AB split-K whose splits of a tile form one
                                         thread-block cluster (2..16 CTAs) and reduce their
                                         partials in rank order through distributed shared
                                         memory: no workspace; same bits as SPLITK          */
+    W8A8_VARIANT_SMALLM = 5          /* M <= 16: dot products on the CUDA cores, 32 weight
+                                        rows per CTA (no tensor memory); K limited by
+                                        shared memory (M x K x 4 + 32 x K bytes)            */
 } w8a8_variant;
 
 /*
