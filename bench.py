@@ -68,6 +68,8 @@ def parse():
                     help="skip the activation quantiser's own measurement")
     ap.add_argument("--no-grouped", action="store_true",
                     help="skip the grouped (MoE) matmul measurements")
+    ap.add_argument("--no-fused", action="store_true",
+                    help="skip the bf16-activation (quantise + matmul) measurement")
     ap.add_argument("--no-per-shape", action="store_true",
                     help="skip the per-shape launch timing (keeps an ncu launch list short)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
@@ -438,6 +440,8 @@ def run_ours(args, rank, world):
         result["quantizer"] = measure_quantizer(hbm, l2)
     if not args.no_grouped:
         result["grouped"] = measure_grouped(hbm, 2.0 * bf16)
+    if not args.no_fused and bound == "hbm":
+        result["from_bf16_activations"] = measure_fused(shapes, l2)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(shapes, wl.host, args.out_dtype, bound,
                                               args.cpu_seconds)
@@ -545,6 +549,60 @@ def measure_floor():
             A, a_s, B, b_s, C, 1, 8, 16, 128, 128, w8.W8A8_OUT_BF16, st, o))),
         "note": "graphs of 64 back-to-back launches with programmatic dependent launch, "
                 "operands resident in L2"}
+
+
+def measure_fused(shapes, l2):
+    """The decode step from bf16 activations, per shape: the quantiser then
+    the matmul (two launches chained with programmatic dependent launch) and
+    the fused call (one launch), each from a CUDA graph of back-to-back calls
+    over rotating inputs larger than L2."""
+    import block_scaled_fp8_w8a8_gb300 as w8
+    out = []
+    for (M, N, K) in shapes:
+        G = -(-K // 128)
+        per = M * K * 2 + N * K + M * N * 2
+        sets = max(2, int(-(-2 * l2 // per)) + 1)
+        xs = [synth.activations(M, K, seed=r, dtype=torch.bfloat16).cuda() for r in range(sets)]
+        w = synth.make_inputs(1, N, K, seed=0)
+        Bs = [w.B.cuda() for _ in range(sets)]
+        b_s = w.b_s.cuda()
+        A = torch.empty(M, K, dtype=torch.uint8, device="cuda")
+        a_s = torch.empty(M, G, dtype=torch.float32, device="cuda")
+        C = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+        o = w8.options(pdl=1, weights_static=1)
+        L = max(sets, 64)
+
+        def two(r, st):
+            w8.check(w8.w8a8_quantize_fp8_per_token_group(xs[r], w8.W8A8_IN_BF16, A, a_s, M, K,
+                                                          128, st))
+            w8.check(w8.w8a8_block_fp8_matmul_ex(A, a_s, Bs[r], b_s, C, M, N, K, 128, 128,
+                                                 w8.W8A8_OUT_BF16, st, o))
+
+        def one(r, st):
+            w8.check(w8.w8a8_block_fp8_quant_matmul(xs[r], w8.W8A8_IN_BF16, Bs[r], b_s, C, M, N,
+                                                    K, 128, 128, w8.W8A8_OUT_BF16, st, o))
+
+        res = {"M": M, "N": N, "K": K}
+        for name, fn in (("quantize_then_matmul_us", two), ("fused_us", one)):
+            stream = torch.cuda.Stream()
+            with torch.cuda.stream(stream):
+                for r in range(sets):
+                    fn(r, stream)
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for j in range(L):
+                    fn(j % sets, torch.cuda.current_stream())
+            g.replay()
+            torch.cuda.synchronize()
+            t_blk, _ = time_blocks(lambda k: g.replay(), 5, 1, 0.1)
+            res[name] = round(t_blk / (5 * L) * 1e6, 3)
+        out.append(res)
+        del xs, Bs, g
+    return {"op": "C = matmul(quantise(X bf16), B): two launches vs the fused call",
+            "per_shape": out,
+            "step_us": {"quantize_then_matmul": round(sum(r["quantize_then_matmul_us"] for r in out), 3),
+                        "fused": round(sum(r["fused_us"] for r in out), 3)}}
 
 
 def measure_grouped(hbm, fp8_peak):

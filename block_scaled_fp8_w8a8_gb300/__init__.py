@@ -22,7 +22,7 @@ from ._binding import (  # noqa: F401
     w8a8_block_fp8_matmul_splitk_noalloc, W8A8_NOALLOC_SCRATCH_BYTES,
     w8a8_quantize_fp8_per_token_group, W8A8_IN_BF16, W8A8_IN_FP16, W8A8_IN_FP32,
     w8a8_block_fp8_grouped_matmul_masked, w8a8_block_fp8_grouped_matmul_contiguous,
-    w8a8_launch_floor_kernel,
+    w8a8_launch_floor_kernel, w8a8_block_fp8_quant_matmul,
     w8a8_get_device_status, w8a8_last_error, w8a8_options, w8a8_shutdown, w8a8_status_string,
 )
 
@@ -137,4 +137,26 @@ def grouped_matmul_contiguous(A, a_s, B, b_s, m_indices, out_dtype="bf16", out=N
     check(w8a8_block_fp8_grouped_matmul_contiguous(A, a_s, B, b_s, out, m_indices, M, E, N, K,
                                                    128, 128, code, stream,
                                                    options(**opts) if opts else None))
+    return out
+
+
+def quant_matmul(X, B, b_s, out_dtype="bf16", out=None, stream=None, **opts):
+    """C = matmul(quantize_fp8_per_token_group(X), B) in one launch, on CUDA
+    tensors: X [M, K] bf16/fp16/fp32, B uint8/float8_e4m3fn [N, K], b_s float32
+    [ceil(N/128), K/128].  Same bits as the two calls in sequence."""
+    import torch
+    M, K = X.shape
+    N = B.shape[0]
+    code = out_code(out_dtype)
+    xk = {torch.bfloat16: W8A8_IN_BF16, torch.float16: W8A8_IN_FP16,
+          torch.float32: W8A8_IN_FP32}.get(X.dtype)
+    if xk is None:
+        raise W8A8Error(W8A8_ERR_INVALID_ARG, f"unsupported activation dtype {X.dtype}")
+    if out is None:
+        out = _out_tensor((M, N), code, X.device)
+    for t in (X, B, b_s, out):
+        if not t.is_contiguous():
+            raise W8A8Error(W8A8_ERR_UNSUPPORTED, "tensors must be contiguous row-major")
+    check(w8a8_block_fp8_quant_matmul(X, xk, B, b_s, out, M, N, K, 128, 128, code, stream,
+                                      options(**opts) if opts else None))
     return out

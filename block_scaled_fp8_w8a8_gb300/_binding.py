@@ -36,6 +36,7 @@ EXPORTED = (
     "w8a8_block_fp8_grouped_matmul_contiguous",
     "w8a8_quantize_fp8_per_token_group",
     "w8a8_launch_floor_kernel",
+    "w8a8_block_fp8_quant_matmul",
     "w8a8_block_fp8_host_staging_size",
     "w8a8_block_fp8_workspace_size",
     "w8a8_block_fp8_plan",
@@ -105,6 +106,9 @@ def load_library():
     lib.w8a8_block_fp8_grouped_matmul_contiguous.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64,
                                                              i64, i64, i32, i32, i32, vp, opt_p]
     lib.w8a8_block_fp8_grouped_matmul_contiguous.restype = ctypes.c_int
+    lib.w8a8_block_fp8_quant_matmul.argtypes = [vp, i32, vp, vp, vp, i64, i64, i64, i32, i32, i32,
+                                                vp, opt_p]
+    lib.w8a8_block_fp8_quant_matmul.restype = ctypes.c_int
     lib.w8a8_launch_floor_kernel.argtypes = [i32, vp]
     lib.w8a8_launch_floor_kernel.restype = ctypes.c_int
     lib.w8a8_quantize_fp8_per_token_group.argtypes = [vp, i32, vp, vp, i64, i64, i32, vp]
@@ -206,6 +210,13 @@ def w8a8_block_fp8_grouped_matmul_contiguous(A, a_s, B, b_s, C, m_indices, M, E,
     return load_library().w8a8_block_fp8_grouped_matmul_contiguous(
         _ptr(A), _ptr(a_s), _ptr(B), _ptr(b_s), _ptr(C), _ptr(m_indices), M, E, N, K,
         block_n, block_k, out_dtype, _stream(stream), _opts(opts))
+
+
+def w8a8_block_fp8_quant_matmul(X, x_dtype, B, b_s, C, M, N, K, block_n=128, block_k=128,
+                                out_dtype=W8A8_OUT_BF16, stream=None, opts=None) -> int:
+    return load_library().w8a8_block_fp8_quant_matmul(
+        _ptr(X), x_dtype, _ptr(B), _ptr(b_s), _ptr(C), M, N, K, block_n, block_k, out_dtype,
+        _stream(stream), _opts(opts))
 
 
 def w8a8_launch_floor_kernel(pdl=1, stream=None) -> int:

@@ -226,7 +226,7 @@ struct Plan {
 };
 
 w8a8_status make_plan(int64_t M, int64_t N, int64_t K, int out_bytes, const w8a8_options *o,
-                      const DeviceInfo &dev, Plan *pl)
+                      const DeviceInfo &dev, Plan *pl, int x_esize = 0)
 {
     const int G = static_cast<int>(cdiv(K, 128));
     const int NB = static_cast<int>(cdiv(N, 128));
@@ -326,9 +326,9 @@ w8a8_status make_plan(int64_t M, int64_t N, int64_t K, int out_bytes, const w8a8
     const int tile_bytes = (cluster && splits > 1) ? 4 : out_bytes;
     int max_stages = std::min(8, gps);
     int stages = stage_hint ? std::min(stage_hint, max_stages) : max_stages;
-    while (stages > 1 && swapab_smem_bytes(mt, stages, gps, tile_bytes) > dev.smem_optin)
+    while (stages > 1 && swapab_smem_bytes(mt, stages, gps, tile_bytes, x_esize) > dev.smem_optin)
         --stages;
-    if (swapab_smem_bytes(mt, stages, gps, tile_bytes) > dev.smem_optin)
+    if (swapab_smem_bytes(mt, stages, gps, tile_bytes, x_esize) > dev.smem_optin)
         return fail(W8A8_ERR_UNSUPPORTED,
                     "K=%lld is too long for one swap-AB CTA; use the split-K variant",
                     (long long)K);
@@ -338,7 +338,7 @@ w8a8_status make_plan(int64_t M, int64_t N, int64_t K, int out_bytes, const w8a8
     pl->splits = splits;
     pl->gps = gps;
     pl->stages = stages;
-    pl->smem = swapab_smem_bytes(mt, stages, gps, tile_bytes);
+    pl->smem = swapab_smem_bytes(mt, stages, gps, tile_bytes, x_esize);
     pl->tile_bytes = tile_bytes;
     if (splits == 1)
         pl->variant = W8A8_VARIANT_SWAPAB;
@@ -405,9 +405,17 @@ struct Grouping {
     int64_t experts = 0;
 };
 
+// Fused calls: the activation X (bf16, fp16 or fp32) is quantised per
+// (token, 128-column group) inside the swap-AB kernel; A and a_s are unused.
+struct FusedAct {
+    const void *X = nullptr;
+    int kind = 0;
+};
+
 w8a8_status run(const void *A, const float *a_s, const void *B, const float *b_s, void *C,
                 int64_t M, int64_t N, int64_t K, int block_n, int block_k, int out,
-                cudaStream_t stream, const w8a8_options *o, const Grouping &gr = Grouping())
+                cudaStream_t stream, const w8a8_options *o, const Grouping &gr = Grouping(),
+                const FusedAct &fa = FusedAct())
 {
     g_last_error[0] = '\0';
     w8a8_status st = check_problem(M, N, K, block_n, block_k, out);
@@ -415,6 +423,19 @@ w8a8_status run(const void *A, const float *a_s, const void *B, const float *b_s
         return st;
     if ((st = check_options(o)) != W8A8_OK)
         return st;
+    const bool fused = fa.X != nullptr;
+    if (fused) {
+        if (fa.kind < W8A8_IN_BF16 || fa.kind > W8A8_IN_FP32)
+            return fail(W8A8_ERR_INVALID_ARG, "unknown activation dtype %d", fa.kind);
+        const int v = o ? o->variant : W8A8_VARIANT_AUTO;
+        if (v != W8A8_VARIANT_AUTO && v != W8A8_VARIANT_SWAPAB && v != W8A8_VARIANT_SPLITK_CLUSTER)
+            return fail(W8A8_ERR_UNSUPPORTED, "the fused activation quantiser runs in the "
+                                              "swap-AB kernel (variant AUTO, SWAPAB or SPLITK_CLUSTER)");
+        if (!aligned(fa.X, 16))
+            return fail(W8A8_ERR_UNSUPPORTED, "X must be 16-byte aligned");
+        A = fa.X;            // stands in for the unused operands in the checks below
+        a_s = b_s;
+    }
     const bool masked = gr.mode == Grouping::MASKED, contiguous = gr.mode == Grouping::CONTIGUOUS;
     if (gr.mode != Grouping::NONE) {
         if (gr.experts < 0)
@@ -464,6 +485,19 @@ w8a8_status run(const void *A, const float *a_s, const void *B, const float *b_s
             forced.m_tile = static_cast<int>(std::min<int64_t>(256, cdiv(M, 16) * 16));
         if (!forced.stages)
             forced.stages = 4;
+    } else if (fused && forced.variant == W8A8_VARIANT_AUTO) {
+        // The measured entry when it is a swap-AB one; otherwise the swap-AB
+        // rules (split-K stays in clusters: no workspace for a fused call).
+        const TableEntry *t = lookup_tuned(M, N, K);
+        forced.variant = W8A8_VARIANT_SWAPAB;
+        if (t && (t->variant == W8A8_VARIANT_SWAPAB || t->variant == W8A8_VARIANT_SPLITK_CLUSTER ||
+                  (t->variant == W8A8_VARIANT_SPLITK && t->split_k <= 16))) {
+            forced.variant = t->variant == W8A8_VARIANT_SWAPAB ? W8A8_VARIANT_SWAPAB
+                                                               : W8A8_VARIANT_SPLITK_CLUSTER;
+            if (!forced.split_k) forced.split_k = t->split_k;
+            if (!forced.m_tile) forced.m_tile = t->m_tile;
+            if (!forced.stages) forced.stages = t->stages;
+        }
     } else if (contiguous && forced.variant == W8A8_VARIANT_AUTO) {
         forced.variant = W8A8_VARIANT_TILED;
         const TableEntry *t = lookup_tuned(M, N, K);
@@ -472,8 +506,10 @@ w8a8_status run(const void *A, const float *a_s, const void *B, const float *b_s
             if (!forced.stages) forced.stages = t->stages;
         }
     }
+    const int x_esize = fused ? (fa.kind == W8A8_IN_FP32 ? 4 : 2) : 0;
     if ((st = make_plan(M, N, K, out == W8A8_OUT_FP32 ? 4 : 2,
-                        gr.mode != Grouping::NONE ? &forced : o, info, &pl)) != W8A8_OK)
+                        (gr.mode != Grouping::NONE || fused) ? &forced : o, info, &pl,
+                        x_esize)) != W8A8_OK)
         return st;
     if (masked && static_cast<int64_t>(pl.m_tiles) * gr.experts > 65535)
         return fail(W8A8_ERR_UNSUPPORTED, "%lld experts x %d token tiles exceed the grid",
@@ -540,8 +576,11 @@ w8a8_status run(const void *A, const float *a_s, const void *B, const float *b_s
     } else {
         CUtensorMap mW, mX, mC;
         const int64_t slabs = masked ? gr.experts : 0;
+        // (fused: mX maps the unquantised X, 128 columns by mma_n rows, no swizzle)
         if ((st = encode_u8_map(&mW, B, N, K, 128, slabs)) != W8A8_OK ||
-            (st = encode_u8_map(&mX, A, M, K, pl.mma_n, slabs)) != W8A8_OK ||
+            (st = fused ? encode_out_map(&mX, const_cast<void *>(fa.X), M, K, fa.kind, 128,
+                                         pl.mma_n, CU_TENSOR_MAP_SWIZZLE_NONE)
+                        : encode_u8_map(&mX, A, M, K, pl.mma_n, slabs)) != W8A8_OK ||
             (st = encode_out_map(&mC, C, M, N, out, 128, pl.mma_n, CU_TENSOR_MAP_SWIZZLE_NONE,
                                  slabs)) != W8A8_OK)
             return st;
@@ -552,8 +591,9 @@ w8a8_status run(const void *A, const float *a_s, const void *B, const float *b_s
         p.ws = nullptr;
         p.counters = nullptr;
         const size_t ws_bytes = splitk_workspace_bytes(M, N, pl);
-        if (ws_bytes && masked)
-            return fail(W8A8_ERR_UNSUPPORTED, "the masked layout splits K only in clusters");
+        if (ws_bytes && (masked || fused))
+            return fail(W8A8_ERR_UNSUPPORTED, "%s splits K only in clusters",
+                        masked ? "the masked layout" : "a fused call");
         if (ws_bytes) {
             if (static_cast<size_t>(pl.m_tiles) * NB > kCounterWords)
                 return fail(W8A8_ERR_UNSUPPORTED, "split-K over %lld output tiles (max %zu)",
@@ -580,6 +620,8 @@ w8a8_status run(const void *A, const float *a_s, const void *B, const float *b_s
         p.masked_m = masked ? gr.ids : nullptr;
         p.experts = masked ? static_cast<int>(gr.experts) : 1;
         p.tiles_per_expert = pl.m_tiles;
+        p.X = fused ? fa.X : nullptr;
+        p.x_kind = fa.kind;
         p.splits = pl.splits;
         p.groups_per_split = pl.gps;
         p.out_kind = out;
@@ -628,6 +670,21 @@ w8a8_status w8a8_block_fp8_matmul_ex(const void *A_dev, const float *a_s_dev, co
 {
     return run(A_dev, a_s_dev, B_dev, b_s_dev, C_dev, M, N, K, block_n, block_k, out_dtype,
                reinterpret_cast<cudaStream_t>(stream), opts);
+}
+
+w8a8_status w8a8_block_fp8_quant_matmul(const void *X_dev, w8a8_in_dtype x_dtype, const void *B_dev,
+                                        const float *b_s_dev, void *C_dev, int64_t M, int64_t N,
+                                        int64_t K, int block_n, int block_k,
+                                        w8a8_out_dtype out_dtype, w8a8_stream_t stream,
+                                        const w8a8_options *opts)
+{
+    if (!X_dev && M > 0)
+        return fail(W8A8_ERR_INVALID_ARG, "null pointer argument");
+    FusedAct fa;
+    fa.X = X_dev;
+    fa.kind = x_dtype;
+    return run(nullptr, nullptr, B_dev, b_s_dev, C_dev, M, N, K, block_n, block_k, out_dtype,
+               reinterpret_cast<cudaStream_t>(stream), opts, Grouping(), fa);
 }
 
 w8a8_status w8a8_block_fp8_grouped_matmul_masked(const void *A_dev, const float *a_s_dev,

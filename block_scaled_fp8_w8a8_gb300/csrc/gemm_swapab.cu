@@ -24,6 +24,7 @@
 // through the workspace and a vectorised ordered reduction.
 #include "kernels.cuh"
 #include "ptx.cuh"
+#include "quant_math.cuh"
 
 namespace w8a8 {
 
@@ -43,15 +44,23 @@ template <int MT> struct SwapLayout {
     static constexpr uint32_t kTmemCols = 2 * MT < 32 ? 32 : 2 * MT;
     static constexpr int kBars = 2 * kMaxStages + 5;
     // Operand stages; after the main loop the same bytes hold the C tile.
-    __host__ __device__ static size_t area(int stages, int out_bytes)
+    // Fused activation quantisation adds, per stage, the unquantised token
+    // tile as the TMA brings it: MT rows of 128 elements of x_esize bytes.
+    __host__ __device__ static uint32_t xstage_bytes(int x_esize)
     {
-        const size_t st = static_cast<size_t>(stages) * (kWBytes + kXBytes);
+        return static_cast<uint32_t>(MT) * 128u * static_cast<uint32_t>(x_esize);
+    }
+    __host__ __device__ static size_t area(int stages, int out_bytes, int x_esize = 0)
+    {
+        const size_t st = static_cast<size_t>(stages) * (kWBytes + kXBytes + xstage_bytes(x_esize));
         const size_t ct = static_cast<size_t>(MT) * 128 * out_bytes;
         return st > ct ? st : ct;
     }
-    static size_t smem(int stages, int gps, int out_bytes)
+    static size_t smem(int stages, int gps, int out_bytes, int x_esize = 0)
     {
-        return 1024 + area(stages, out_bytes) + static_cast<size_t>(gps) * MT * 4 + kBars * 8 + 16;
+        // + one "activation codes ready" barrier per K group (fused quantisation)
+        return 1024 + area(stages, out_bytes, x_esize) + static_cast<size_t>(gps) * MT * 4 + kBars * 8 + 16 +
+               static_cast<size_t>(gps) * 8;
     }
 };
 
@@ -80,10 +89,80 @@ __device__ __forceinline__ void add4(float4 &a, const float4 &b)
     a.w += b.w;
 }
 
+// Fused activation quantisation: warps 2 and 3 (idle in the plain kernel) turn
+// the token tile's rows of one K group of X (bf16, fp16 or fp32; brought into
+// the stage by the producer's TMA, rows past M and columns past K read as
+// zeros) into E4M3 codes in the operand stage, in the 128-byte-swizzled layout
+// a TMA load of the quantised operand would produce (16-byte chunk c of row j
+// at (c ^ (j & 7))), and write the folded scales s * b_s[nb, g] for the
+// group's promotion -- with the stand-alone quantiser's arithmetic, so that
+// the result equals quantise-then-multiply bit for bit.  Eight lanes per row,
+// 16 elements each; rows past M (and tile rows past mma_n) get zero scales and
+// no codes (their token columns are never stored).
+template <int KIND, int MT>
+__device__ __forceinline__ void quantize_group(const SwapParams &p, uint32_t xsrc, uint32_t xdst,
+                                               float *scales, int m0, float bsv, int qt)
+{
+    constexpr int kEsize = KIND == W8A8_IN_FP32 ? 4 : 2;
+    constexpr int kWords = KIND == W8A8_IN_FP32 ? 16 : 8;
+    // Rows handled together by a team: independent chains that the scheduler
+    // interleaves (the largest tile runs these warps on 56 registers: one row).
+    constexpr int kBatch = MT >= 256 ? 1 : (MT / 8 < 4 ? MT / 8 : 4);
+    const int team = qt >> 3, lane8 = qt & 7;
+    for (int j0 = team; j0 < MT; j0 += 8 * kBatch) {
+        uint32_t w[kBatch][kWords];
+        float sc[kBatch];
+#pragma unroll
+        for (int r = 0; r < kBatch; ++r) {
+            const int j = j0 + 8 * r;
+            if (j < p.mma_n && m0 + j < p.M) {
+                const uint32_t src = xsrc + static_cast<uint32_t>((j * 128 + 16 * lane8) * kEsize);
+#pragma unroll
+                for (int i = 0; i < kWords / 4; ++i)
+                    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                                 : "=r"(w[r][4 * i]), "=r"(w[r][4 * i + 1]), "=r"(w[r][4 * i + 2]),
+                                   "=r"(w[r][4 * i + 3])
+                                 : "r"(src + 16u * i));
+            } else {
+#pragma unroll
+                for (int i = 0; i < kWords; ++i)
+                    w[r][i] = 0u;
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < kBatch; ++r)
+            sc[r] = quant::amax16<KIND>(w[r]);
+#pragma unroll
+        for (int off = 4; off > 0; off >>= 1)
+#pragma unroll
+            for (int r = 0; r < kBatch; ++r)
+                sc[r] = fmaxf(sc[r], __shfl_xor_sync(0xffffffffu, sc[r], off));
+#pragma unroll
+        for (int r = 0; r < kBatch; ++r) {
+            const int j = j0 + 8 * r;
+            // Token columns past M never leave the kernel (the store clips them)
+            // and have zero scales: their codes are left as they are.
+            float folded = 0.f;
+            if (j < p.mma_n && m0 + j < p.M) {
+                const float scale = quant::group_scale(sc[r]);
+                const uint4 codes = quant::encode16<KIND>(w[r], scale);
+                const uint32_t dst = xdst + static_cast<uint32_t>(j) * 128u +
+                                     static_cast<uint32_t>((lane8 ^ (j & 7)) * 16);
+                asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(codes.x),
+                             "r"(codes.y), "r"(codes.z), "r"(codes.w)
+                             : "memory");
+                folded = scale * bsv;
+            }
+            if (lane8 == 0 && j < MT)
+                scales[j] = folded;
+        }
+    }
+}
+
 // GROUPED selects the masked MoE layout at compile time, so that the plain
 // kernel carries none of its bookkeeping (the largest token tile's promotion
 // loop uses every register the launch allows).
-template <int MT, bool GROUPED>
+template <int MT, bool GROUPED, bool FUSED>
 __global__ void __launch_bounds__(SwapLayout<MT>::kThreads, SwapLayout<MT>::kMinBlocks)
     k_swapab(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
              const __grid_constant__ CUtensorMap tmC, const SwapParams p, const int stages)
@@ -94,7 +173,10 @@ __global__ void __launch_bounds__(SwapLayout<MT>::kThreads, SwapLayout<MT>::kMin
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const uint32_t sW = smem_addr(smem);
     const uint32_t sX = sW + stages * L::kWBytes;
-    float *sscale = reinterpret_cast<float *>(smem + L::area(stages, p.out_bytes));
+    const int x_esize = FUSED ? (p.x_kind == W8A8_IN_FP32 ? 4 : 2) : 0;
+    const uint32_t sXs = sX + stages * L::kXBytes;          // FUSED: unquantised tiles
+    const uint32_t xs_bytes = L::xstage_bytes(x_esize);
+    float *sscale = reinterpret_cast<float *>(smem + L::area(stages, p.out_bytes, x_esize));
     uint64_t *bars = reinterpret_cast<uint64_t *>(sscale + p.groups_per_split * MT);
     const uint32_t bar0 = smem_addr(bars);
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
@@ -106,6 +188,10 @@ __global__ void __launch_bounds__(SwapLayout<MT>::kThreads, SwapLayout<MT>::kMin
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     volatile int *last_flag = reinterpret_cast<volatile int *>(tmem_slot + 2);
     volatile int *rows_slot = reinterpret_cast<volatile int *>(tmem_slot + 3);
+    // FUSED: one barrier per K group of this CTA, completed by the two
+    // quantiser warps once the group's codes and scales are in shared memory.
+    const uint32_t ready0 = smem_addr(tmem_slot + 4);
+    auto ready_bar = [&](int i) { return ready0 + 8u * i; };
 
     const uint32_t warp = warp_index(), lane = lane_index();
     const int nb = blockIdx.x;                 // 128-row block of B (and of C's columns)
@@ -130,6 +216,9 @@ __global__ void __launch_bounds__(SwapLayout<MT>::kThreads, SwapLayout<MT>::kMin
             mbar_init(tempty_bar(b), 4 * L::kPromoWG);
         }
         mbar_init(drain_bar, 1);
+        if constexpr (FUSED)
+            for (int i = 0; i < p.groups_per_split; ++i)
+                mbar_init(ready_bar(i), 2);
         *abort_flag = 0;
         *last_flag = 0;
         mbar_fence_init();
@@ -182,7 +271,8 @@ __global__ void __launch_bounds__(SwapLayout<MT>::kThreads, SwapLayout<MT>::kMin
             regs_dealloc<56>();     // 128 x 56 + 256 x 224 = 384 x 168 (the launch's registers)
         if (is_producer) {
             // ---------------------------------------------------------- TMA producer
-            const uint32_t tx = L::kWBytes + static_cast<uint32_t>(p.mma_n) * 128u;
+            const uint32_t tx = L::kWBytes + static_cast<uint32_t>(p.mma_n) * 128u *
+                                                 static_cast<uint32_t>(FUSED ? x_esize : 1);
             // Weights do not depend on the previous grid when the caller says so:
             // start the first stages' B loads before waiting for it.
             const int pre = p.prefetch_weights ? min(stages, ng) : 0;
@@ -220,7 +310,9 @@ __global__ void __launch_bounds__(SwapLayout<MT>::kThreads, SwapLayout<MT>::kMin
                     }
                 }
                 if (i != p.debug_skip_tma) {
-                    if constexpr (grouped)
+                    if constexpr (FUSED)
+                        tma_load_2d(sXs + stage * xs_bytes, &tmX, full_bar(stage), g * 128, m0);
+                    else if constexpr (grouped)
                         tma_load_3d(sX + stage * L::kXBytes, &tmX, full_bar(stage), g * 128, m0,
                                     expert);
                     else
@@ -266,7 +358,8 @@ __global__ void __launch_bounds__(SwapLayout<MT>::kThreads, SwapLayout<MT>::kMin
                 const uint32_t buf = i & 1;
                 const uint32_t bphase = (i >> 1) & 1;
                 if (!wait_bounded(tempty_bar(buf), bphase ^ 1u, guard, SITE_SWAP_MMA_TMEM) ||
-                    !wait_bounded(full_bar(stage), phase, guard, SITE_SWAP_MMA_FULL)) {
+                    !wait_bounded(full_bar(stage), phase, guard, SITE_SWAP_MMA_FULL) ||
+                    (FUSED && !wait_bounded(ready_bar(i), 0, guard, SITE_SWAP_QUANT))) {
                     ok = false;
                     break;
                 }
@@ -288,6 +381,41 @@ __global__ void __launch_bounds__(SwapLayout<MT>::kThreads, SwapLayout<MT>::kMin
                 mma_commit(drain_bar);
                 wait_drain(drain_bar, 0, p.status, p.wait_limit, (SITE_DRAIN << 8) | 4u);
             }
+        } else if (FUSED && warp >= 2) {
+            // ---------------------------------------------------------- activation quantiser
+            const int qt = static_cast<int>(threadIdx.x) - 64;
+            int stage = 0;
+            uint32_t phase = 0;
+            const float *bs_row = p.b_s + static_cast<size_t>(nb) * p.G;
+            float bsv_next = ng > 0 ? __ldg(bs_row + g_begin) : 0.f;
+            for (int i = 0; i < ng; ++i) {
+                const float bsv = bsv_next;          // loaded one group ahead
+                if (i + 1 < ng)
+                    bsv_next = __ldg(bs_row + g_begin + i + 1);
+                // The stage's unquantised tile has landed (the producer reuses a
+                // stage only after the MMA has released it, so its codes area is
+                // free as well).
+                if (!__all_sync(0xffffffffu, wait_bounded(full_bar(stage), phase, guard,
+                                                          SITE_SWAP_QUANT)))
+                    break;
+                const uint32_t xsrc = sXs + stage * xs_bytes;
+                const uint32_t xdst = sX + stage * L::kXBytes;
+                float *scales = sscale + i * MT;
+                if (p.x_kind == W8A8_IN_BF16)
+                    quantize_group<W8A8_IN_BF16, MT>(p, xsrc, xdst, scales, m0, bsv, qt);
+                else if (p.x_kind == W8A8_IN_FP16)
+                    quantize_group<W8A8_IN_FP16, MT>(p, xsrc, xdst, scales, m0, bsv, qt);
+                else
+                    quantize_group<W8A8_IN_FP32, MT>(p, xsrc, xdst, scales, m0, bsv, qt);
+                fence_async_smem();          // the codes are read by the tensor cores
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(ready_bar(i));
+                if (++stage == stages) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
         }
         __syncwarp();
     } else {
@@ -304,7 +432,9 @@ __global__ void __launch_bounds__(SwapLayout<MT>::kThreads, SwapLayout<MT>::kMin
 
         // Folded scales s[g][j] = a_s[m0+j, g] * b_s[nb, g] (zero past the
         // tile's valid rows; a grouped tile reads its expert's slabs).
-        if constexpr (grouped) {
+        if constexpr (FUSED) {
+            // the quantiser warps write the folded scales group by group
+        } else if constexpr (grouped) {
             const size_t a_row0 = static_cast<size_t>(expert) * p.M + m0;
             const size_t b_row = static_cast<size_t>(expert) * p.NB + nb;
             const int tile_rows = *rows_slot;
@@ -330,7 +460,8 @@ __global__ void __launch_bounds__(SwapLayout<MT>::kThreads, SwapLayout<MT>::kMin
                 sscale[idx] = v;
             }
         }
-        named_barrier(1, kPromoThreads);
+        if constexpr (!FUSED)
+            named_barrier(1, kPromoThreads);
 
         float acc[L::kCols];
 #pragma unroll
@@ -344,7 +475,8 @@ __global__ void __launch_bounds__(SwapLayout<MT>::kThreads, SwapLayout<MT>::kMin
             // warp proceeds only if every lane saw the buffer (tcgen05.ld below
             // is a warp-wide instruction).
             ok = __all_sync(0xffffffffu,
-                            wait_bounded(tfull_bar(buf), bphase, guard, SITE_SWAP_PROMOTE));
+                            wait_bounded(tfull_bar(buf), bphase, guard, SITE_SWAP_PROMOTE) &&
+                                (!FUSED || wait_bounded(ready_bar(i), 0, guard, SITE_SWAP_PROMOTE)));
             if (!ok)
                 break;
             tc_fence_after_sync();
@@ -517,13 +649,14 @@ __global__ void __launch_bounds__(SwapLayout<MT>::kThreads, SwapLayout<MT>::kMin
     }
 }
 
-template <int MT, bool GROUPED>
+template <int MT, bool GROUPED, bool FUSED = false>
 cudaError_t launch_swapab_t(const CUtensorMap &tmW, const CUtensorMap &tmX, const CUtensorMap &tmC,
                             const SwapParams &p, const LaunchCfg &cfg)
 {
     using L = SwapLayout<MT>;
-    auto kernel = k_swapab<MT, GROUPED>;
-    const size_t smem = L::smem(cfg.stages, p.groups_per_split, p.out_bytes);
+    auto kernel = k_swapab<MT, GROUPED, FUSED>;
+    const size_t smem = L::smem(cfg.stages, p.groups_per_split, p.out_bytes,
+                                FUSED ? (p.x_kind == W8A8_IN_FP32 ? 4 : 2) : 0);
     static volatile int smem_set[kMaxDeviceFlags] = {};
     cudaError_t e = ensure_smem_limit(kernel, smem_set);
     if (e != cudaSuccess)
@@ -567,15 +700,15 @@ cudaError_t launch_swapab_t(const CUtensorMap &tmW, const CUtensorMap &tmX, cons
 
 }  // namespace
 
-size_t swapab_smem_bytes(int mt, int stages, int gps, int out_bytes)
+size_t swapab_smem_bytes(int mt, int stages, int gps, int out_bytes, int x_esize)
 {
     if (stages < 1 || stages > kMaxStages)
         return 0;
     switch (mt) {
-    case 32: return SwapLayout<32>::smem(stages, gps, out_bytes);
-    case 64: return SwapLayout<64>::smem(stages, gps, out_bytes);
-    case 128: return SwapLayout<128>::smem(stages, gps, out_bytes);
-    case 256: return SwapLayout<256>::smem(stages, gps, out_bytes);
+    case 32: return SwapLayout<32>::smem(stages, gps, out_bytes, x_esize);
+    case 64: return SwapLayout<64>::smem(stages, gps, out_bytes, x_esize);
+    case 128: return SwapLayout<128>::smem(stages, gps, out_bytes, x_esize);
+    case 256: return SwapLayout<256>::smem(stages, gps, out_bytes, x_esize);
     default: return 0;
     }
 }
@@ -586,6 +719,15 @@ cudaError_t launch_swapab(const CUtensorMap &tmW, const CUtensorMap &tmX, const 
     if (cfg.stages < 1 || cfg.stages > kMaxStages)
         return cudaErrorInvalidValue;
     const bool grouped = p.masked_m != nullptr;
+    if (p.X != nullptr) {               // fused activation quantisation (never grouped)
+        switch (mt) {
+        case 32: return launch_swapab_t<32, false, true>(tmW, tmX, tmC, p, cfg);
+        case 64: return launch_swapab_t<64, false, true>(tmW, tmX, tmC, p, cfg);
+        case 128: return launch_swapab_t<128, false, true>(tmW, tmX, tmC, p, cfg);
+        case 256: return launch_swapab_t<256, false, true>(tmW, tmX, tmC, p, cfg);
+        default: return cudaErrorInvalidValue;
+        }
+    }
     switch (mt) {
     case 32: return grouped ? launch_swapab_t<32, true>(tmW, tmX, tmC, p, cfg)
                             : launch_swapab_t<32, false>(tmW, tmX, tmC, p, cfg);

@@ -22,6 +22,7 @@ enum WaitSite : uint32_t {
     SITE_DRAIN = 9,
     SITE_TILED_SCALES = 10,
     SITE_SMALL_WEIGHTS = 11,
+    SITE_SWAP_QUANT = 12,
 };
 
 // Tokens on the MMA M side: one CTA per SM walks 128 x BN output tiles.
@@ -72,6 +73,11 @@ struct SwapParams {
     const int *masked_m;
     int experts;
     int tiles_per_expert;
+    // Fused activation quantisation: X [M, K] of x_kind (w8a8_in_dtype) is
+    // quantised per (token, 128-column group) inside the kernel instead of
+    // reading A and a_s.  nullptr: A and a_s are read.
+    const void *X;
+    int x_kind;
 };
 
 // Up to four byte ranges copied by one gather kernel (host-mapped sources).
@@ -109,7 +115,8 @@ cudaError_t launch_smallm(const CUtensorMap &tmB, const SmallParams &p, const La
 
 // Shared memory bytes each kernel configuration needs (0 = unsupported configuration).
 size_t tiled_smem_bytes(int bn, int stages);
-size_t swapab_smem_bytes(int mt, int stages, int groups_per_split, int out_bytes);
+// x_esize: fused activation quantisation's input element size (0: not fused).
+size_t swapab_smem_bytes(int mt, int stages, int groups_per_split, int out_bytes, int x_esize = 0);
 
 // tmC: C as a 2-D [M, N] tensor of the output type, box {64 bytes of columns,
 // 32 rows}, 64-byte swizzle (the tiled kernel's per-warp epilogue chunks).

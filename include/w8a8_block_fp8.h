@@ -68,6 +68,9 @@ typedef enum {
 
 typedef enum { W8A8_OUT_BF16 = 0, W8A8_OUT_FP16 = 1, W8A8_OUT_FP32 = 2 } w8a8_out_dtype;
 
+/* Element type of an unquantised activation (quantiser and fused calls). */
+typedef enum { W8A8_IN_BF16 = 0, W8A8_IN_FP16 = 1, W8A8_IN_FP32 = 2 } w8a8_in_dtype;
+
 /* Kernel variants.  AUTO lets the (M, N, K) dispatcher choose. */
 typedef enum {
     W8A8_VARIANT_AUTO = 0,
@@ -202,6 +205,28 @@ w8a8_status w8a8_block_fp8_matmul_splitk_noalloc(const void *A_dev, const float 
                                                  w8a8_stream_t stream);
 
 /*
+ * The matmul from an unquantised activation: C = matmul(quantise(X), B) with
+ * quantise() exactly as w8a8_quantize_fp8_per_token_group (per token and
+ * 128-wide K group, scale amax / 448, E4M3 codes), done inside the swap-AB
+ * kernel: the quantiser warps turn X into the MMA operand in shared memory,
+ * so that the decode step "quantise the activation, multiply" is one launch.
+ * Bit for bit the same C as the two calls in sequence with the same plan.
+ *   X_dev    device, row-major [M, K] of x_dtype (bf16, fp16 or fp32), 16-byte aligned
+ *   B_dev, b_s_dev, C_dev, shapes and out_dtype as in w8a8_block_fp8_matmul.
+ *   opts: variant AUTO (the measured swap-AB plan for the shape, else the swap-AB
+ *   rules), SWAPAB or SPLITK_CLUSTER; other variants are W8A8_ERR_UNSUPPORTED.
+ *   X must be finite (see the quantiser).  Aimed at decode sizes: every CTA
+ *   quantises its token tile, so large M is better served by the quantiser
+ *   followed by the tiled matmul.  The pages have no fused form; the
+ *   quantiser's reading is the one declared with w8a8_quantize_fp8_per_token_group.
+ */
+w8a8_status w8a8_block_fp8_quant_matmul(const void *X_dev, w8a8_in_dtype x_dtype, const void *B_dev,
+                                        const float *b_s_dev, void *C_dev, int64_t M, int64_t N,
+                                        int64_t K, int block_n, int block_k,
+                                        w8a8_out_dtype out_dtype, w8a8_stream_t stream,
+                                        const w8a8_options *opts);
+
+/*
  * Grouped (mixture-of-experts) forms of the same matmul: E experts, each with
  * its own weights B[e] [N, K] and block scales b_s[e] [ceil(N/128), ceil(K/128)];
  * every token row is multiplied by the weights of the expert it is routed to,
@@ -282,7 +307,6 @@ w8a8_status w8a8_block_fp8_grouped_matmul_contiguous(const void *A_dev, const fl
  * negative size, unknown dtype), W8A8_ERR_UNSUPPORTED (group_size, K or
  * alignment outside the above), W8A8_ERR_CUDA (launch failed).
  */
-typedef enum { W8A8_IN_BF16 = 0, W8A8_IN_FP16 = 1, W8A8_IN_FP32 = 2 } w8a8_in_dtype;
 w8a8_status w8a8_quantize_fp8_per_token_group(const void *X_dev, w8a8_in_dtype x_dtype,
                                               void *A_dev, float *a_s_dev, int64_t M, int64_t K,
                                               int group_size, w8a8_stream_t stream);
