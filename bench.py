@@ -104,13 +104,13 @@ def source_digest(kernel: str = "matmul") -> str:
 # longer matches).
 MEASURED_TRAFFIC = {
     # profiles/k_swapab_decode_m214.md: read 1.172 MB, write 0 (C stays in L2 within the launch)
-    ("53eeccc5d6e05ef3", "214x4096x256", 2): 1172224,
-    # profiles/k_tiled_prefill_16384x4096x4096.md: read 95.61 MB + write 99.11 MB
-    ("53eeccc5d6e05ef3", "16384x4096x4096", 2): 194723072,
-    # profiles/k_quant_group128_16384x4096_bf16.md: read 134.28 MB + write 37.95 MB
-    ("ce940a1728174b49", "quant_16384x4096", 1): 172228352,
-    # profiles/k_swapab_grouped_moe_decode_256x1536x4096.md: read 1.645 GB + write 25.95 MB
-    ("8e787da19f26f0df", "grouped_decode_masked", 2): 1671156976,
+    ("c73aaeffcb3ff8a9", "214x4096x256", 2): 1171968,
+    # profiles/k_tiled_prefill_16384x4096x4096.md: read 96.87 MB + write 98.95 MB
+    ("c73aaeffcb3ff8a9", "16384x4096x4096", 2): 195814656,
+    # profiles/k_quant_group128_16384x4096_bf16.md: read 134.26 MB + write 38.14 MB
+    ("1f4e1e007900fae3", "quant_16384x4096", 1): 172397824,
+    # profiles/k_swapab_grouped_moe_decode_256x1536x4096.md: read 1.645 GB + write 25.71 MB
+    ("c73aaeffcb3ff8a9", "grouped_decode_masked", 2): 1670980984,
 }
 
 
