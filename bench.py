@@ -80,8 +80,8 @@ def parse():
 # helpers and launch declarations, and for the matmul the host planner and the
 # measured dispatch table).
 KERNEL_SOURCES = {
-    "matmul": ("api.cu", "gemm_swapab.cu", "gemm_tiled.cu", "kernels.cuh", "ptx.cuh",
-               "dispatch_table.h", "tuning_table.inc"),
+    "matmul": ("api.cu", "gemm_swapab.cu", "gemm_tiled.cu", "gemm_pair.cu", "epilogue.cuh",
+               "kernels.cuh", "ptx.cuh", "dispatch_table.h", "tuning_table.inc"),
     "quant": ("quant.cu", "kernels.cuh", "ptx.cuh"),
 }
 

@@ -25,6 +25,7 @@ W8A8_OUT_BF16, W8A8_OUT_FP16, W8A8_OUT_FP32 = 0, 1, 2
 W8A8_VARIANT_AUTO, W8A8_VARIANT_TILED, W8A8_VARIANT_SWAPAB, W8A8_VARIANT_SPLITK = 0, 1, 2, 3
 W8A8_VARIANT_SPLITK_CLUSTER = 4
 W8A8_VARIANT_SMALLM = 5
+W8A8_VARIANT_TILED_PAIR = 6
 
 # Every extern "C" symbol of include/w8a8_block_fp8.h.
 EXPORTED = (

@@ -196,7 +196,7 @@ w8a8_status check_options(const w8a8_options *o)
 {
     if (!o)
         return W8A8_OK;
-    if (o->variant < W8A8_VARIANT_AUTO || o->variant > W8A8_VARIANT_SMALLM)
+    if (o->variant < W8A8_VARIANT_AUTO || o->variant > W8A8_VARIANT_TILED_PAIR)
         return fail(W8A8_ERR_INVALID_ARG, "unknown variant %d", o->variant);
     if (o->split_k < 0 || o->stages < 0 || o->stages > 8 || o->grid_limit < 0 || o->m_tile < 0 ||
         o->debug_skip_load < 0)
@@ -214,13 +214,18 @@ int mt_for(int mma_n)
     return mma_n <= 32 ? 32 : mma_n <= 64 ? 64 : mma_n <= 128 ? 128 : 256;
 }
 
+constexpr size_t kCounterWords = 65536;
+constexpr size_t kCounterBytes = kCounterWords * 4;
+
 // The launch plan of one call.
 struct Plan {
     int variant;      // W8A8_VARIANT_TILED / SWAPAB / SPLITK
     int bn;           // tiled
     int stages;
     int grid;         // tiled: persistent CTAs
-    int mma_n, mt, m_tiles, splits, gps;   // swap family
+    int mma_n, mt, m_tiles, splits, gps;   // swap family (splits: tiled 2 = stream-K)
+    int64_t sk_len;                        // tiled stream-K: (tile, group) steps per CTA
+    int sk_first_tile;                     // tiled stream-K: tiles before it run whole
     int tile_bytes;                        // swap family: bytes per staged C-tile element
     size_t smem;
 };
@@ -273,18 +278,57 @@ w8a8_status make_plan(int64_t M, int64_t N, int64_t K, int out_bytes, const w8a8
         return W8A8_OK;
     }
 
+    if (variant == W8A8_VARIANT_TILED_PAIR) {
+        const int bn = bn_hint ? bn_hint : 256;
+        if (bn == 128)
+            return fail(W8A8_ERR_UNSUPPORTED, "the CTA-pair kernel takes block_n_tile 192 or 256");
+        const int stages = bn == 256 ? (stage_hint == 4 ? 4 : 6) : 6;
+        pl->bn = bn;
+        pl->stages = stages;
+        pl->smem = pair_smem_bytes(bn, stages);
+        if (pl->smem == 0 || pl->smem > dev.smem_optin)
+            return fail(W8A8_ERR_UNSUPPORTED, "CTA-pair kernel needs %zu B of shared memory",
+                        pl->smem);
+        const int clusters = pair_max_clusters(bn, stages);
+        if (clusters <= 0)
+            return fail(W8A8_ERR_CUDA, "no CTA pair of the tiled kernel fits on this device");
+        int64_t pairs = std::min<int64_t>(cdiv(M, 256) * cdiv(N, bn), clusters);
+        if (o && o->grid_limit)
+            pairs = std::min<int64_t>(pairs, std::max(o->grid_limit / 2, 1));
+        pl->grid = static_cast<int>(2 * std::max<int64_t>(pairs, 1));
+        return W8A8_OK;
+    }
+
     if (variant == W8A8_VARIANT_TILED) {
         int bn = bn_hint ? bn_hint : (N % 256 == 0 ? 256 : 128);
         int stages = bn == 256   ? (stage_hint == 3 ? 3 : 4)
                      : bn == 192 ? 4
                                  : ((stage_hint == 4 || stage_hint == 5) ? stage_hint : 6);
         const int64_t tiles = cdiv(M, 128) * cdiv(N, bn);
-        int64_t grid = std::min<int64_t>(tiles, dev.sm_count);
+        int64_t grid_cap = dev.sm_count;
         if (o && o->grid_limit)
-            grid = std::min<int64_t>(grid, o->grid_limit);
+            grid_cap = std::min<int64_t>(grid_cap, o->grid_limit);
+        int64_t grid = std::max<int64_t>(std::min<int64_t>(tiles, grid_cap), 1);
+        // Stream-K (split_k >= 2, or a measured table entry): whole tiles for all
+        // but the last one or two waves' worth, which the CTAs share in equal
+        // ranges of K-group steps, so that no wave runs on a fraction of the
+        // SMs.  Needs at least one whole wave of tiles, which keeps every range
+        // at least G steps long (at most two CTAs per tile).  Off by default:
+        // measured, it gains only where a partial last wave is short (e.g.
+        // 16384 x 1536 x 4096: 100.2 -> 96.0 us) and loses a little elsewhere.
+        const bool sk = split_hint >= 2;
+        if (sk && (tiles < grid || tiles > static_cast<int64_t>(kCounterWords) ||
+                   tiles * G >= (1ll << 31)))
+            return fail(W8A8_ERR_UNSUPPORTED,
+                        "stream-K needs at least one tile per CTA (%lld tiles, %lld CTAs)",
+                        static_cast<long long>(tiles), static_cast<long long>(grid));
+        const int64_t sk_first = sk ? (tiles / grid - 1) * grid : 0;
         pl->bn = bn;
         pl->stages = stages;
-        pl->grid = static_cast<int>(std::max<int64_t>(grid, 1));
+        pl->grid = static_cast<int>(grid);
+        pl->splits = sk ? 2 : 1;
+        pl->sk_first_tile = static_cast<int>(sk_first);
+        pl->sk_len = sk ? cdiv((tiles - sk_first) * G, grid) : 0;
         pl->smem = tiled_smem_bytes(bn, stages);
         if (pl->smem == 0 || pl->smem > dev.smem_optin)
             return fail(W8A8_ERR_UNSUPPORTED, "tiled kernel needs %zu B of shared memory",
@@ -348,12 +392,13 @@ w8a8_status make_plan(int64_t M, int64_t N, int64_t K, int out_bytes, const w8a8
 // Split-K workspace layout: a fixed region of kCounterWords arrival counters
 // at the start (so that it stays all-zero whatever sequence of shapes reuses
 // the workspace: every call returns its counters to zero), then the fp32
-// partials [splits, M, N].
-constexpr size_t kCounterWords = 65536;
-constexpr size_t kCounterBytes = kCounterWords * 4;
+// partials: [splits, M, N] for the swap-AB split-K; for the tiled kernel's
+// stream-K two partial tiles (128 x BN) per persistent CTA.
 
 size_t splitk_workspace_bytes(int64_t M, int64_t N, const Plan &pl)
 {
+    if (pl.variant == W8A8_VARIANT_TILED && pl.splits == 2)
+        return kCounterBytes + static_cast<size_t>(pl.grid) * 2 * pl.bn * 128 * 4;
     if (pl.variant != W8A8_VARIANT_SPLITK || pl.splits <= 1)
         return 0;
     const size_t partial = static_cast<size_t>(pl.splits) * M * N * 4;
@@ -394,6 +439,23 @@ w8a8_status library_workspace(int dev, cudaStream_t stream, size_t bytes, void *
     w.bytes = bytes;
     *out = w.ptr;
     return W8A8_OK;
+}
+
+// The split-K / stream-K workspace of a call: the caller's (checked), else the
+// library's own for this device and stream.
+w8a8_status acquire_workspace(const w8a8_options *o, int dev, cudaStream_t stream, size_t bytes,
+                              void **out)
+{
+    void *ws = o ? o->workspace_dev : nullptr;
+    if (ws) {
+        if (o->workspace_bytes < bytes || !aligned(ws, 256))
+            return fail(W8A8_ERR_WORKSPACE,
+                        "workspace of %zu bytes at %p: need %zu bytes, 256-byte aligned",
+                        o->workspace_bytes, ws, bytes);
+        *out = ws;
+        return W8A8_OK;
+    }
+    return library_workspace(dev, stream, bytes, out);
 }
 
 // Grouped (MoE) calls: which layout, the device array of per-expert counts
@@ -506,6 +568,13 @@ w8a8_status run(const void *A, const float *a_s, const void *B, const float *b_s
             if (!forced.stages) forced.stages = t->stages;
         }
     }
+    if (contiguous) {
+        // Whole tiles only: a stream-K piece would need the expert of its tile
+        // in every role, and a grouped call keeps no workspace.
+        if (forced.split_k >= 2)
+            return fail(W8A8_ERR_UNSUPPORTED, "the contiguous layout runs whole tiles (split_k 0 or 1)");
+        forced.split_k = 1;
+    }
     const int x_esize = fused ? (fa.kind == W8A8_IN_FP32 ? 4 : 2) : 0;
     if ((st = make_plan(M, N, K, out == W8A8_OUT_FP32 ? 4 : 2,
                         (gr.mode != Grouping::NONE || fused) ? &forced : o, info, &pl,
@@ -546,11 +615,13 @@ w8a8_status run(const void *A, const float *a_s, const void *B, const float *b_s
         p.status = info.status;
         p.wait_limit = limit;
         e = launch_smallm(mB, p, cfg);
-    } else if (pl.variant == W8A8_VARIANT_TILED) {
+    } else if (pl.variant == W8A8_VARIANT_TILED || pl.variant == W8A8_VARIANT_TILED_PAIR) {
+        const bool pair = pl.variant == W8A8_VARIANT_TILED_PAIR;
         CUtensorMap mA, mB, mC;
         const int chunk_cols = out == W8A8_OUT_FP32 ? 16 : 32;   // 64 bytes of a row
         if ((st = encode_u8_map(&mA, A, M, K, 128)) != W8A8_OK ||
-            (st = encode_u8_map(&mB, B, N, K, pl.bn, contiguous ? gr.experts : 0)) != W8A8_OK ||
+            (st = encode_u8_map(&mB, B, N, K, pair ? pl.bn / 2 : pl.bn,
+                                contiguous ? gr.experts : 0)) != W8A8_OK ||
             (st = encode_out_map(&mC, C, M, N, out, chunk_cols, 32, CU_TENSOR_MAP_SWIZZLE_64B)) !=
                 W8A8_OK)
             return st;
@@ -563,7 +634,7 @@ w8a8_status run(const void *A, const float *a_s, const void *B, const float *b_s
         p.K = static_cast<int>(K);
         p.G = G;
         p.NB = NB;
-        p.num_m_tiles = static_cast<int>(cdiv(M, 128));
+        p.num_m_tiles = static_cast<int>(cdiv(M, pair ? 256 : 128));
         p.num_n_tiles = static_cast<int>(cdiv(N, pl.bn));
         p.num_tiles = p.num_m_tiles * p.num_n_tiles;
         p.out_kind = out;
@@ -572,7 +643,17 @@ w8a8_status run(const void *A, const float *a_s, const void *B, const float *b_s
         p.wait_limit = limit;
         p.m_indices = contiguous ? gr.ids : nullptr;
         p.experts = contiguous ? static_cast<int>(gr.experts) : 1;
-        e = launch_tiled(mA, mB, mC, p, pl.bn, cfg);
+        if (!pair && pl.splits == 2) {
+            void *ws = nullptr;
+            if ((st = acquire_workspace(o, dev, stream, splitk_workspace_bytes(M, N, pl), &ws)) !=
+                W8A8_OK)
+                return st;
+            p.sk_len = pl.sk_len;
+            p.sk_first_tile = pl.sk_first_tile;
+            p.counters = static_cast<unsigned *>(ws);
+            p.ws = reinterpret_cast<float *>(static_cast<char *>(ws) + kCounterBytes);
+        }
+        e = pair ? launch_pair(mA, mB, mC, p, pl.bn, cfg) : launch_tiled(mA, mB, mC, p, pl.bn, cfg);
     } else {
         CUtensorMap mW, mX, mC;
         const int64_t slabs = masked ? gr.experts : 0;
@@ -598,15 +679,9 @@ w8a8_status run(const void *A, const float *a_s, const void *B, const float *b_s
             if (static_cast<size_t>(pl.m_tiles) * NB > kCounterWords)
                 return fail(W8A8_ERR_UNSUPPORTED, "split-K over %lld output tiles (max %zu)",
                             static_cast<long long>(pl.m_tiles) * NB, kCounterWords);
-            void *ws = o ? o->workspace_dev : nullptr;
-            if (ws) {
-                if (o->workspace_bytes < ws_bytes || !aligned(ws, 256))
-                    return fail(W8A8_ERR_WORKSPACE,
-                                "workspace of %zu bytes at %p: need %zu bytes, 256-byte aligned",
-                                o->workspace_bytes, ws, ws_bytes);
-            } else if ((st = library_workspace(dev, stream, ws_bytes, &ws)) != W8A8_OK) {
+            void *ws = nullptr;
+            if ((st = acquire_workspace(o, dev, stream, ws_bytes, &ws)) != W8A8_OK)
                 return st;
-            }
             p.counters = static_cast<unsigned *>(ws);
             p.ws = reinterpret_cast<float *>(static_cast<char *>(ws) + kCounterBytes);
         }

@@ -26,6 +26,7 @@
 // The block-wise scales are arbitrary fp32 values (amax / 448), which the
 // hardware's block-scaled MMA kinds (power-of-two scale factors per 32 K
 // elements) cannot represent; hence the per-group software promotion.
+#include "epilogue.cuh"
 #include "kernels.cuh"
 #include "ptx.cuh"
 
@@ -62,70 +63,119 @@ __device__ __forceinline__ int tile_expert(const TiledParams &p, int t)
     return min(max(p.m_indices[mb * 128], 0), p.experts - 1);
 }
 
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
-                                             uint32_t d)
-{
-    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
-                 "r"(d)
-                 : "memory");
-}
-
-__device__ __forceinline__ uint32_t pack_out2(uint64_t pair, bool bf)
-{
-    float lo, hi;
-    unpack2f(pair, lo, hi);
-    return bf ? pack_bf16x2(lo, hi) : pack_f16x2(lo, hi);
-}
-
-// Epilogue of one warp: its 32 rows (lane = row) x 2*NP accumulator columns
-// (NP fp32 pairs) go out in chunks of 64 bytes per row.  Each chunk is written
-// to one of the warp's EB buffers of 2 KB in the layout a TMA store with the
-// 64-byte swizzle reads (16-byte piece j of row r at r*64 + 16*(j ^ ((r >> 1) & 3)),
-// which also spreads a quarter-warp's 16-byte writes over all banks), then one
-// lane issues the store of the box {64 bytes of columns, 32 rows} at (x, y).
-// A buffer is rewritten only once the store that last used it (EB stores
-// earlier, possibly in the previous tile) has finished reading it.
-template <int NP, int EB>
-__device__ __forceinline__ void store_tile_rows(const uint64_t (&acc)[NP], const CUtensorMap *tmC,
-                                                uint32_t buf0, uint32_t lane, int col0, int y,
-                                                int N, int out_kind)
-{
-    const uint32_t sw = (lane >> 1) & 3u;
-    const bool fp32 = out_kind == OUT_FP32;
-    const bool bf = out_kind == OUT_BF16;
-    const int chunks = fp32 ? NP / 8 : NP / 16;
-    const int ccols = fp32 ? 16 : 32;
-#pragma unroll
-    for (int k = 0; k < NP / 8; ++k) {
-        const int x = col0 + ccols * k;
-        if (k >= chunks || x >= N)
-            break;
-        const uint32_t buf = buf0 + 2048u * (k % EB);
-        if (lane == 0)
-            tma_store_wait_read_n<EB - 1>();
-        __syncwarp();
-        const uint32_t rowa = buf + lane * 64u;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            if (fp32) {
-                const uint64_t p0 = acc[8 * k + 2 * j], p1 = acc[8 * k + 2 * j + 1];
-                st_shared_v4(rowa + 16u * (j ^ sw), static_cast<uint32_t>(p0),
-                             static_cast<uint32_t>(p0 >> 32), static_cast<uint32_t>(p1),
-                             static_cast<uint32_t>(p1 >> 32));
-            } else if (k < NP / 16) {
-                const int b = 16 * k + 4 * j;
-                st_shared_v4(rowa + 16u * (j ^ sw), pack_out2(acc[b], bf),
-                             pack_out2(acc[b + 1], bf), pack_out2(acc[b + 2], bf),
-                             pack_out2(acc[b + 3], bf));
-            }
-        }
-        fence_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-            tma_store_2d(tmC, buf, x, y);
-            tma_store_commit();
-        }
+// The pieces of work of one CTA, in order, as (tile, first K group, end K
+// group).  First whole tiles blockIdx.x, blockIdx.x + gridDim.x, ... below
+// sk_first_tile (all tiles without stream-K); then, with stream-K, the CTA's
+// range of sk_len (tile, group) steps among the remaining tiles -- usually the
+// tail of one tile, maybe whole tiles, and the head of another.  Keeping the
+// stream-K share to the last one or two waves' worth of tiles keeps the tiles
+// in flight at any time adjacent, so their A and B panels are shared in L2.
+// (The host enables stream-K only when num_tiles * G < 2^31.)
+struct SegWalk {
+    int pos, end, G, dp_end, len;
+    bool in_sk;
+    __device__ explicit SegWalk(const TiledParams &p)
+        : pos(static_cast<int>(blockIdx.x)), end(0), G(p.G),
+          dp_end(p.sk_len > 0 ? p.sk_first_tile : p.num_tiles), len(static_cast<int>(p.sk_len)),
+          in_sk(false)
+    {
+        if (len > 0)
+            end = p.num_tiles * p.G;     // one past the last step
     }
+    __device__ bool next(int &t, int &g0, int &g1)
+    {
+        if (!in_sk) {
+            if (pos < dp_end) {
+                t = pos;
+                g0 = 0;
+                g1 = G;
+                pos += static_cast<int>(gridDim.x);
+                return true;
+            }
+            if (len == 0)
+                return false;
+            in_sk = true;
+            pos = dp_end * G + static_cast<int>(blockIdx.x) * len;
+            end = min(end, pos + len);
+        }
+        if (pos >= end)
+            return false;
+        t = pos / G;
+        g0 = pos - t * G;
+        g1 = min(G, g0 + (end - pos));
+        pos += g1 - g0;
+        return true;
+    }
+};
+
+// Stream-K fix-up of one piece of tile t, run by all promotion threads of the
+// CTA (thread = row, CPW columns of warpgroup h in acc).  The host keeps every
+// stream-K range at least G steps long, so a tile has at most two
+// contributors: the piece's fp32 partial goes to this CTA's workspace slot for
+// the tile (laid out [column quad][row][4], so that a warp's 16-byte stores
+// are contiguous), the CTA counts itself in counters[t], and the second to
+// arrive adds the first's partial to its own, resets the counter for the next
+// call and returns true with the tile's sums in acc; the first returns false.
+// The sum is the same in either order, so the bits are the same on every run.
+// (A sum whose loads sit behind a loop over contributors, or in batches that
+// read-modify-write acc, measured 20-50 us per tile or slowed the whole-tile
+// promotion loop by 20 %; this form does neither.)
+template <int BN, int CPW, int NP>
+__device__ __forceinline__ bool stream_k_fixup(const TiledParams &p, uint64_t (&acc)[NP], int t,
+                                               int row, int h, volatile int *last_flag)
+{
+    constexpr int kPromoThreads = 128 * (BN / CPW);
+    constexpr size_t kSlotFloats = static_cast<size_t>(BN) * 128;
+    // Steps counted from the first stream-K tile (32-bit: the host enables
+    // stream-K only when num_tiles * G < 2^31).
+    const int len = static_cast<int>(p.sk_len);
+    const int s0 = (t - p.sk_first_tile) * p.G;
+    const int c_first = s0 / len;
+    const int c_last = (s0 + p.G - 1) / len;
+    // Slot of CTA c for this tile: 0 if its range starts in tile t, else 1.
+    auto slot = [&](int c) {
+        const int first_tile = p.sk_first_tile + c * len / p.G;
+        return p.ws + (static_cast<size_t>(c) * 2 + (first_tile == t ? 0 : 1)) * kSlotFloats;
+    };
+    const int me = static_cast<int>(blockIdx.x);
+    const int quad0 = h * (CPW / 4);
+    float *mine = slot(me);
+#pragma unroll
+    for (int j = 0; j < CPW / 4; ++j) {
+        float4 v;
+        unpack2f(acc[2 * j], v.x, v.y);
+        unpack2f(acc[2 * j + 1], v.z, v.w);
+        __stcg(reinterpret_cast<float4 *>(mine) + (quad0 + j) * 128 + row, v);
+    }
+    __threadfence();
+    named_barrier(2, kPromoThreads);
+    if (threadIdx.x == 128) {
+        const unsigned n = static_cast<unsigned>(c_last - c_first + 1);
+        const unsigned before = atomicAdd(p.counters + t, 1u);
+        const bool last = before == n - 1;
+        if (last)
+            p.counters[t] = 0u;
+        *last_flag = last ? 1 : 0;
+    }
+    named_barrier(2, kPromoThreads);
+    if (!*last_flag)
+        return false;
+    __threadfence();
+    // Two contributors (the host keeps every range at least one tile's K
+    // groups long): acc + the other's partial, the same sum in either order
+    // (fp32 addition commutes).  One load per column quad, all independent.
+    const float4 *src =
+        reinterpret_cast<const float4 *>(slot(c_first == me ? c_last : c_first)) + quad0 * 128 + row;
+#pragma unroll
+    for (int j = 0; j < CPW / 4; ++j) {
+        const float4 v = __ldcg(src + j * 128);
+        float x, y, z, w;
+        unpack2f(acc[2 * j], x, y);
+        unpack2f(acc[2 * j + 1], z, w);
+        acc[2 * j] = pack2f(x + v.x, y + v.y);
+        acc[2 * j + 1] = pack2f(z + v.z, w + v.w);
+    }
+    return true;
 }
 
 // BN output columns per tile, STAGES shared-memory stages, CPW columns per
@@ -181,6 +231,7 @@ __global__ void __launch_bounds__(TiledLayout<BN, STAGES, CPW, EB>::kThreads, 1)
     const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 2 * L::kBufs + 2 * kScaleSlots);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + L::kBars);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    volatile int *last_flag = reinterpret_cast<volatile int *>(tmem_slot + 2);   // stream-K
 
     const uint32_t warp = warp_index(), lane = lane_index();
 
@@ -229,12 +280,14 @@ __global__ void __launch_bounds__(TiledLayout<BN, STAGES, CPW, EB>::kThreads, 1)
             long long issued = 0;
             bool ok = true;
             int e_next = tile_expert(p, blockIdx.x);
-            for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+            SegWalk walk(p);
+            int t, g0, g1;
+            while (ok && walk.next(t, g0, g1)) {
                 int mb, nb;
                 tile_coords(t, p.num_m_tiles, p.num_n_tiles, mb, nb);
                 const int e = e_next;
                 e_next = tile_expert(p, t + gridDim.x);   // in flight during this tile
-                for (int g = 0; g < p.G; ++g) {
+                for (int g = g0; g < g1; ++g) {
                     if (!wait_bounded(empty_bar(stage), phase ^ 1u, guard, SITE_TILED_PRODUCER)) {
                         ok = false;
                         break;
@@ -287,8 +340,10 @@ __global__ void __launch_bounds__(TiledLayout<BN, STAGES, CPW, EB>::kThreads, 1)
             uint32_t phase = 0;
             uint32_t it = 0;
             bool ok = true;
-            for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
-                for (int g = 0; g < p.G; ++g) {
+            SegWalk walk(p);
+            int t, g0, g1;
+            while (ok && walk.next(t, g0, g1)) {
+                for (int g = g0; g < g1; ++g) {
                     const uint32_t buf = it % L::kBufs;
                     const uint32_t bphase = (it / L::kBufs) & 1u;
                     if (!wait_bounded(tempty_bar(buf), bphase ^ 1u, guard, SITE_TILED_MMA_TMEM) ||
@@ -322,12 +377,14 @@ __global__ void __launch_bounds__(TiledLayout<BN, STAGES, CPW, EB>::kThreads, 1)
             uint32_t sphase = 0;
             bool ok = true;
             int e_next = tile_expert(p, blockIdx.x);
-            for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+            SegWalk walk(p);
+            int t, g0, g1;
+            while (ok && walk.next(t, g0, g1)) {
                 int mb, nb;
                 tile_coords(t, p.num_m_tiles, p.num_n_tiles, mb, nb);
                 const size_t b_row0 = static_cast<size_t>(e_next) * p.NB;
                 e_next = tile_expert(p, t + gridDim.x);
-                for (int g = 0; g < p.G; ++g) {
+                for (int g = g0; g < g1; ++g) {
                     ok = __all_sync(0xffffffffu, wait_bounded(sempty_bar(slot), sphase ^ 1u, guard,
                                                               SITE_TILED_SCALES));
                     if (!ok)
@@ -370,7 +427,9 @@ __global__ void __launch_bounds__(TiledLayout<BN, STAGES, CPW, EB>::kThreads, 1)
         uint32_t it = 0;
         int slot = 0;
         uint32_t sphase = 0;
-        for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
+        SegWalk walk(p);
+        int t, g0, g1;
+        while (walk.next(t, g0, g1)) {
             int mb, nb;
             tile_coords(t, p.num_m_tiles, p.num_n_tiles, mb, nb);
             const int col0 = nb * BN + h * CPW;
@@ -379,7 +438,7 @@ __global__ void __launch_bounds__(TiledLayout<BN, STAGES, CPW, EB>::kThreads, 1)
             for (int j = 0; j < L::kPairs; ++j)
                 acc[j] = 0ull;
             bool ok = true;
-            for (int g = 0; g < p.G; ++g) {
+            for (int g = g0; g < g1; ++g) {
                 const uint32_t buf = it % L::kBufs;
                 const uint32_t bphase = (it / L::kBufs) & 1u;
                 // All lanes wait, so that the whole warp sleeps in the barrier
@@ -420,6 +479,11 @@ __global__ void __launch_bounds__(TiledLayout<BN, STAGES, CPW, EB>::kThreads, 1)
             }
             if (!ok)
                 break;
+            if (g0 > 0 || g1 < p.G) {
+                // Stream-K: a piece of a tile shared with other CTAs.
+                if (!stream_k_fixup<BN, CPW, L::kPairs>(p, acc, t, row, h, last_flag))
+                    continue;          // another contributor finishes this tile
+            }
             // Epilogue: this warp's 32 rows x CPW columns leave in chunks of 64
             // bytes per row through 2 KB shared-memory buffers (64-byte
             // swizzle, conflict-free 16-byte writes) and asynchronous TMA stores,

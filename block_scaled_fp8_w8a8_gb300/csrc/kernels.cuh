@@ -23,6 +23,7 @@ enum WaitSite : uint32_t {
     SITE_TILED_SCALES = 10,
     SITE_SMALL_WEIGHTS = 11,
     SITE_SWAP_QUANT = 12,
+    SITE_PAIR_PEER = 13,   // CTA-pair kernel: waiting for the other CTA's stage
 };
 
 // Tokens on the MMA M side: one CTA per SM walks 128 x BN output tiles.
@@ -41,6 +42,19 @@ struct TiledParams {
     // (-1: a padding block, computed with expert 0's weights).  nullptr: one B.
     const int *m_indices;
     int experts;
+    // Stream-K (one-CTA kernel only; sk_len 0 = whole tiles): tiles below
+    // sk_first_tile are dealt out whole, round robin; the (tile, K group)
+    // steps of the others, in tile order, are cut into gridDim.x equal
+    // contiguous ranges of sk_len >= G steps, one per CTA.  A tile whose steps
+    // fall in two CTAs' ranges is finished by the second to arrive: both write
+    // their fp32 partial tile to ws (two slots per CTA, for the tile its range
+    // starts in and the one it ends in) and count themselves in
+    // counters[tile]; the second adds the first's partial and stores the tile.
+    // counters is zero between calls.
+    long long sk_len;
+    int sk_first_tile;
+    float *ws;
+    unsigned *counters;
 };
 
 // Swap-AB: weights on the MMA M side (128 rows of B = one b_s row block),
@@ -122,6 +136,14 @@ size_t swapab_smem_bytes(int mt, int stages, int groups_per_split, int out_bytes
 // 32 rows}, 64-byte swizzle (the tiled kernel's per-warp epilogue chunks).
 cudaError_t launch_tiled(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmC,
                          const TiledParams &p, int bn, const LaunchCfg &cfg);
+// CTA-pair variant of the tiled kernel (clusters of 2, 256 x bn tiles): tmA has
+// a box of 128 rows, tmB a box of bn/2 rows, tmC as for launch_tiled;
+// p.num_m_tiles counts 256-row tiles; cfg.grid is even (two CTAs per pair) and
+// at most 2 x pair_max_clusters(bn, stages).  The grouped layout is not supported.
+size_t pair_smem_bytes(int bn, int stages);
+int pair_max_clusters(int bn, int stages);     // < 0 on error
+cudaError_t launch_pair(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmC,
+                        const TiledParams &p, int bn, const LaunchCfg &cfg);
 // tmC: C as a 2-D [M, N] tensor of the output type, box {128 columns, mma_n rows},
 // no swizzle (used by the epilogue's TMA store when splits == 1).
 cudaError_t launch_swapab(const CUtensorMap &tmW, const CUtensorMap &tmX, const CUtensorMap &tmC,

@@ -338,6 +338,76 @@ __device__ __forceinline__ void tmem_load_64cols(uint32_t taddr, uint32_t (&r)[6
                  : "memory");
 }
 
+// ------------------------------------------------------------------ tcgen05, CTA pairs
+//
+// With .cta_group::2 the two CTAs of a cluster whose ranks differ only in bit 0
+// (a CTA pair on one TPC) act as one MMA unit: one thread of the even CTA
+// issues an M = 256 MMA whose A rows 0..127 come from the even CTA's shared
+// memory and rows 128..255 from the odd CTA's (same shared-memory offsets), B's
+// N columns are split the same way (N/2 rows of B in each CTA), and each CTA's
+// TMEM receives its own 128 rows of D.  Every tcgen05 instruction of such a
+// kernel uses .cta_group::2; allocation and release are collective (one warp of
+// each CTA of the pair).
+
+__device__ __forceinline__ uint32_t cluster_ctarank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst, uint32_t ncols)
+{
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst),
+                 "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair()
+{
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols)
+{
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+
+// D[tmem of both CTAs] (+)= A[smem of both] * B[smem of both]^T: one 256 x N x 32
+// FP8 step of the pair, issued by one thread of the even CTA.
+__device__ __forceinline__ void mma_e4m3_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                              uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "setp.ne.b32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+                 "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+                 : "memory");
+}
+
+// Arrive once on the mbarrier at shared-memory offset `bar` of every CTA in
+// `cta_mask` when all earlier tcgen05.mma of this thread have completed.
+__device__ __forceinline__ void mma_commit_pair_mc(uint32_t bar, uint16_t cta_mask)
+{
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::"
+                 "cluster.b64 [%0], %1;" ::"r"(bar),
+                 "h"(cta_mask)
+                 : "memory");
+}
+
+// Arrive on an mbarrier of another CTA of the cluster, given by its address in
+// the cluster's shared window (see cluster_map), with the instruction's default
+// semantics.  The pair kernel uses it only to say "this CTA has finished
+// reading its TMEM buffer" (ordered by tcgen05.wait::ld and
+// tcgen05.fence::before_thread_sync before the arrive) and "this CTA's stage
+// has landed" (the TMA data is in shared memory before its barrier completes,
+// and the arrive comes after that completion was observed); neither needs the
+// arriving thread's own memory writes to become visible.  A .release.cluster
+// arrive measured about 1 us each on GB300, which serialised the pipeline.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr)
+{
+    asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
 // ------------------------------------------------------------------ thread-block clusters
 
 // Cluster-wide barrier; every thread of every CTA of the cluster must call it

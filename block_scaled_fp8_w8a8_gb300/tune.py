@@ -73,6 +73,14 @@ def candidates(M, N, K, sms=152):
     if M >= 64:
         for bn, stages in ((256, 4), (256, 3), (192, 4), (128, 6), (128, 5), (128, 4)):
             out.append(dict(variant=b.W8A8_VARIANT_TILED, block_n_tile=bn, stages=stages))
+            # stream-K where there is at least one tile per SM and a partial last wave
+            tiles = -(-M // 128) * -(-N // bn)
+            if tiles >= sms and tiles % sms and bn != 128:
+                out.append(dict(variant=b.W8A8_VARIANT_TILED, block_n_tile=bn, stages=stages,
+                                split_k=2))
+    if M >= 512:
+        for bn, stages in ((256, 6), (256, 4), (192, 6)):
+            out.append(dict(variant=b.W8A8_VARIANT_TILED_PAIR, block_n_tile=bn, stages=stages))
     if M <= 4:
         out.append(dict(variant=b.W8A8_VARIANT_SMALLM))   # rejected where it does not fit
     if M <= 1024:
@@ -171,6 +179,8 @@ def main():
                     help="tune the full trace grid and write M ranges")
     ap.add_argument("--grid-n", type=int, default=None,
                     help="with --grid: only the shapes with this N")
+    ap.add_argument("--min-m", type=int, default=0,
+                    help="with --grid: only the shapes with M at least this")
     ap.add_argument("--jsonl", default=None,
                     help="append each shape's best configuration to this file as it is found")
     ap.add_argument("--table-from", default=None,
@@ -187,6 +197,8 @@ def main():
     shapes = grid_shapes() if args.grid else DEFAULT_SHAPES
     if args.grid and args.grid_n:
         shapes = [s for s in shapes if s[1] == args.grid_n]
+    if args.grid and args.min_m:
+        shapes = [s for s in shapes if s[0] >= args.min_m]
     if args.shapes:
         shapes = [tuple(int(v) for v in s.split("x")) for s in args.shapes.split(",")]
     l2 = torch.cuda.get_device_properties(0).L2_cache_size

@@ -82,20 +82,35 @@ typedef enum {
                                         thread-block cluster (2..16 CTAs) and reduce their
                                         partials in rank order through distributed shared
                                         memory: no workspace; same bits as SPLITK          */
-    W8A8_VARIANT_SMALLM = 5          /* M <= 16: dot products on the CUDA cores, 32 weight
+    W8A8_VARIANT_SMALLM = 5,         /* M <= 16: dot products on the CUDA cores, 32 weight
                                         rows per CTA (no tensor memory); K limited by
                                         shared memory (M x K x 4 + 32 x K bytes)            */
+    W8A8_VARIANT_TILED_PAIR = 6      /* as TILED, but two CTAs (a cluster of 2 on one SM
+                                        pair) share one 256 x BN tile through
+                                        tcgen05 .cta_group::2 MMAs: each loads its 128 rows
+                                        of A and half of the tile's BN rows of B; for large
+                                        M.  Not for the grouped layouts.                    */
 } w8a8_variant;
 
 /*
  * Optional controls for w8a8_block_fp8_matmul_ex.  Zero-initialise and set
  * what you need; every zero field means "library default".
  *   variant            force a kernel variant (w8a8_variant); AUTO = dispatcher
- *   split_k            number of K splits for W8A8_VARIANT_SPLITK (0 = choose)
- *   block_n_tile       TILED only: 128, 192 or 256 output columns per tile (0 = choose)
+ *   split_k            SPLITK / SPLITK_CLUSTER: number of K splits (0 = choose).
+ *                      TILED: 0 = the measured table's choice, else whole tiles;
+ *                      1 = whole tiles; 2 (or more) = stream-K: whole tiles for
+ *                      all but the last one or two waves' worth, whose (tile,
+ *                      128-wide K group) steps the persistent CTAs share in
+ *                      equal contiguous ranges; a tile shared by two CTAs is
+ *                      finished by the second, which adds the first's fp32
+ *                      partial (same bits on every run).  Needs a workspace like
+ *                      SPLITK and at least as many tiles as CTAs, else
+ *                      W8A8_ERR_UNSUPPORTED
+ *   block_n_tile       TILED / TILED_PAIR: 128, 192 or 256 output columns per tile (0 = choose)
  *   m_tile             SWAPAB/SPLITK only: tokens per tile, multiple of 16, <= 256 (0 = choose)
  *   stages             shared-memory pipeline depth 1..8 (0 = choose)
- *   grid_limit         TILED only: cap on the number of persistent CTAs (0 = one per SM)
+ *   grid_limit         TILED / TILED_PAIR: cap on the number of persistent CTAs (0 = one
+ *                      per SM; TILED_PAIR: as many pairs as can be resident at once)
  *   pdl                1 = launch with programmatic dependent launch, so that the
  *                      kernel's prologue overlaps the previous kernel on the stream
  *   weights_static     1 = B and b_s are not written by the work that precedes this
@@ -106,7 +121,7 @@ typedef enum {
  *                      n-th operand load, so that a bounded device wait runs out
  *                      and the call surfaces W8A8_ERR_DEVICE_TIMEOUT through
  *                      w8a8_get_device_status(); C is then undefined.  0 = off.
- *   workspace_dev      SPLITK only: caller-owned device scratch of workspace_bytes
+ *   workspace_dev      SPLITK and stream-K TILED: caller-owned device scratch of workspace_bytes
  *                      bytes, 256-byte aligned, at least
  *                      w8a8_block_fp8_workspace_size() bytes, all zero before its
  *                      first use (every call leaves its counter words zero again).
@@ -328,7 +343,8 @@ size_t w8a8_block_fp8_host_staging_size(int64_t M, int64_t N, int64_t K, w8a8_ou
  * Bytes of split-K workspace a call with these options needs (0 when the
  * variant the call would run needs none).  Layout: a fixed block of 65536
  * 32-bit arrival counters (256 KiB, one per output tile in use; at most 65536
- * tiles) followed by the fp32 partial sums [split_k, M, N].  The counter block
+ * tiles) followed by the fp32 partial sums: [split_k, M, N] for SPLITK, two
+ * 128 x BN tiles per persistent CTA for a stream-K TILED call.  The counter block
  * must be zero before the workspace's first use; every completed call leaves
  * it zero again, so one workspace can serve any sequence of shapes on one
  * stream.  After a W8A8_ERR_DEVICE_TIMEOUT, zero it again.
@@ -338,7 +354,8 @@ size_t w8a8_block_fp8_workspace_size(int64_t M, int64_t N, int64_t K, const w8a8
 /*
  * Which variant (and its parameters) the dispatcher picks for a problem;
  * writes into *plan_out (zero-initialised first).  No CUDA call is made
- * except a cached query of the current device's SM count.
+ * except cached queries of the current device's properties (and, for the
+ * CTA-pair variant, of how many pairs of its kernel can be resident at once).
  */
 w8a8_status w8a8_block_fp8_plan(int64_t M, int64_t N, int64_t K, w8a8_out_dtype out_dtype,
                                 const w8a8_options *opts, w8a8_options *plan_out);

@@ -25,6 +25,7 @@ LIMIT = 2_000_000   # SM cycles, about 1 ms
     (w8.W8A8_VARIANT_TILED, 1), (w8.W8A8_VARIANT_TILED, 3),
     (w8.W8A8_VARIANT_SWAPAB, 1), (w8.W8A8_VARIANT_SWAPAB, 2),
     (w8.W8A8_VARIANT_SPLITK, 1),
+    (w8.W8A8_VARIANT_TILED_PAIR, 1), (w8.W8A8_VARIANT_TILED_PAIR, 3),
 ])
 def test_bounded_wait_reports_timeout_and_context_survives(variant, skip):
     M, N, K = 130, 512, 512
