@@ -16,6 +16,7 @@ from ._binding import (  # noqa: F401
     W8A8_ERR_DEVICE_TIMEOUT, W8A8_ERR_WORKSPACE, W8A8_ERR_NO_DEVICE, W8A8_OUT_BF16,
     W8A8_OUT_FP16, W8A8_OUT_FP32, W8A8_VARIANT_AUTO, W8A8_VARIANT_TILED, W8A8_VARIANT_SWAPAB,
     W8A8_VARIANT_SPLITK, W8A8_VARIANT_SPLITK_CLUSTER, W8A8_VARIANT_SMALLM, W8A8_VARIANT_TILED_PAIR,
+    W8A8_VARIANT_GENERIC, w8a8_block_fp8_matmul_strided,
     check, library_path, load_library,
     w8a8_abi_version,
     w8a8_block_fp8_host_staging_size, w8a8_block_fp8_matmul, w8a8_block_fp8_matmul_ex,
@@ -47,12 +48,15 @@ def options(**kw) -> w8a8_options:
     return o
 
 
-def matmul(A, a_s, B, b_s, out_dtype="bf16", out=None, stream=None, **opts):
+def matmul(A, a_s, B, b_s, out_dtype="bf16", out=None, stream=None, block_n=128, block_k=128,
+           **opts):
     """C = A B^T with block de-quantisation, on CUDA tensors.
 
-    A: uint8 or float8_e4m3fn [M, K]; a_s: float32 [M, K/128]; B: uint8 or
-    float8_e4m3fn [N, K]; b_s: float32 [ceil(N/128), K/128].  ``out`` (a
-    preallocated [M, N] tensor) is optional; keyword options map to
+    A: uint8 or float8_e4m3fn [M, K]; a_s: float32 [M, ceil(K/block_k)]; B:
+    uint8 or float8_e4m3fn [N, K]; b_s: float32 [ceil(N/block_n),
+    ceil(K/block_k)].  Every tensor needs unit stride along its last dimension;
+    its row stride is passed through (views of larger buffers work).  ``out``
+    (a preallocated [M, N] tensor) is optional; keyword options map to
     w8a8_options fields.  Raises W8A8Error on a non-zero status.
     """
     import torch
@@ -63,11 +67,15 @@ def matmul(A, a_s, B, b_s, out_dtype="bf16", out=None, stream=None, **opts):
         tdt = {W8A8_OUT_BF16: torch.bfloat16, W8A8_OUT_FP16: torch.float16,
                W8A8_OUT_FP32: torch.float32}[code]
         out = torch.empty((M, N), dtype=tdt, device=A.device)
-    for t in (A, a_s, B, b_s, out):
-        if not t.is_contiguous():
-            raise W8A8Error(W8A8_ERR_UNSUPPORTED, "tensors must be contiguous row-major")
-    st = w8a8_block_fp8_matmul_ex(A, a_s, B, b_s, out, M, N, K, 128, 128, code, stream,
-                                  options(**opts) if opts else None)
+
+    def ld(t):
+        if t.dim() != 2 or (t.size(1) > 1 and t.stride(1) != 1):
+            raise W8A8Error(W8A8_ERR_UNSUPPORTED, "each row must be contiguous (unit stride)")
+        return t.stride(0) if t.size(0) > 1 else t.size(1)
+
+    st = w8a8_block_fp8_matmul_strided(A, ld(A), a_s, ld(a_s), B, ld(B), b_s, ld(b_s), out,
+                                       ld(out), M, N, K, block_n, block_k, code, stream,
+                                       options(**opts) if opts else None)
     check(st)
     return out
 

@@ -26,11 +26,13 @@ W8A8_VARIANT_AUTO, W8A8_VARIANT_TILED, W8A8_VARIANT_SWAPAB, W8A8_VARIANT_SPLITK 
 W8A8_VARIANT_SPLITK_CLUSTER = 4
 W8A8_VARIANT_SMALLM = 5
 W8A8_VARIANT_TILED_PAIR = 6
+W8A8_VARIANT_GENERIC = 7
 
 # Every extern "C" symbol of include/w8a8_block_fp8.h.
 EXPORTED = (
     "w8a8_block_fp8_matmul",
     "w8a8_block_fp8_matmul_ex",
+    "w8a8_block_fp8_matmul_strided",
     "w8a8_block_fp8_matmul_host",
     "w8a8_block_fp8_matmul_splitk_noalloc",
     "w8a8_block_fp8_grouped_matmul_masked",
@@ -96,6 +98,8 @@ def load_library():
     lib.w8a8_block_fp8_matmul.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i32, i32, i32, vp]
     lib.w8a8_block_fp8_matmul_ex.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i32, i32, i32, vp,
                                              opt_p]
+    lib.w8a8_block_fp8_matmul_strided.argtypes = [vp, i64, vp, i64, vp, i64, vp, i64, vp, i64, i64,
+                                                  i64, i64, i32, i32, i32, vp, opt_p]
     lib.w8a8_block_fp8_matmul_host.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i32, i32, i32,
                                                vp, sz, vp, opt_p]
     lib.w8a8_block_fp8_matmul_splitk_noalloc.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i32,
@@ -173,6 +177,14 @@ def w8a8_block_fp8_matmul_ex(A, a_s, B, b_s, C, M, N, K, block_n=128, block_k=12
     return load_library().w8a8_block_fp8_matmul_ex(_ptr(A), _ptr(a_s), _ptr(B), _ptr(b_s),
                                                     _ptr(C), M, N, K, block_n, block_k, out_dtype,
                                                     _stream(stream), _opts(opts))
+
+
+def w8a8_block_fp8_matmul_strided(A, lda, a_s, ld_as, B, ldb, b_s, ld_bs, C, ldc, M, N, K,
+                                  block_n=128, block_k=128, out_dtype=W8A8_OUT_BF16, stream=None,
+                                  opts=None) -> int:
+    return load_library().w8a8_block_fp8_matmul_strided(
+        _ptr(A), lda, _ptr(a_s), ld_as, _ptr(B), ldb, _ptr(b_s), ld_bs, _ptr(C), ldc, M, N, K,
+        block_n, block_k, out_dtype, _stream(stream), _opts(opts))
 
 
 def w8a8_block_fp8_matmul_host(A_host, a_s_host, B_host, b_s_host, C_host, M, N, K,

@@ -114,14 +114,16 @@ w8a8_status current_device(int *dev_out, DeviceInfo *info_out)
 // 128 columns (one K group, 128 bytes) by box_rows rows, 128-byte swizzle,
 // out-of-range elements read as zero.
 w8a8_status encode_u8_map(CUtensorMap *map, const void *base, int64_t rows, int64_t cols,
-                          int box_rows, int64_t slabs = 0)
+                          int box_rows, int64_t slabs = 0, int64_t ld = 0)
 {
+    // ld: bytes per row (a multiple of 16), 0 = dense (cols)
+    const int64_t pitch = ld ? ld : cols;
     // slabs > 0: a 3-D map over [slabs, rows, cols] (one expert per slab), boxes
     // of one slab; rows past `rows` inside a slab read as zeros.
     const cuuint32_t rank = slabs > 0 ? 3u : 2u;
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows),
                           static_cast<cuuint64_t>(slabs)};
-    cuuint64_t strides[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(cols * rows)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(pitch), static_cast<cuuint64_t>(pitch * rows)};
     cuuint32_t box[3] = {128u, static_cast<cuuint32_t>(box_rows), 1u};
     cuuint32_t elem[3] = {1u, 1u, 1u};
     CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, rank, const_cast<void *>(base), dims,
@@ -139,9 +141,11 @@ w8a8_status encode_u8_map(CUtensorMap *map, const void *base, int64_t rows, int6
 // of box_cols columns by box_rows rows with the given shared-memory swizzle.
 w8a8_status encode_out_map(CUtensorMap *map, void *base, int64_t rows, int64_t cols, int out,
                            int box_cols, int box_rows, CUtensorMapSwizzle swizzle,
-                           int64_t slabs = 0)
+                           int64_t slabs = 0, int64_t ld = 0)
 {
+    // ld: elements per row (row bytes a multiple of 16), 0 = dense (cols)
     const int eb = out == W8A8_OUT_FP32 ? 4 : 2;
+    const int64_t pitch = ld ? ld : cols;
     const CUtensorMapDataType dt = out == W8A8_OUT_FP32   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
                                    : out == W8A8_OUT_FP16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
                                                           : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
@@ -149,8 +153,8 @@ w8a8_status encode_out_map(CUtensorMap *map, void *base, int64_t rows, int64_t c
     const cuuint32_t rank = slabs > 0 ? 3u : 2u;
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows),
                           static_cast<cuuint64_t>(slabs)};
-    cuuint64_t strides[2] = {static_cast<cuuint64_t>(cols) * eb,
-                             static_cast<cuuint64_t>(cols) * eb * static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(pitch) * eb,
+                             static_cast<cuuint64_t>(pitch) * eb * static_cast<cuuint64_t>(rows)};
     cuuint32_t box[3] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows), 1u};
     cuuint32_t elem[3] = {1u, 1u, 1u};
     CUresult r = g_encode(map, dt, rank, base, dims, strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -196,7 +200,7 @@ w8a8_status check_options(const w8a8_options *o)
 {
     if (!o)
         return W8A8_OK;
-    if (o->variant < W8A8_VARIANT_AUTO || o->variant > W8A8_VARIANT_TILED_PAIR)
+    if (o->variant < W8A8_VARIANT_AUTO || o->variant > W8A8_VARIANT_GENERIC)
         return fail(W8A8_ERR_INVALID_ARG, "unknown variant %d", o->variant);
     if (o->split_k < 0 || o->stages < 0 || o->stages > 8 || o->grid_limit < 0 || o->m_tile < 0 ||
         o->debug_skip_load < 0)
@@ -474,17 +478,129 @@ struct FusedAct {
     int kind = 0;
 };
 
+// Row strides of one call, in elements (bytes for A and B); 0 = dense.
+struct Strides {
+    int64_t lda = 0, ldb = 0, ldc = 0, ld_as = 0, ld_bs = 0;
+};
+
+// Why the tensor-core kernels cannot take a problem (the page's shape guards:
+// group_k == 128, FP8 operands, rows the TMA can address), or nullptr.
+const char *fast_path_gap(const void *A, const float *a_s, const void *B, const float *b_s,
+                          const void *C, int64_t M, int64_t N, int64_t K, int block_n,
+                          int block_k, int out, const Strides &sd)
+{
+    const int eb = out == W8A8_OUT_FP32 ? 4 : 2;
+    if (block_n != 128 || block_k != 128)
+        return "scale blocks other than [128, 128]";
+    if (K < 16 || K % 16 != 0)
+        return "K is not a positive multiple of 16";
+    if ((N * eb) % 16 != 0)
+        return "rows of C are not a multiple of 16 bytes";
+    if (M > (1ll << 31) - 1 || N > (1ll << 31) - 1 || K > (1ll << 31) - 1)
+        return "a size of 2^31 or more";
+    if (!aligned(A, 16) || !aligned(B, 16) || !aligned(C, 16))
+        return "A, B or C is not 16-byte aligned";
+    if (!aligned(a_s, 4) || !aligned(b_s, 4))
+        return "a_s or b_s is not 4-byte aligned";
+    if (sd.lda % 16 != 0 || sd.ldb % 16 != 0 || (sd.ldc * eb) % 16 != 0)
+        return "a row stride of A, B or C is not a multiple of 16 bytes";
+    if (sd.ld_as != cdiv(K, 128) || sd.ld_bs != cdiv(K, 128))
+        return "the scale rows are not dense";
+    return nullptr;
+}
+
+// The generic CUDA-core kernel: any sizes, strides, alignment of A and B, and
+// scale block sizes.
+w8a8_status run_generic(const void *A, const float *a_s, const void *B, const float *b_s, void *C,
+                        int64_t M, int64_t N, int64_t K, int block_n, int block_k, int out,
+                        const Strides &sd, cudaStream_t stream, const w8a8_options *o)
+{
+    if (!C || (K > 0 && (!A || !a_s || !B || !b_s)))
+        return fail(W8A8_ERR_INVALID_ARG, "null pointer argument");
+    if (!aligned(C, out == W8A8_OUT_FP32 ? 4 : 2) || !aligned(a_s, 4) || !aligned(b_s, 4))
+        return fail(W8A8_ERR_UNSUPPORTED, "C must be aligned to its element size and a_s, b_s to 4 bytes");
+    int dev;
+    DeviceInfo info;
+    w8a8_status st;
+    if ((st = current_device(&dev, &info)) != W8A8_OK)
+        return st;
+    GenericParams p = {};
+    p.A = static_cast<const uint8_t *>(A);
+    p.a_s = a_s;
+    p.B = static_cast<const uint8_t *>(B);
+    p.b_s = b_s;
+    p.C = C;
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    p.lda = sd.lda;
+    p.ldb = sd.ldb;
+    p.ldc = sd.ldc;
+    p.ld_as = sd.ld_as;
+    p.ld_bs = sd.ld_bs;
+    p.block_n = block_n;
+    p.block_k = block_k;
+    p.out_kind = out;
+    LaunchCfg cfg = {};
+    cfg.pdl = o ? o->pdl : 0;
+    cfg.stream = stream;
+    const cudaError_t e = launch_generic(p, cfg);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "generic kernel launch");
+    return W8A8_OK;
+}
+
 w8a8_status run(const void *A, const float *a_s, const void *B, const float *b_s, void *C,
                 int64_t M, int64_t N, int64_t K, int block_n, int block_k, int out,
                 cudaStream_t stream, const w8a8_options *o, const Grouping &gr = Grouping(),
-                const FusedAct &fa = FusedAct())
+                const FusedAct &fa = FusedAct(), const Strides &sd_in = Strides())
 {
     g_last_error[0] = '\0';
-    w8a8_status st = check_problem(M, N, K, block_n, block_k, out);
-    if (st != W8A8_OK)
-        return st;
-    if ((st = check_options(o)) != W8A8_OK)
-        return st;
+    w8a8_status st;
+    const bool plain = fa.X == nullptr && gr.mode == Grouping::NONE;
+    Strides sd;
+    if (plain) {
+        // Arguments no kernel takes; then the tensor-core kernels' guards, and
+        // everything outside them falls through to the generic kernel (as the
+        // page's dispatcher does).
+        if (M < 0 || N < 0 || K < 0)
+            return fail(W8A8_ERR_INVALID_ARG, "negative size (M=%lld N=%lld K=%lld)",
+                        (long long)M, (long long)N, (long long)K);
+        if (out < W8A8_OUT_BF16 || out > W8A8_OUT_FP32)
+            return fail(W8A8_ERR_INVALID_ARG, "unknown out_dtype %d", out);
+        if (block_n < 1 || block_k < 1)
+            return fail(W8A8_ERR_INVALID_ARG, "block_n=%d block_k=%d: must be positive", block_n,
+                        block_k);
+        if ((st = check_options(o)) != W8A8_OK)
+            return st;
+        const int64_t groups = K > 0 ? cdiv(K, block_k) : 0;
+        sd.lda = sd_in.lda ? sd_in.lda : K;
+        sd.ldb = sd_in.ldb ? sd_in.ldb : K;
+        sd.ldc = sd_in.ldc ? sd_in.ldc : N;
+        sd.ld_as = sd_in.ld_as ? sd_in.ld_as : groups;
+        sd.ld_bs = sd_in.ld_bs ? sd_in.ld_bs : groups;
+        if (sd.lda < K || sd.ldb < K || sd.ldc < N || sd.ld_as < groups || sd.ld_bs < groups)
+            return fail(W8A8_ERR_INVALID_ARG, "a row stride is shorter than its row");
+        if (M == 0 || N == 0)
+            return W8A8_OK;
+        const int v = o ? o->variant : W8A8_VARIANT_AUTO;
+        const char *gap = fast_path_gap(A, a_s, B, b_s, C, M, N, K, block_n, block_k, out, sd);
+        if (v == W8A8_VARIANT_GENERIC || (v == W8A8_VARIANT_AUTO && gap))
+            return run_generic(A, a_s, B, b_s, C, M, N, K, block_n, block_k, out, sd, stream, o);
+        if (gap)
+            return fail(W8A8_ERR_UNSUPPORTED, "%s: only the generic kernel (variant AUTO or "
+                                              "GENERIC) takes this problem", gap);
+    } else {
+        if ((st = check_problem(M, N, K, block_n, block_k, out)) != W8A8_OK)
+            return st;
+        if ((st = check_options(o)) != W8A8_OK)
+            return st;
+        if (o && o->variant == W8A8_VARIANT_GENERIC)
+            return fail(W8A8_ERR_UNSUPPORTED, "grouped and fused calls run on the tensor cores");
+        sd.lda = sd.ldb = K;
+        sd.ldc = N;
+        sd.ld_as = sd.ld_bs = cdiv(K, 128);
+    }
     const bool fused = fa.X != nullptr;
     if (fused) {
         if (fa.kind < W8A8_IN_BF16 || fa.kind > W8A8_IN_FP32)
@@ -598,7 +714,7 @@ w8a8_status run(const void *A, const float *a_s, const void *B, const float *b_s
     cudaError_t e;
     if (pl.variant == W8A8_VARIANT_SMALLM) {
         CUtensorMap mB;
-        if ((st = encode_u8_map(&mB, B, N, K, 32)) != W8A8_OK)
+        if ((st = encode_u8_map(&mB, B, N, K, 32, 0, sd.ldb)) != W8A8_OK)
             return st;
         SmallParams p = {};
         p.A = static_cast<const uint8_t *>(A);
@@ -610,6 +726,8 @@ w8a8_status run(const void *A, const float *a_s, const void *B, const float *b_s
         p.K = static_cast<int>(K);
         p.G = G;
         p.out_kind = out;
+        p.lda = sd.lda;
+        p.ldc = sd.ldc;
         p.prefetch_weights = (o && o->pdl && o->weights_static) ? 1 : 0;
         p.debug_skip_tma = debug_skip;
         p.status = info.status;
@@ -619,11 +737,11 @@ w8a8_status run(const void *A, const float *a_s, const void *B, const float *b_s
         const bool pair = pl.variant == W8A8_VARIANT_TILED_PAIR;
         CUtensorMap mA, mB, mC;
         const int chunk_cols = out == W8A8_OUT_FP32 ? 16 : 32;   // 64 bytes of a row
-        if ((st = encode_u8_map(&mA, A, M, K, 128)) != W8A8_OK ||
+        if ((st = encode_u8_map(&mA, A, M, K, 128, 0, sd.lda)) != W8A8_OK ||
             (st = encode_u8_map(&mB, B, N, K, pair ? pl.bn / 2 : pl.bn,
-                                contiguous ? gr.experts : 0)) != W8A8_OK ||
-            (st = encode_out_map(&mC, C, M, N, out, chunk_cols, 32, CU_TENSOR_MAP_SWIZZLE_64B)) !=
-                W8A8_OK)
+                                contiguous ? gr.experts : 0, sd.ldb)) != W8A8_OK ||
+            (st = encode_out_map(&mC, C, M, N, out, chunk_cols, 32, CU_TENSOR_MAP_SWIZZLE_64B, 0,
+                                 sd.ldc)) != W8A8_OK)
             return st;
         TiledParams p = {};
         p.a_s = a_s;
@@ -658,12 +776,12 @@ w8a8_status run(const void *A, const float *a_s, const void *B, const float *b_s
         CUtensorMap mW, mX, mC;
         const int64_t slabs = masked ? gr.experts : 0;
         // (fused: mX maps the unquantised X, 128 columns by mma_n rows, no swizzle)
-        if ((st = encode_u8_map(&mW, B, N, K, 128, slabs)) != W8A8_OK ||
+        if ((st = encode_u8_map(&mW, B, N, K, 128, slabs, sd.ldb)) != W8A8_OK ||
             (st = fused ? encode_out_map(&mX, const_cast<void *>(fa.X), M, K, fa.kind, 128,
                                          pl.mma_n, CU_TENSOR_MAP_SWIZZLE_NONE)
-                        : encode_u8_map(&mX, A, M, K, pl.mma_n, slabs)) != W8A8_OK ||
+                        : encode_u8_map(&mX, A, M, K, pl.mma_n, slabs, sd.lda)) != W8A8_OK ||
             (st = encode_out_map(&mC, C, M, N, out, 128, pl.mma_n, CU_TENSOR_MAP_SWIZZLE_NONE,
-                                 slabs)) != W8A8_OK)
+                                 slabs, sd.ldc)) != W8A8_OK)
             return st;
         SwapParams p = {};
         p.a_s = a_s;
@@ -697,6 +815,7 @@ w8a8_status run(const void *A, const float *a_s, const void *B, const float *b_s
         p.tiles_per_expert = pl.m_tiles;
         p.X = fused ? fa.X : nullptr;
         p.x_kind = fa.kind;
+        p.ldc = sd.ldc;
         p.splits = pl.splits;
         p.groups_per_split = pl.gps;
         p.out_kind = out;
@@ -745,6 +864,25 @@ w8a8_status w8a8_block_fp8_matmul_ex(const void *A_dev, const float *a_s_dev, co
 {
     return run(A_dev, a_s_dev, B_dev, b_s_dev, C_dev, M, N, K, block_n, block_k, out_dtype,
                reinterpret_cast<cudaStream_t>(stream), opts);
+}
+
+w8a8_status w8a8_block_fp8_matmul_strided(const void *A_dev, int64_t lda, const float *a_s_dev,
+                                          int64_t ld_as, const void *B_dev, int64_t ldb,
+                                          const float *b_s_dev, int64_t ld_bs, void *C_dev,
+                                          int64_t ldc, int64_t M, int64_t N, int64_t K, int block_n,
+                                          int block_k, w8a8_out_dtype out_dtype,
+                                          w8a8_stream_t stream, const w8a8_options *opts)
+{
+    if (lda < 0 || ld_as < 0 || ldb < 0 || ld_bs < 0 || ldc < 0)
+        return fail(W8A8_ERR_INVALID_ARG, "negative row stride");
+    Strides sd;
+    sd.lda = lda;
+    sd.ldb = ldb;
+    sd.ldc = ldc;
+    sd.ld_as = ld_as;
+    sd.ld_bs = ld_bs;
+    return run(A_dev, a_s_dev, B_dev, b_s_dev, C_dev, M, N, K, block_n, block_k, out_dtype,
+               reinterpret_cast<cudaStream_t>(stream), opts, Grouping(), FusedAct(), sd);
 }
 
 w8a8_status w8a8_block_fp8_quant_matmul(const void *X_dev, w8a8_in_dtype x_dtype, const void *B_dev,
@@ -908,8 +1046,22 @@ w8a8_status w8a8_block_fp8_plan(int64_t M, int64_t N, int64_t K, w8a8_out_dtype 
     if (!plan_out)
         return fail(W8A8_ERR_INVALID_ARG, "plan_out is NULL");
     w8a8_status st = check_problem(M, N, K, 128, 128, out_dtype);
-    if (st != W8A8_OK || (st = check_options(opts)) != W8A8_OK)
+    if (st == W8A8_ERR_INVALID_ARG)
         return st;
+    const w8a8_status guards = st;
+    if ((st = check_options(opts)) != W8A8_OK)
+        return st;
+    const int v = opts ? opts->variant : W8A8_VARIANT_AUTO;
+    if (v == W8A8_VARIANT_GENERIC || (guards != W8A8_OK && v == W8A8_VARIANT_AUTO)) {
+        // outside the tensor-core kernels' size guards: the generic kernel
+        std::memset(plan_out, 0, sizeof(*plan_out));
+        plan_out->variant = W8A8_VARIANT_GENERIC;
+        plan_out->grid_limit = static_cast<int>(std::min<int64_t>(cdiv(M, 64) * cdiv(N, 64), 1ll << 30));
+        g_last_error[0] = '\0';
+        return W8A8_OK;
+    }
+    if (guards != W8A8_OK)
+        return guards;
     int dev;
     DeviceInfo info;
     if ((st = current_device(&dev, &info)) != W8A8_OK)

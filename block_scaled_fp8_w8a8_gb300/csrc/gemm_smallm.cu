@@ -127,7 +127,7 @@ __global__ void __launch_bounds__(kThreads)
     const int chunks = K / 16;
     for (int c = tid; c < M * chunks; c += kThreads) {
         const int m = c / chunks, k0 = (c - m * chunks) * 16;
-        const uint4 v = *reinterpret_cast<const uint4 *>(p.A + static_cast<size_t>(m) * K + k0);
+        const uint4 v = *reinterpret_cast<const uint4 *>(p.A + static_cast<size_t>(m) * p.lda + k0);
         float f[16];
         decode16(v, f);
         float4 *dst = reinterpret_cast<float4 *>(sA + static_cast<size_t>(m) * K + k0);
@@ -215,7 +215,7 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
         for (int w = 0; w < kWarps; ++w)
             s += sRed[(w * MM + m) * kRows + r];
-        store_out(p.C, static_cast<size_t>(m) * p.N + n, s, p.out_kind);
+        store_out(p.C, static_cast<size_t>(m) * p.ldc + n, s, p.out_kind);
     }
 }
 

@@ -592,7 +592,8 @@ __global__ void __launch_bounds__(SwapLayout<MT>::kThreads, SwapLayout<MT>::kMin
                     }
                     for (; s < p.splits; ++s)
                         add4(sum, __ldcg(reinterpret_cast<const float4 *>(src + s * plane)));
-                    store4(p.C, off, sum, p.out_kind);
+                    store4(p.C, static_cast<size_t>(m0 + r) * p.ldc + nb * 128 + 4 * c4, sum,
+                           p.out_kind);
                 }
                 if (tid == 0)
                     p.counters[tile] = 0u;   // ready for the next call
@@ -635,7 +636,7 @@ __global__ void __launch_bounds__(SwapLayout<MT>::kThreads, SwapLayout<MT>::kMin
                 }
                 for (; s < p.splits; ++s)
                     add4(sum, ld_cluster_f4(cluster_map(local, static_cast<uint32_t>(s))));
-                store4(p.C, (c_row0 + r) * p.N + nb * 128 + 4 * c4, sum, p.out_kind);
+                store4(p.C, (c_row0 + r) * p.ldc + nb * 128 + 4 * c4, sum, p.out_kind);
             }
         }
         cluster_sync();                      // no CTA leaves while its tile is being read

@@ -92,6 +92,7 @@ struct SwapParams {
     // reading A and a_s.  nullptr: A and a_s are read.
     const void *X;
     int x_kind;
+    long long ldc;         // elements per row of C (N when dense; grouped layouts are dense)
 };
 
 // Up to four byte ranges copied by one gather kernel (host-mapped sources).
@@ -113,11 +114,12 @@ struct LaunchCfg {
 // Small M (at most kSmallMaxM tokens) on the CUDA cores: 32 weight rows per CTA.
 constexpr int kSmallMaxM = 16;
 struct SmallParams {
-    const uint8_t *A;      // [M, K]
+    const uint8_t *A;      // [M, lda]
     const float *a_s;      // [M, G]
     const float *b_s;      // [NB, G]
-    void *C;               // [M, N]
+    void *C;               // [M, ldc]
     int M, N, K, G;
+    long long lda, ldc;    // row strides in elements (K and N when dense)
     int out_kind;
     int prefetch_weights;  // issue the weight loads before waiting on the previous grid
     int debug_skip_tma;    // test hook: >= 0 skips the weight load of that K group
@@ -126,6 +128,21 @@ struct SmallParams {
 };
 size_t smallm_smem_bytes(int M, int K);     // 0: M outside 1..kSmallMaxM
 cudaError_t launch_smallm(const CUtensorMap &tmB, const SmallParams &p, const LaunchCfg &cfg);
+
+// Generic fall-through on the CUDA cores: any sizes, strides (in elements),
+// alignments and scale block sizes.  64 x 64 tiles of C per CTA.
+struct GenericParams {
+    const uint8_t *A;      // [M, lda]
+    const float *a_s;      // [M, ld_as], ceil(K / block_k) used
+    const uint8_t *B;      // [N, ldb]
+    const float *b_s;      // [ceil(N / block_n), ld_bs]
+    void *C;               // [M, ldc] of out_kind
+    int64_t M, N, K;
+    int64_t lda, ldb, ldc, ld_as, ld_bs;
+    int64_t block_n, block_k;
+    int out_kind;
+};
+cudaError_t launch_generic(const GenericParams &p, const LaunchCfg &cfg);
 
 // Shared memory bytes each kernel configuration needs (0 = unsupported configuration).
 size_t tiled_smem_bytes(int bn, int stages);

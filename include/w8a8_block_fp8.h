@@ -25,13 +25,20 @@
  *    asynchronous on `stream` (a cudaStream_t; NULL is the legacy default
  *    stream): the caller keeps the buffers alive until the stream has passed
  *    the call.  C is fully overwritten; it need not be initialised.
- *  - Supported problems (anything else returns W8A8_ERR_UNSUPPORTED before any
- *    CUDA call; the shape guards of the page's Numerical safety section):
- *    block_n == block_k == 128; K >= 16 and K % 16 == 0 (16-byte rows of A
- *    and B); N >= 1 with N % 8 == 0 for bf16/fp16 output and N % 4 == 0 for
- *    fp32 output (16-byte rows of C); M >= 0; A/B/C 16-byte aligned, a_s/b_s
- *    4-byte aligned, dense row-major tensors.  M == 0 returns W8A8_OK and
- *    launches nothing.
+ *  - The tensor-core kernels take the problems inside the shape guards of the
+ *    page's Numerical safety section: block_n == block_k == 128; K >= 16 and
+ *    K % 16 == 0 (16-byte rows of A and B); N % 8 == 0 for bf16/fp16 output
+ *    and N % 4 == 0 for fp32 output (16-byte rows of C); A/B/C 16-byte
+ *    aligned, a_s/b_s 4-byte aligned; row strides that are multiples of 16
+ *    bytes and dense scale rows.  As in the page's dispatcher, every other
+ *    problem of the plain matmul calls (w8a8_block_fp8_matmul, _ex, _strided)
+ *    falls through to a generic CUDA-core kernel (W8A8_VARIANT_GENERIC): any
+ *    M, N, K >= 0 (K == 0 gives zeros), any block_n, block_k >= 1, any row
+ *    strides, A and B at any address, C aligned to its element size and
+ *    a_s/b_s to 4 bytes.  M == 0 or N == 0 returns W8A8_OK and launches
+ *    nothing.  The grouped, fused, host-buffer and allocation-free calls run
+ *    on the tensor cores only and return W8A8_ERR_UNSUPPORTED outside the
+ *    guards, before any CUDA call.
  *  - Errors are returned synchronously as w8a8_status; a human-readable detail
  *    string for the calling thread's last error is available from
  *    w8a8_last_error().  A device-side wait that gives up (a bounded wait that
@@ -85,11 +92,14 @@ typedef enum {
     W8A8_VARIANT_SMALLM = 5,         /* M <= 16: dot products on the CUDA cores, 32 weight
                                         rows per CTA (no tensor memory); K limited by
                                         shared memory (M x K x 4 + 32 x K bytes)            */
-    W8A8_VARIANT_TILED_PAIR = 6      /* as TILED, but two CTAs (a cluster of 2 on one SM
+    W8A8_VARIANT_TILED_PAIR = 6,     /* as TILED, but two CTAs (a cluster of 2 on one SM
                                         pair) share one 256 x BN tile through
                                         tcgen05 .cta_group::2 MMAs: each loads its 128 rows
                                         of A and half of the tile's BN rows of B; for large
                                         M.  Not for the grouped layouts.                    */
+    W8A8_VARIANT_GENERIC = 7         /* CUDA cores, 64 x 64 tiles, plain loads: any sizes,
+                                        strides, alignments and scale block sizes (the
+                                        fall-through of AUTO outside the guards above)     */
 } w8a8_variant;
 
 /*
@@ -149,8 +159,10 @@ typedef struct {
 
 /*
  * C = A * B^T with block de-quantisation, as defined at the top of this file.
- * block_n and block_k give the scale granularity and must both be 128.
- * All pointers are device pointers; asynchronous on `stream`.
+ * block_n and block_k give the scale granularity (128 x 128 on the tensor
+ * cores; other positive sizes, with a_s [M, ceil(K/block_k)] and b_s
+ * [ceil(N/block_n), ceil(K/block_k)], run on the generic kernel).  Dense
+ * row-major tensors.  All pointers are device pointers; asynchronous on `stream`.
  */
 w8a8_status w8a8_block_fp8_matmul(const void *A_dev, const float *a_s_dev,
                                   const void *B_dev, const float *b_s_dev, void *C_dev,
@@ -163,6 +175,29 @@ w8a8_status w8a8_block_fp8_matmul_ex(const void *A_dev, const float *a_s_dev,
                                      int64_t M, int64_t N, int64_t K, int block_n, int block_k,
                                      w8a8_out_dtype out_dtype, w8a8_stream_t stream,
                                      const w8a8_options *opts);
+
+/*
+ * As w8a8_block_fp8_matmul_ex with explicit row strides and scale block sizes.
+ *
+ *   A    [M, lda] bytes, the first K of each row used        (lda >= K)
+ *   a_s  [M, ld_as] floats, the first ceil(K / block_k) used (ld_as >= that)
+ *   B    [N, ldb] bytes, the first K of each row used        (ldb >= K)
+ *   b_s  [ceil(N / block_n), ld_bs] floats                   (ld_bs >= ceil(K / block_k))
+ *   C    [M, ldc] elements of out_dtype, the first N written (ldc >= N)
+ *
+ * A stride of 0 means the dense value (K, K, N, ceil(K/block_k)); a stride
+ * shorter than its row is W8A8_ERR_INVALID_ARG.  Scale group g covers
+ * k in [g*block_k, min((g+1)*block_k, K)) and weight rows n use b_s row
+ * n / block_n.  Problems inside the tensor-core guards (block sizes 128,
+ * strides that are multiples of 16 bytes, dense scale rows, ...) run on the
+ * tensor-core kernels; the rest on the generic kernel.
+ */
+w8a8_status w8a8_block_fp8_matmul_strided(const void *A_dev, int64_t lda, const float *a_s_dev,
+                                          int64_t ld_as, const void *B_dev, int64_t ldb,
+                                          const float *b_s_dev, int64_t ld_bs, void *C_dev,
+                                          int64_t ldc, int64_t M, int64_t N, int64_t K, int block_n,
+                                          int block_k, w8a8_out_dtype out_dtype,
+                                          w8a8_stream_t stream, const w8a8_options *opts);
 
 /*
  * End-to-end call on HOST buffers: brings A, a_s, B and b_s from host memory

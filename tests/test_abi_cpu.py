@@ -46,15 +46,13 @@ def test_options_struct_layout():
 
 
 @pytest.mark.parametrize("M,N,K,bn,bk,out,status", [
-    (4, 100, 256, 128, 128, 0, w8.W8A8_ERR_UNSUPPORTED),     # N % 16
-    (4, 128, 250, 128, 128, 0, w8.W8A8_ERR_UNSUPPORTED),     # K % 128
-    (4, 128, 0, 128, 128, 0, w8.W8A8_ERR_UNSUPPORTED),       # K == 0
-    (4, 0, 128, 128, 128, 0, w8.W8A8_ERR_UNSUPPORTED),       # N == 0
-    (4, 128, 256, 64, 128, 0, w8.W8A8_ERR_UNSUPPORTED),      # block_n
-    (4, 128, 256, 128, 256, 0, w8.W8A8_ERR_UNSUPPORTED),     # block_k
-    (-1, 128, 256, 128, 128, 0, w8.W8A8_ERR_INVALID_ARG),    # negative M
-    (4, 128, 256, 128, 128, 7, w8.W8A8_ERR_INVALID_ARG),     # out dtype
-    (0, 128, 256, 128, 128, 0, w8.W8A8_OK),                  # empty M: nothing to do
+    (4, 128, 256, 0, 128, 0, w8.W8A8_ERR_INVALID_ARG),      # block_n <= 0
+    (4, 128, 256, 128, -2, 0, w8.W8A8_ERR_INVALID_ARG),     # block_k <= 0
+    (-1, 128, 256, 128, 128, 0, w8.W8A8_ERR_INVALID_ARG),   # negative M
+    (4, -8, 256, 128, 128, 0, w8.W8A8_ERR_INVALID_ARG),     # negative N
+    (4, 128, 256, 128, 128, 7, w8.W8A8_ERR_INVALID_ARG),    # out dtype
+    (0, 128, 256, 128, 128, 0, w8.W8A8_OK),                 # empty M: nothing to do
+    (4, 0, 128, 128, 128, 0, w8.W8A8_OK),                   # empty N: nothing to do
 ])
 def test_argument_checks(lib, M, N, K, bn, bk, out, status):
     st = w8.w8a8_block_fp8_matmul(16, 16, 16, 16, 16, M, N, K, bn, bk, out, stream=0)
@@ -63,10 +61,55 @@ def test_argument_checks(lib, M, N, K, bn, bk, out, status):
         assert w8.w8a8_last_error()
 
 
+# Outside the tensor-core guards: a forced tensor-core variant is refused before
+# any CUDA call, naming the guard; AUTO falls through to the generic kernel.
+@pytest.mark.parametrize("M,N,K,bn,bk,why", [
+    (4, 100, 256, 128, 128, "16 bytes"),       # rows of C
+    (4, 128, 250, 128, 128, "multiple of 16"),  # K
+    (4, 128, 0, 128, 128, "multiple of 16"),    # K == 0
+    (4, 128, 256, 64, 128, "scale blocks"),     # block_n
+    (4, 128, 256, 128, 256, "scale blocks"),    # block_k
+])
+def test_forced_tensor_core_variant_outside_guards(lib, M, N, K, bn, bk, why):
+    o = w8.options(variant=w8.W8A8_VARIANT_TILED)
+    st = w8.w8a8_block_fp8_matmul_ex(16, 16, 16, 16, 16, M, N, K, bn, bk, 0, opts=o, stream=0)
+    assert st == w8.W8A8_ERR_UNSUPPORTED
+    assert why in w8.w8a8_last_error()
+
+
+def test_outside_guards_reaches_the_device_query(lib):
+    """AUTO outside the guards passes validation and goes for the device (the
+    generic kernel): without a GPU that is W8A8_ERR_NO_DEVICE.  (Not run where
+    a GPU is present: the pointers here are fake.)"""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    for (M, N, K, bn, bk) in [(4, 100, 256, 128, 128), (4, 128, 250, 128, 128),
+                              (4, 128, 256, 64, 32), (4, 128, 0, 128, 128)]:
+        st = w8.w8a8_block_fp8_matmul(16, 16, 16, 16, 16, M, N, K, bn, bk, 0, stream=0)
+        assert st == w8.W8A8_ERR_NO_DEVICE, (M, N, K, bn, bk, w8.w8a8_last_error())
+
+
+def test_stride_checks(lib):
+    f = w8.w8a8_block_fp8_matmul_strided
+    # a stride shorter than its row, or negative
+    assert f(16, 100, 16, 2, 16, 256, 16, 2, 16, 128, 4, 128, 256, stream=0) == w8.W8A8_ERR_INVALID_ARG
+    assert f(16, 256, 16, 1, 16, 256, 16, 2, 16, 128, 4, 128, 256, stream=0) == w8.W8A8_ERR_INVALID_ARG
+    assert f(16, 256, 16, 2, 16, 256, 16, 2, 16, 64, 4, 128, 256, stream=0) == w8.W8A8_ERR_INVALID_ARG
+    assert f(16, -1, 16, 2, 16, 256, 16, 2, 16, 128, 4, 128, 256, stream=0) == w8.W8A8_ERR_INVALID_ARG
+    # a stride that is not a multiple of 16 bytes keeps a forced tensor-core variant out
+    o = w8.options(variant=w8.W8A8_VARIANT_SWAPAB)
+    st = f(16, 264, 16, 2, 16, 256, 16, 2, 16, 128, 4, 128, 256, stream=0, opts=o)
+    assert st == w8.W8A8_ERR_INVALID_ARG or st == w8.W8A8_ERR_UNSUPPORTED
+
+
 def test_pointer_checks(lib):
     assert w8.w8a8_block_fp8_matmul(0, 16, 16, 16, 16, 4, 128, 256, stream=0) == w8.W8A8_ERR_INVALID_ARG
-    assert w8.w8a8_block_fp8_matmul(16, 16, 24, 16, 16, 4, 128, 256, stream=0) == w8.W8A8_ERR_UNSUPPORTED
+    o = w8.options(variant=w8.W8A8_VARIANT_TILED)
+    assert w8.w8a8_block_fp8_matmul_ex(16, 16, 24, 16, 16, 4, 128, 256, opts=o,
+                                       stream=0) == w8.W8A8_ERR_UNSUPPORTED
     assert "aligned" in w8.w8a8_last_error()
+    # the generic kernel needs 4-byte aligned scales too: refused before any CUDA call
     assert w8.w8a8_block_fp8_matmul(16, 18, 16, 16, 16, 4, 128, 256, stream=0) == w8.W8A8_ERR_UNSUPPORTED
 
 

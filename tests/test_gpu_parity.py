@@ -204,8 +204,13 @@ def test_invalid_calls_do_not_launch():
     x = synth.make_inputs(8, 128, 256, seed=0)
     A, a_s, B, b_s = to_device(x)
     C = torch.empty((8, 128), dtype=torch.bfloat16, device="cuda")
-    assert w8.w8a8_block_fp8_matmul(A, a_s, B, b_s, C, 8, 128, 256, 64, 128) == w8.W8A8_ERR_UNSUPPORTED
-    assert w8.w8a8_block_fp8_matmul(A.data_ptr() + 1, a_s, B, b_s, C, 8, 128, 256) == w8.W8A8_ERR_UNSUPPORTED
+    # outside the tensor-core guards a forced tensor-core variant is refused
+    # (AUTO would run the generic kernel: tests/test_gpu_generic.py)
+    tiled = w8.options(variant=w8.W8A8_VARIANT_TILED)
+    assert w8.w8a8_block_fp8_matmul_ex(A, a_s, B, b_s, C, 8, 128, 256, 64, 128,
+                                       opts=tiled) == w8.W8A8_ERR_UNSUPPORTED
+    assert w8.w8a8_block_fp8_matmul_ex(A.data_ptr() + 1, a_s, B, b_s, C, 8, 128, 256,
+                                       opts=tiled) == w8.W8A8_ERR_UNSUPPORTED
     assert w8.w8a8_block_fp8_matmul(A, a_s, B, b_s, C, 0, 128, 256) == w8.W8A8_OK
     ws = torch.empty(16, dtype=torch.uint8, device="cuda")
     o = w8.options(variant=w8.W8A8_VARIANT_SPLITK, split_k=2, workspace_dev=ws.data_ptr(),
