@@ -374,9 +374,11 @@ w8a8_status make_plan(int64_t M, int64_t N, int64_t K, int out_bytes, const w8a8
     const int tile_bytes = (cluster && splits > 1) ? 4 : out_bytes;
     int max_stages = std::min(8, gps);
     int stages = stage_hint ? std::min(stage_hint, max_stages) : max_stages;
-    while (stages > 1 && swapab_smem_bytes(mt, stages, gps, tile_bytes, x_esize) > dev.smem_optin)
+    const int csplits = (cluster && splits > 1) ? splits : 0;
+    while (stages > 1 &&
+           swapab_smem_bytes(mt, stages, gps, tile_bytes, x_esize, csplits) > dev.smem_optin)
         --stages;
-    if (swapab_smem_bytes(mt, stages, gps, tile_bytes, x_esize) > dev.smem_optin)
+    if (swapab_smem_bytes(mt, stages, gps, tile_bytes, x_esize, csplits) > dev.smem_optin)
         return fail(W8A8_ERR_UNSUPPORTED,
                     "K=%lld is too long for one swap-AB CTA; use the split-K variant",
                     (long long)K);
@@ -386,7 +388,7 @@ w8a8_status make_plan(int64_t M, int64_t N, int64_t K, int out_bytes, const w8a8
     pl->splits = splits;
     pl->gps = gps;
     pl->stages = stages;
-    pl->smem = swapab_smem_bytes(mt, stages, gps, tile_bytes, x_esize);
+    pl->smem = swapab_smem_bytes(mt, stages, gps, tile_bytes, x_esize, csplits);
     pl->tile_bytes = tile_bytes;
     if (splits == 1)
         pl->variant = W8A8_VARIANT_SWAPAB;

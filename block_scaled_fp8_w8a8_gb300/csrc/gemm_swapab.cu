@@ -42,7 +42,7 @@ template <int MT> struct SwapLayout {
     static constexpr uint32_t kWBytes = 128u * 128u;
     static constexpr uint32_t kXBytes = static_cast<uint32_t>(MT) * 128u;
     static constexpr uint32_t kTmemCols = 2 * MT < 32 ? 32 : 2 * MT;
-    static constexpr int kBars = 2 * kMaxStages + 5;
+    static constexpr int kBars = 2 * kMaxStages + 6;
     // Operand stages; after the main loop the same bytes hold the C tile.
     // Fused activation quantisation adds, per stage, the unquantised token
     // tile as the TMA brings it: MT rows of 128 elements of x_esize bytes.
@@ -56,11 +56,19 @@ template <int MT> struct SwapLayout {
         const size_t ct = static_cast<size_t>(MT) * 128 * out_bytes;
         return st > ct ? st : ct;
     }
-    static size_t smem(int stages, int gps, int out_bytes, int x_esize = 0)
+    // Cluster split-K: each CTA receives, from every split, the rows of the
+    // tile it reduces: `splits` slots of ceil(MT / splits) rows of 128 fp32.
+    __host__ __device__ static int recv_slot_rows(int splits) { return (MT + splits - 1) / splits; }
+    __host__ __device__ static size_t recv_bytes(int splits)
     {
-        // + one "activation codes ready" barrier per K group (fused quantisation)
+        return splits > 1 ? static_cast<size_t>(splits) * recv_slot_rows(splits) * 128 * 4 : 0;
+    }
+    static size_t smem(int stages, int gps, int out_bytes, int x_esize = 0, int cluster_splits = 0)
+    {
+        // + one "activation codes ready" barrier per K group (fused quantisation),
+        // + the cluster receive area (16-byte aligned)
         return 1024 + area(stages, out_bytes, x_esize) + static_cast<size_t>(gps) * MT * 4 + kBars * 8 + 16 +
-               static_cast<size_t>(gps) * 8;
+               static_cast<size_t>(gps) * 8 + 16 + recv_bytes(cluster_splits);
     }
 };
 
@@ -184,6 +192,7 @@ __global__ void __launch_bounds__(SwapLayout<MT>::kThreads, SwapLayout<MT>::kMin
     auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * kMaxStages + b); };
     auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * kMaxStages + 2 + b); };
     const uint32_t drain_bar = bar0 + 8u * (2 * kMaxStages + 4);
+    const uint32_t recv_bar = bar0 + 8u * (2 * kMaxStages + 5);   // cluster split-K
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + L::kBars);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     volatile int *last_flag = reinterpret_cast<volatile int *>(tmem_slot + 2);
@@ -192,6 +201,8 @@ __global__ void __launch_bounds__(SwapLayout<MT>::kThreads, SwapLayout<MT>::kMin
     // quantiser warps once the group's codes and scales are in shared memory.
     const uint32_t ready0 = smem_addr(tmem_slot + 4);
     auto ready_bar = [&](int i) { return ready0 + 8u * i; };
+    // Cluster split-K receive area: [split][row of this CTA's share][128] fp32.
+    const uint32_t recv0 = (ready0 + 8u * static_cast<uint32_t>(p.groups_per_split) + 15u) & ~15u;
 
     const uint32_t warp = warp_index(), lane = lane_index();
     const int nb = blockIdx.x;                 // 128-row block of B (and of C's columns)
@@ -216,6 +227,8 @@ __global__ void __launch_bounds__(SwapLayout<MT>::kThreads, SwapLayout<MT>::kMin
             mbar_init(tempty_bar(b), 4 * L::kPromoWG);
         }
         mbar_init(drain_bar, 1);
+        if (p.cluster_reduce)
+            mbar_init(recv_bar, 1);
         if constexpr (FUSED)
             for (int i = 0; i < p.groups_per_split; ++i)
                 mbar_init(ready_bar(i), 2);
@@ -235,6 +248,11 @@ __global__ void __launch_bounds__(SwapLayout<MT>::kThreads, SwapLayout<MT>::kMin
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
+    // Cluster split-K: every CTA's receive barrier is initialised before any
+    // split pushes into it.  (This sync runs before the dependency wait, so it
+    // overlaps the previous kernel.)
+    if (p.cluster_reduce)
+        cluster_sync();
     const uint32_t tmem_base = *tmem_slot;
     const WaitGuard guard{abort_flag, p.status, p.wait_limit};
 
@@ -601,45 +619,59 @@ __global__ void __launch_bounds__(SwapLayout<MT>::kThreads, SwapLayout<MT>::kMin
         }
     }
 
-    if (p.cluster_reduce) {
-        // Every thread of every CTA of the cluster passes both barriers exactly once.
-        cluster_sync();                      // all partial tiles are in shared memory
-        if (warp >= 4) {
-            // This CTA (cluster rank r of S) reduces rows [r0, r1) of the tile:
-            // items of 4 consecutive columns, consecutive threads on consecutive
-            // items, the S partials summed in rank order 0..S-1 (the same order,
-            // and so the same bits, as the workspace reduction).
-            uint32_t rank;
-            asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(rank));
-            const int tid = static_cast<int>(threadIdx.x) - 128;
-            constexpr int kPromoThreads = 128 * L::kPromoWG;
-            const int rows = grouped ? *rows_slot : min(p.mma_n, p.M - m0);
+    if (p.cluster_reduce && warp >= 4) {
+        // Cluster split-K.  The splits of a tile form one cluster; the CTA of
+        // cluster rank r reduces rows [r0, r1) of the tile.  Every split pushes
+        // each row of its partial tile (in shared memory since the promotion)
+        // into the receive area of that row's owner with asynchronous 16-byte
+        // stores counted on the owner's receive barrier; each owner waits for
+        // its barrier, sums the splits' rows in split order 0..S-1 (the same
+        // order, and so the same bits, as the workspace reduction) and stores
+        // them.  No CTA reads another's shared memory, and a CTA leaves only
+        // after everything pushed into it has landed.  (After a timeout the
+        // pushed rows are garbage and the status word already says so.)
+        uint32_t rank;
+        asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(rank));
+        const int tid = static_cast<int>(threadIdx.x) - 128;
+        constexpr int kPromoThreads = 128 * L::kPromoWG;
+        const int S = p.splits;
+        const int rows = grouped ? *rows_slot : min(p.mma_n, p.M - m0);
+        const int slot_rows = L::recv_slot_rows(S);
+        named_barrier(1, kPromoThreads);              // the whole partial tile is written
+        const uint32_t tile = smem_addr(smem);
+        for (int it = tid; it < rows * 32; it += kPromoThreads) {
+            const int r = it >> 5, c4 = it & 31;
+            const int owner = (S * (r + 1) - 1) / rows;
+            const int r_own0 = rows * owner / S;
+            float4 v;
+            asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                         : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                         : "r"(tile + static_cast<uint32_t>(r * 128 + 4 * c4) * 4u));
+            const uint32_t dst = recv0 + static_cast<uint32_t>(((static_cast<int>(rank) * slot_rows +
+                                                                (r - r_own0)) * 128 + 4 * c4) * 4);
+            st_async_v4(cluster_map(dst, static_cast<uint32_t>(owner)), v,
+                        cluster_map(recv_bar, static_cast<uint32_t>(owner)));
+        }
+        const int r0 = rows * static_cast<int>(rank) / S;
+        const int r1 = rows * (static_cast<int>(rank) + 1) / S;
+        if (tid == 0)
+            mbar_arrive_expect_tx(recv_bar, static_cast<uint32_t>(S * (r1 - r0) * 128 * 4));
+        const bool got = __all_sync(0xffffffffu,
+                                    wait_bounded_cluster(recv_bar, 0, guard, SITE_SWAP_PROMOTE));
+        if (got) {
             const size_t c_row0 = static_cast<size_t>(expert) * p.M + m0;
-            const int r0 = rows * static_cast<int>(rank) / p.splits;
-            const int r1 = rows * (static_cast<int>(rank) + 1) / p.splits;
             const int c4n = min(128, p.N - nb * 128) / 4;
-            const int items = (r1 - r0) * c4n;
-            const uint32_t tile = smem_addr(smem);
-            for (int it = tid; it < items; it += kPromoThreads) {
-                const int r = r0 + it / c4n, c4 = it % c4n;
-                const uint32_t local = tile + static_cast<uint32_t>(r * 128 + 4 * c4) * 4u;
+            const float *recv = reinterpret_cast<const float *>(smem_raw) +
+                                (recv0 - smem_addr(smem_raw)) / 4;
+            for (int it = tid; it < (r1 - r0) * c4n; it += kPromoThreads) {
+                const int rl = it / c4n, c4 = it - (it / c4n) * c4n;
                 float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
-                int s = 0;
-                for (; s + 8 <= p.splits; s += 8) {
-                    float4 v[8];
-#pragma unroll
-                    for (int u = 0; u < 8; ++u)
-                        v[u] = ld_cluster_f4(cluster_map(local, static_cast<uint32_t>(s + u)));
-#pragma unroll
-                    for (int u = 0; u < 8; ++u)
-                        add4(sum, v[u]);
-                }
-                for (; s < p.splits; ++s)
-                    add4(sum, ld_cluster_f4(cluster_map(local, static_cast<uint32_t>(s))));
-                store4(p.C, (c_row0 + r) * p.ldc + nb * 128 + 4 * c4, sum, p.out_kind);
+                for (int s2 = 0; s2 < S; ++s2)
+                    add4(sum, *reinterpret_cast<const float4 *>(
+                                  recv + (static_cast<size_t>(s2 * slot_rows + rl) * 128 + 4 * c4)));
+                store4(p.C, (c_row0 + r0 + rl) * p.ldc + nb * 128 + 4 * c4, sum, p.out_kind);
             }
         }
-        cluster_sync();                      // no CTA leaves while its tile is being read
     }
 
     tc_fence_before_sync();
@@ -657,7 +689,8 @@ cudaError_t launch_swapab_t(const CUtensorMap &tmW, const CUtensorMap &tmX, cons
     using L = SwapLayout<MT>;
     auto kernel = k_swapab<MT, GROUPED, FUSED>;
     const size_t smem = L::smem(cfg.stages, p.groups_per_split, p.out_bytes,
-                                FUSED ? (p.x_kind == W8A8_IN_FP32 ? 4 : 2) : 0);
+                                FUSED ? (p.x_kind == W8A8_IN_FP32 ? 4 : 2) : 0,
+                                p.cluster_reduce ? p.splits : 0);
     static volatile int smem_set[kMaxDeviceFlags] = {};
     cudaError_t e = ensure_smem_limit(kernel, smem_set);
     if (e != cudaSuccess)
@@ -701,15 +734,16 @@ cudaError_t launch_swapab_t(const CUtensorMap &tmW, const CUtensorMap &tmX, cons
 
 }  // namespace
 
-size_t swapab_smem_bytes(int mt, int stages, int gps, int out_bytes, int x_esize)
+size_t swapab_smem_bytes(int mt, int stages, int gps, int out_bytes, int x_esize,
+                         int cluster_splits)
 {
     if (stages < 1 || stages > kMaxStages)
         return 0;
     switch (mt) {
-    case 32: return SwapLayout<32>::smem(stages, gps, out_bytes, x_esize);
-    case 64: return SwapLayout<64>::smem(stages, gps, out_bytes, x_esize);
-    case 128: return SwapLayout<128>::smem(stages, gps, out_bytes, x_esize);
-    case 256: return SwapLayout<256>::smem(stages, gps, out_bytes, x_esize);
+    case 32: return SwapLayout<32>::smem(stages, gps, out_bytes, x_esize, cluster_splits);
+    case 64: return SwapLayout<64>::smem(stages, gps, out_bytes, x_esize, cluster_splits);
+    case 128: return SwapLayout<128>::smem(stages, gps, out_bytes, x_esize, cluster_splits);
+    case 256: return SwapLayout<256>::smem(stages, gps, out_bytes, x_esize, cluster_splits);
     default: return 0;
     }
 }

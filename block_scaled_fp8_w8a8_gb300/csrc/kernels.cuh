@@ -147,7 +147,9 @@ cudaError_t launch_generic(const GenericParams &p, const LaunchCfg &cfg);
 // Shared memory bytes each kernel configuration needs (0 = unsupported configuration).
 size_t tiled_smem_bytes(int bn, int stages);
 // x_esize: fused activation quantisation's input element size (0: not fused).
-size_t swapab_smem_bytes(int mt, int stages, int groups_per_split, int out_bytes, int x_esize = 0);
+// cluster_splits: the splits of a cluster split-K launch (its receive area), else 0.
+size_t swapab_smem_bytes(int mt, int stages, int groups_per_split, int out_bytes, int x_esize = 0,
+                         int cluster_splits = 0);
 
 // tmC: C as a 2-D [M, N] tensor of the output type, box {64 bytes of columns,
 // 32 rows}, 64-byte swizzle (the tiled kernel's per-warp epilogue chunks).

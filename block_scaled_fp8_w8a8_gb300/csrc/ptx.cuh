@@ -408,6 +408,47 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr)
     asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
+// Asynchronous 16-byte store into the shared memory of a CTA of the cluster
+// (addresses in the cluster's shared window, see cluster_map); its 16 bytes
+// count as completed transaction bytes on the mbarrier `cbar` of that CTA.
+__device__ __forceinline__ void st_async_v4(uint32_t caddr, float4 v, uint32_t cbar)
+{
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+                     caddr),
+                 "r"(__float_as_uint(v.x)), "r"(__float_as_uint(v.y)), "r"(__float_as_uint(v.z)),
+                 "r"(__float_as_uint(v.w)), "r"(cbar)
+                 : "memory");
+}
+
+// Bounded wait with acquire at cluster scope, for a barrier completed by
+// other CTAs of the cluster (st.async transaction bytes).
+__device__ __forceinline__ bool wait_bounded_cluster(uint32_t bar, uint32_t parity,
+                                                     const WaitGuard &g, uint32_t site)
+{
+    auto probe = [&]() {
+        uint32_t done;
+        asm volatile("{\n\t.reg .pred p;\n\t"
+                     "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+                     "selp.u32 %0, 1, 0, p;\n\t}"
+                     : "=r"(done)
+                     : "r"(bar), "r"(parity)
+                     : "memory");
+        return done != 0;
+    };
+    const long long t0 = clock64();
+    for (;;) {
+        if (probe())
+            return true;
+        if (*g.abort_flag)
+            return false;
+        if (static_cast<unsigned long long>(clock64() - t0) > g.limit) {
+            *g.abort_flag = 1;
+            atomicCAS(g.status_word, 0u, (site << 8) | 4u);
+            return false;
+        }
+    }
+}
+
 // ------------------------------------------------------------------ thread-block clusters
 
 // Cluster-wide barrier; every thread of every CTA of the cluster must call it
