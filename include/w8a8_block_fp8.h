@@ -202,12 +202,16 @@ w8a8_status w8a8_block_fp8_matmul_strided(const void *A_dev, int64_t lda, const 
 /*
  * End-to-end call on HOST buffers: brings A, a_s, B and b_s from host memory
  * into `staging_dev`, runs the matmul, and copies C back into host memory, all
- * in order on `stream`.  When all four inputs are page-locked host memory the
- * device can address (e.g. cudaHostAlloc / torch pin_memory), one gather
- * kernel reads them over the CPU-GPU link; otherwise they are copied with
- * cudaMemcpyAsync (synchronous for pageable memory).  The
+ * in order on `stream`.  When all four inputs are host memory the device can
+ * address -- page-locked memory (e.g. cudaHostAlloc / torch pin_memory) or, on
+ * a device that reads through the host's page tables (ATS, as on
+ * Grace-Blackwell nodes), also pageable memory -- one gather kernel reads them
+ * over the CPU-GPU link; otherwise they are copied with cudaMemcpyAsync
+ * (synchronous for pageable memory).  C goes back the same way: one kernel
+ * writes it where the device can address C_host, else cudaMemcpyAsync.  The
  * call returns once the work is enqueued; synchronise `stream` before reading
- * C_host.  staging_dev is caller-owned device memory of at least
+ * C_host.  With page-locked buffers the call can be captured in a CUDA graph
+ * (every replay then moves the buffers' current contents).  staging_dev is caller-owned device memory of at least
  * w8a8_block_fp8_host_staging_size(M, N, K, out_dtype) bytes, 256-byte aligned.
  */
 w8a8_status w8a8_block_fp8_matmul_host(const void *A_host, const float *a_s_host,

@@ -172,14 +172,16 @@ def test_host_buffer_call_matches_device_call():
     assert torch.equal(C_host.view(torch.int16), dev.cpu().view(torch.int16))
 
 
-@pytest.mark.parametrize("kind", ["pageable", "pinned_misaligned"])
+@pytest.mark.parametrize("kind", ["pageable", "pinned_misaligned", "pageable_all"])
 def test_host_buffer_call_other_host_memory(kind):
-    """Pageable inputs take the copy path; pinned inputs at odd addresses take
-    the gather kernel's byte path.  Both give the device call's bits."""
+    """Pageable inputs are read by the gather kernel where the device walks the
+    host's page tables (ATS), else copied; pinned inputs at odd addresses take
+    the gather kernel's byte path; a pageable result buffer is written by a
+    kernel (ATS) or copied.  All give the device call's bits."""
     M, N, K = 37, 264, 528
     x = synth.make_inputs(M, N, K, seed=2)
     dev = run(x, "bf16")
-    if kind == "pageable":
+    if kind in ("pageable", "pageable_all"):
         ins = [t.clone() for t in (x.A, x.a_s, x.B, x.b_s)]
         ptrs = [t.data_ptr() for t in ins]
     else:
@@ -190,7 +192,9 @@ def test_host_buffer_call_other_host_memory(kind):
             big[3:3 + raw.numel()] = raw
             ins.append(big)
             ptrs.append(big.data_ptr() + 3)
-    C_host = torch.empty((M, N), dtype=torch.bfloat16).pin_memory()
+    C_host = torch.empty((M, N), dtype=torch.bfloat16)
+    if kind != "pageable_all":
+        C_host = C_host.pin_memory()
     nbytes = w8.w8a8_block_fp8_host_staging_size(M, N, K, w8.W8A8_OUT_BF16)
     staging = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
     stream = torch.cuda.current_stream()
