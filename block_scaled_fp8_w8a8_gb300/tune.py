@@ -181,6 +181,8 @@ def main():
                     help="with --grid: only the shapes with this N")
     ap.add_argument("--min-m", type=int, default=0,
                     help="with --grid: only the shapes with M at least this")
+    ap.add_argument("--max-m", type=int, default=0,
+                    help="with --grid: only the shapes with M at most this")
     ap.add_argument("--jsonl", default=None,
                     help="append each shape's best configuration to this file as it is found")
     ap.add_argument("--table-from", default=None,
@@ -199,6 +201,8 @@ def main():
         shapes = [s for s in shapes if s[1] == args.grid_n]
     if args.grid and args.min_m:
         shapes = [s for s in shapes if s[0] >= args.min_m]
+    if args.grid and args.max_m:
+        shapes = [s for s in shapes if s[0] <= args.max_m]
     if args.shapes:
         shapes = [tuple(int(v) for v in s.split("x")) for s in args.shapes.split(",")]
     l2 = torch.cuda.get_device_properties(0).L2_cache_size
