@@ -62,7 +62,8 @@ class w8a8_options(ctypes.Structure):
         ("pdl", ctypes.c_int),
         ("debug_skip_load", ctypes.c_int),
         ("weights_static", ctypes.c_int),
-        ("reserved_i", ctypes.c_int * 3),
+        ("debug_fail_alloc", ctypes.c_int),
+        ("reserved_i", ctypes.c_int * 2),
         ("workspace_dev", ctypes.c_void_p),
         ("workspace_bytes", ctypes.c_size_t),
         ("wait_limit_cycles", ctypes.c_ulonglong),

@@ -417,8 +417,12 @@ size_t splitk_workspace_bytes(int64_t M, int64_t N, const Plan &pl)
     return kCounterBytes + (partial + 255) / 256 * 256;
 }
 
-w8a8_status library_workspace(int dev, cudaStream_t stream, size_t bytes, void **out)
+w8a8_status library_workspace(int dev, cudaStream_t stream, size_t bytes, void **out,
+                              bool inject_failure = false)
 {
+    if (inject_failure)     // host-side fault injection (w8a8_options.debug_fail_alloc)
+        return fail(W8A8_ERR_CUDA, "cudaMalloc(workspace) failed: out of memory (injected by "
+                                   "debug_fail_alloc)");
     std::lock_guard<std::mutex> lock(g_mutex);
     Workspace &w = g_workspaces[std::make_pair(dev, stream)];
     if (w.bytes >= bytes) {
@@ -467,7 +471,7 @@ w8a8_status acquire_workspace(const w8a8_options *o, int dev, cudaStream_t strea
         *out = ws;
         return W8A8_OK;
     }
-    return library_workspace(dev, stream, bytes, out);
+    return library_workspace(dev, stream, bytes, out, o && o->debug_fail_alloc);
 }
 
 // Grouped (MoE) calls: which layout, the device array of per-expert counts

@@ -131,6 +131,9 @@ typedef enum {
  *                      n-th operand load, so that a bounded device wait runs out
  *                      and the call surfaces W8A8_ERR_DEVICE_TIMEOUT through
  *                      w8a8_get_device_status(); C is then undefined.  0 = off.
+ *   debug_fail_alloc   test hook: 1 makes a call that would take the library's own
+ *                      workspace fail as if cudaMalloc had failed (W8A8_ERR_CUDA,
+ *                      nothing launched, the cached workspace untouched).  0 = off.
  *   workspace_dev      SPLITK and stream-K TILED: caller-owned device scratch of workspace_bytes
  *                      bytes, 256-byte aligned, at least
  *                      w8a8_block_fp8_workspace_size() bytes, all zero before its
@@ -150,7 +153,8 @@ typedef struct {
     int pdl;
     int debug_skip_load;
     int weights_static;
-    int reserved_i[3];
+    int debug_fail_alloc;
+    int reserved_i[2];
     void *workspace_dev;
     size_t workspace_bytes;
     unsigned long long wait_limit_cycles;

@@ -282,3 +282,64 @@ def test_ragged_k_and_n(M, N, K, out, variant):
     ref = oracle.reference_c(x.A, x.a_s, x.B, x.b_s)
     C = run(x, out, **VARIANTS[variant])
     assert_close(C, ref, what=f"{variant} {M}x{N}x{K} {out}")
+
+
+# ------------------------------------------------------------------ canaries and host-side faults
+
+CANARY_VARIANTS = {
+    "tiled256": dict(variant=w8.W8A8_VARIANT_TILED, block_n_tile=256),
+    "tiled192": dict(variant=w8.W8A8_VARIANT_TILED, block_n_tile=192),
+    "tiled128": dict(variant=w8.W8A8_VARIANT_TILED, block_n_tile=128),
+    "streamk": dict(variant=w8.W8A8_VARIANT_TILED, block_n_tile=128, split_k=2, grid_limit=5),
+    "pair": dict(variant=w8.W8A8_VARIANT_TILED_PAIR),
+    "swapab": dict(variant=w8.W8A8_VARIANT_SWAPAB),
+    "splitk": dict(variant=w8.W8A8_VARIANT_SPLITK, split_k=3),
+    "cluster": dict(variant=w8.W8A8_VARIANT_SPLITK_CLUSTER, split_k=3),
+    "smallm": dict(variant=w8.W8A8_VARIANT_SMALLM),
+    "generic": dict(variant=w8.W8A8_VARIANT_GENERIC),
+}
+
+
+@pytest.mark.parametrize("variant", list(CANARY_VARIANTS))
+@pytest.mark.parametrize("out", ["bf16", "fp32"])
+def test_no_store_past_c(variant, out):
+    """C is the head of a larger buffer whose tail holds a pattern: ragged M and N
+    tails (M not a multiple of any tile, N not a multiple of 128) must leave
+    every byte past C untouched."""
+    M = 13 if variant == "smallm" else 301
+    N, K = 200, 384
+    x = synth.make_inputs(M, N, K, seed=77)
+    ref = oracle.reference_c(x.A, x.a_s, x.B, x.b_s)
+    A, a_s, B, b_s = to_device(x)
+    dt = OUT_TORCH[out]
+    big = torch.full((M * N + 4096,), -7.0, dtype=dt, device="cuda")
+    C = big[:M * N].view(M, N)
+    w8.matmul(A, a_s, B, b_s, out_dtype=out, out=C, **CANARY_VARIANTS[variant])
+    torch.cuda.synchronize()
+    assert w8.w8a8_get_device_status()[0] == w8.W8A8_OK
+    assert torch.all(big[M * N:] == -7.0), f"{variant}: a store landed past C"
+    assert_close(C, ref, what=f"canary {variant} {out}")
+
+
+@pytest.mark.parametrize("opts", [dict(variant=w8.W8A8_VARIANT_SPLITK, split_k=4),
+                                  dict(variant=w8.W8A8_VARIANT_TILED, block_n_tile=128,
+                                       split_k=2, grid_limit=3)])
+def test_injected_workspace_failure(opts):
+    """Host-side fault injection: the library's workspace allocation reports
+    failure; the call returns W8A8_ERR_CUDA without launching, and the next call
+    (no injection) is right."""
+    M, N, K = 300, 512, 1024
+    x = synth.make_inputs(M, N, K, seed=78)
+    A, a_s, B, b_s = to_device(x)
+    C = torch.zeros((M, N), dtype=torch.float32, device="cuda")
+    o = w8.options(debug_fail_alloc=1, **opts)
+    st = w8.w8a8_block_fp8_matmul_ex(A, a_s, B, b_s, C, M, N, K, 128, 128, w8.W8A8_OUT_FP32,
+                                     torch.cuda.current_stream(), o)
+    assert st == w8.W8A8_ERR_CUDA
+    assert "injected" in w8.w8a8_last_error()
+    torch.cuda.synchronize()
+    assert w8.w8a8_get_device_status()[0] == w8.W8A8_OK
+    assert torch.count_nonzero(C) == 0                 # nothing ran
+    C2 = w8.matmul(A, a_s, B, b_s, out_dtype="fp32", **opts)
+    torch.cuda.synchronize()
+    assert_close(C2, oracle.reference_c(x.A, x.a_s, x.B, x.b_s), what="after injected failure")
