@@ -17,9 +17,10 @@
 // every run (the page's atomic_add version is not).
 //
 // Per CTA: warp 0 TMA producer (B block 128 x 128 B and the token tile
-// mma_n x 128 B per group), warp 1 MMA issuer (tcgen05.mma kind::f8f6f4,
-// M = 128, N = mma_n, 4 x K=32 per group) into one of two TMEM buffers,
-// 1 or 2 promotion warpgroups: thread = weight row n, columns = tokens.
+// mma_n x 128 B per group), lane 0 of warps 1-3 MMA issuers (tcgen05.mma
+// kind::f8f6f4, M = 128, N = mma_n, 4 x K=32 per group; the K groups dealt out
+// round robin, each into its own TMEM accumulator), 1 or 2 promotion
+// warpgroups: thread = weight row n, columns = tokens.
 // Unsplit tiles leave through shared memory and one TMA store; split tiles
 // through the workspace and a vectorised ordered reduction.
 #include "kernels.cuh"
@@ -41,8 +42,15 @@ template <int MT> struct SwapLayout {
     static constexpr int kMinBlocks = MT <= 64 ? 2 : 1;
     static constexpr uint32_t kWBytes = 128u * 128u;
     static constexpr uint32_t kXBytes = static_cast<uint32_t>(MT) * 128u;
-    static constexpr uint32_t kTmemCols = 2 * MT < 32 ? 32 : 2 * MT;
-    static constexpr int kBars = 2 * kMaxStages + 6;
+    // TMEM accumulators, one per K group in flight: with 8 (4) of them a short
+    // K loop of 32-column (64-column) tiles never waits for a promotion.  At
+    // most two CTAs are resident per SM (registers), so 2 x 256 columns fit.
+    static constexpr int kBufs = MT <= 32 ? 8 : (MT <= 64 ? 4 : 2);
+    static constexpr uint32_t kTmemCols = kBufs * MT < 32 ? 32 : kBufs * MT;
+    static constexpr int kMaxIssuers = 3;
+    // full/empty per stage, tfull/tempty per TMEM buffer, one drain barrier
+    // per MMA issuer, the cluster receive barrier
+    static constexpr int kBars = 2 * kMaxStages + 2 * kBufs + kMaxIssuers + 1;
     // Operand stages; after the main loop the same bytes hold the C tile.
     // Fused activation quantisation adds, per stage, the unquantised token
     // tile as the TMA brings it: MT rows of 128 elements of x_esize bytes.
@@ -87,6 +95,23 @@ __device__ __forceinline__ void store4(void *C, size_t idx, float4 v, int out_ki
         }
         *reinterpret_cast<uint2 *>(static_cast<uint16_t *>(C) + idx) = u;
     }
+}
+
+// Number of threads that issue the MMAs of a CTA's `ng` K groups (group i goes
+// to issuer i mod n).  Each issuer's loop is a chain of latencies (barrier
+// probe, fence, 4 x tcgen05.mma, 2 commits: ~700 cycles a group, of which the
+// tensor core needs ~200 at MMA N <= 64), so several issuers in different
+// warps overlap them.  An mbarrier wait by parity cannot tell phase k from
+// phase k + 2, so every barrier that is waited for more than once (a stage
+// reused after `stages` groups, a TMEM buffer reused after `bufs` groups)
+// must be waited for by one thread only: n must divide the number of stages
+// (buffers), or there must be no reuse at all.
+__device__ __forceinline__ int mma_issuers(int ng, int stages, int bufs, int max_issuers)
+{
+    for (int n = max_issuers; n > 1; --n)
+        if ((ng <= stages || stages % n == 0) && (ng <= bufs || bufs % n == 0))
+            return n;
+    return 1;
 }
 
 __device__ __forceinline__ void add4(float4 &a, const float4 &b)
@@ -190,9 +215,9 @@ __global__ void __launch_bounds__(SwapLayout<MT>::kThreads, SwapLayout<MT>::kMin
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
     auto empty_bar = [&](int s) { return bar0 + 8u * (kMaxStages + s); };
     auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * kMaxStages + b); };
-    auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * kMaxStages + 2 + b); };
-    const uint32_t drain_bar = bar0 + 8u * (2 * kMaxStages + 4);
-    const uint32_t recv_bar = bar0 + 8u * (2 * kMaxStages + 5);   // cluster split-K
+    auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * kMaxStages + L::kBufs + b); };
+    auto drain_bar = [&](int w) { return bar0 + 8u * (2 * kMaxStages + 2 * L::kBufs + w); };
+    const uint32_t recv_bar = bar0 + 8u * (2 * kMaxStages + 2 * L::kBufs + L::kMaxIssuers);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + L::kBars);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     volatile int *last_flag = reinterpret_cast<volatile int *>(tmem_slot + 2);
@@ -222,11 +247,12 @@ __global__ void __launch_bounds__(SwapLayout<MT>::kThreads, SwapLayout<MT>::kMin
             mbar_init(full_bar(s), 1);
             mbar_init(empty_bar(s), 1);
         }
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < L::kBufs; ++b) {
             mbar_init(tfull_bar(b), 1);
             mbar_init(tempty_bar(b), 4 * L::kPromoWG);
         }
-        mbar_init(drain_bar, 1);
+        for (int w = 0; w < L::kMaxIssuers; ++w)
+            mbar_init(drain_bar(w), 1);
         if (p.cluster_reduce)
             mbar_init(recv_bar, 1);
         if constexpr (FUSED)
@@ -366,16 +392,22 @@ __global__ void __launch_bounds__(SwapLayout<MT>::kThreads, SwapLayout<MT>::kMin
                                p.wait_limit, (SITE_DRAIN << 8) | 4u);
                 }
             }
-        } else if (warp == 1 && lane == 0) {
-            // ---------------------------------------------------------- MMA issuer
+        } else if (lane == 0 && (warp == 1 || (!FUSED && warp <= static_cast<uint32_t>(L::kMaxIssuers)))) {
+            // ---------------------------------------------------------- MMA issuers
+            // Lane 0 of warps 1.. (warps 2 and 3 quantise in the fused kernel,
+            // which keeps one issuer); issuer w takes groups w, w + n, ...
+            const int n_iss = FUSED ? 1 : mma_issuers(ng, stages, L::kBufs, L::kMaxIssuers);
+            const int w = static_cast<int>(warp) - 1;
             const uint32_t idesc = idesc_e4m3_f32(128, static_cast<uint32_t>(p.mma_n));
-            int stage = 0;
-            uint32_t phase = 0;
             bool ok = true;
-            for (int i = 0; i < ng; ++i) {
-                const uint32_t buf = i & 1;
-                const uint32_t bphase = (i >> 1) & 1;
-                if (!wait_bounded(tempty_bar(buf), bphase ^ 1u, guard, SITE_SWAP_MMA_TMEM) ||
+            for (int i = w; w < n_iss && i < ng; i += n_iss) {
+                const int stage = i % stages;
+                const uint32_t phase = (i / stages) & 1;
+                const uint32_t buf = i % L::kBufs;
+                const uint32_t bphase = (i / L::kBufs) & 1;
+                // a buffer's first use needs no wait
+                if ((i >= L::kBufs &&
+                     !wait_bounded(tempty_bar(buf), bphase ^ 1u, guard, SITE_SWAP_MMA_TMEM)) ||
                     !wait_bounded(full_bar(stage), phase, guard, SITE_SWAP_MMA_FULL) ||
                     (FUSED && !wait_bounded(ready_bar(i), 0, guard, SITE_SWAP_QUANT))) {
                     ok = false;
@@ -390,14 +422,12 @@ __global__ void __launch_bounds__(SwapLayout<MT>::kThreads, SwapLayout<MT>::kMin
                     mma_e4m3(d, ad + 2u * kk, bd + 2u * kk, idesc, kk > 0 ? 1u : 0u);
                 mma_commit(empty_bar(stage));
                 mma_commit(tfull_bar(buf));
-                if (++stage == stages) {
-                    stage = 0;
-                    phase ^= 1u;
-                }
             }
-            if (!ok) {
-                mma_commit(drain_bar);
-                wait_drain(drain_bar, 0, p.status, p.wait_limit, (SITE_DRAIN << 8) | 4u);
+            if (!ok || *abort_flag) {
+                // an aborting CTA frees its tensor memory only after every
+                // issuer's MMAs have completed
+                mma_commit(drain_bar(w));
+                wait_drain(drain_bar(w), 0, p.status, p.wait_limit, (SITE_DRAIN << 8) | 4u);
             }
         } else if (FUSED && warp >= 2) {
             // ---------------------------------------------------------- activation quantiser
@@ -487,8 +517,8 @@ __global__ void __launch_bounds__(SwapLayout<MT>::kThreads, SwapLayout<MT>::kMin
             acc[j] = 0.f;
         bool ok = true;
         for (int i = 0; i < ng; ++i) {
-            const uint32_t buf = i & 1;
-            const uint32_t bphase = (i >> 1) & 1;
+            const uint32_t buf = i % L::kBufs;
+            const uint32_t bphase = (i / L::kBufs) & 1;
             // All lanes wait (the whole warp sleeps in the barrier probe); the
             // warp proceeds only if every lane saw the buffer (tcgen05.ld below
             // is a warp-wide instruction).
