@@ -103,16 +103,16 @@ def source_digest(kernel: str = "matmul") -> str:
 # figure whose kernel sources have changed since is not reported (the key no
 # longer matches).
 MEASURED_TRAFFIC = {
-    # profiles/k_swapab_decode_m214.md: read 1.171 MB, write 0 (C stays in L2 within the launch)
-    ("1c0dd9e8f7cf2385", "214x4096x256", 2): 1170944,
-    # profiles/k_tiled_prefill_16384x4096x4096.md: read 95.58 MB + write 98.63 MB
-    ("1c0dd9e8f7cf2385", "16384x4096x4096", 2): 194210816,
-    # profiles/k_tiled_streamk_prefill_16384x1536x4096.md: read 76.29 MB + write 37.55 MB
-    ("1c0dd9e8f7cf2385", "16384x1536x4096", 2): 113841920,
-    # profiles/k_quant_group128_16384x4096_bf16.md: read 134.26 MB + write 37.87 MB
-    ("aa9beb2168bda2f2", "quant_16384x4096", 1): 172132608,
-    # profiles/k_swapab_grouped_moe_decode_256x1536x4096.md: read 1.645 GB + write 26.00 MB
-    ("1c0dd9e8f7cf2385", "grouped_decode_masked", 2): 1671167488,
+    # profiles/k_swapab_decode_m214.md: read 1.172 MB, write 0 (C stays in L2 within the launch)
+    ("210f62729635e540", "214x4096x256", 2): 1172224,
+    # profiles/k_tiled_prefill_16384x4096x4096.md: read 95.47 MB + write 98.86 MB
+    ("210f62729635e540", "16384x4096x4096", 2): 194323968,
+    # profiles/k_tiled_streamk_prefill_16384x1536x4096.md: read 76.31 MB + write 37.35 MB
+    ("210f62729635e540", "16384x1536x4096", 2): 113659648,
+    # profiles/k_quant_group128_16384x4096_bf16.md: read 134.26 MB + write 38.18 MB
+    ("aa9beb2168bda2f2", "quant_16384x4096", 1): 172443648,
+    # profiles/k_swapab_grouped_moe_decode_256x1536x4096.md: read 1.645 GB + write 26.09 MB
+    ("210f62729635e540", "grouped_decode_masked", 2): 1671250944,
 }
 
 
