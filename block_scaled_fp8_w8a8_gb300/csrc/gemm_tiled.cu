@@ -8,9 +8,11 @@
 // that concurrently running tiles share A and B panels in L2).  Per CTA:
 //   warp 0      TMA producer: one 128-wide K group of A (128 x 128 B) and of
 //               B (BN x 128 B) per shared-memory stage, 128-byte swizzled.
-//   warp 1      MMA issuer: 4 x tcgen05.mma kind::f8f6f4 (K = 32 each) turn
-//               one stage into the group's fp32 partial P_g in a TMEM buffer;
-//               commits free the stage and publish the buffer.
+//   warps 1, 3  MMA issuers (lane 0; warp 3 only for BN = 128 with an even
+//               stage count, taking every other group): 4 x tcgen05.mma
+//               kind::f8f6f4 (K = 32 each) turn one stage into the group's
+//               fp32 partial P_g in a TMEM buffer; commits free the stage and
+//               publish the buffer.
 //   warp 2      scale loader: cp.async gathers of a_s[m0..m0+127, g] and of the
 //               tile's b_s[., g] into a ring of shared-memory slots, so that
 //               the promotion never waits on global memory.
@@ -35,6 +37,18 @@ namespace w8a8 {
 namespace {
 
 constexpr int kGroupRaster = 16;   // M tiles per raster group
+
+// MMA issuer threads.  One thread's loop per K group (barrier probes, four
+// MMAs, two commits) keeps the tensor core busy when each MMA is long
+// (N = 192, 256); at N = 128 a second issuer taking every other group overlaps
+// the loop's latencies (K = 4096: 12 % faster; measured 2-4 % slower at
+// N = 192 with short K).  Every stage and TMEM buffer (512 / BN of them) must
+// be waited for by one thread in phase order, since a parity wait cannot tell
+// phase k from k + 2: two issuers need even stage and buffer counts.
+template <int BN, int STAGES> __host__ __device__ constexpr uint32_t kTiledIssuers()
+{
+    return (BN == 128 && STAGES % 2 == 0 && (512 / BN) % 2 == 0) ? 2u : 1u;
+}
 constexpr int kScaleSlots = 8;     // depth of the scale ring
 constexpr int kSlotFloats = 144;   // 128 a_s values + up to 2 b_s values, padded
 
@@ -199,7 +213,7 @@ template <int BN, int STAGES, int CPW, int EB> struct TiledLayout {
     static constexpr int kRegsLow = 56;
     static constexpr int kRegsHigh = kThreads == 384 ? 224 : 152;
     static constexpr size_t kScaleBytes = kScaleSlots * kSlotFloats * 4;
-    static constexpr int kBars = 2 * STAGES + 2 * kBufs + 2 * kScaleSlots + 1;
+    static constexpr int kBars = 2 * STAGES + 2 * kBufs + 2 * kScaleSlots + 2;
     static constexpr size_t kSmem =
         1024 + kStageBytes + kEpiBytes + kScaleBytes + kBars * 8 + 16;
 };
@@ -228,7 +242,7 @@ __global__ void __launch_bounds__(TiledLayout<BN, STAGES, CPW, EB>::kThreads, 1)
     auto sempty_bar = [&](int q) {
         return bar0 + 8u * (2 * STAGES + 2 * L::kBufs + kScaleSlots + q);
     };
-    const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 2 * L::kBufs + 2 * kScaleSlots);
+    auto drain_bar = [&](int w) { return bar0 + 8u * (2 * STAGES + 2 * L::kBufs + 2 * kScaleSlots + w); };
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + L::kBars);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     volatile int *last_flag = reinterpret_cast<volatile int *>(tmem_slot + 2);   // stream-K
@@ -248,7 +262,8 @@ __global__ void __launch_bounds__(TiledLayout<BN, STAGES, CPW, EB>::kThreads, 1)
             mbar_init(sfull_bar(q), 32);                 // one cp.async arrival per loader lane
             mbar_init(sempty_bar(q), 4 * L::kPromoWG);
         }
-        mbar_init(drain_bar, 1);
+        mbar_init(drain_bar(0), 1);
+        mbar_init(drain_bar(1), 1);
         *abort_flag = 0;
         mbar_fence_init();
     }
@@ -333,8 +348,12 @@ __global__ void __launch_bounds__(TiledLayout<BN, STAGES, CPW, EB>::kThreads, 1)
                                p.wait_limit, (SITE_DRAIN << 8) | 4u);
                 }
             }
-        } else if (warp == 1 && lane == 0) {
-            // ---------------------------------------------------------- MMA issuer
+        } else if ((warp == 1 || (warp == 3 && kTiledIssuers<BN, STAGES>() == 2)) && lane == 0) {
+            // ---------------------------------------------------------- MMA issuers
+            // Lane 0 of warps 1 and 3 take alternate K groups (both walk the
+            // same work list) where kTiledIssuers says so.
+            constexpr uint32_t n_iss = kTiledIssuers<BN, STAGES>();
+            const uint32_t w = warp == 1 ? 0u : 1u;
             constexpr uint32_t idesc = idesc_e4m3_f32(128, BN);
             int stage = 0;
             uint32_t phase = 0;
@@ -344,22 +363,24 @@ __global__ void __launch_bounds__(TiledLayout<BN, STAGES, CPW, EB>::kThreads, 1)
             int t, g0, g1;
             while (ok && walk.next(t, g0, g1)) {
                 for (int g = g0; g < g1; ++g) {
-                    const uint32_t buf = it % L::kBufs;
-                    const uint32_t bphase = (it / L::kBufs) & 1u;
-                    if (!wait_bounded(tempty_bar(buf), bphase ^ 1u, guard, SITE_TILED_MMA_TMEM) ||
-                        !wait_bounded(full_bar(stage), phase, guard, SITE_TILED_MMA_FULL)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after_sync();
-                    const uint32_t d = tmem_base + buf * BN;
-                    const uint64_t ad = sw128_kmajor_desc(sA + stage * L::kABytes);
-                    const uint64_t bd = sw128_kmajor_desc(sB + stage * L::kBBytes);
+                    if (it % n_iss == w) {
+                        const uint32_t buf = it % L::kBufs;
+                        const uint32_t bphase = (it / L::kBufs) & 1u;
+                        if (!wait_bounded(tempty_bar(buf), bphase ^ 1u, guard, SITE_TILED_MMA_TMEM) ||
+                            !wait_bounded(full_bar(stage), phase, guard, SITE_TILED_MMA_FULL)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after_sync();
+                        const uint32_t d = tmem_base + buf * BN;
+                        const uint64_t ad = sw128_kmajor_desc(sA + stage * L::kABytes);
+                        const uint64_t bd = sw128_kmajor_desc(sB + stage * L::kBBytes);
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        mma_e4m3(d, ad + 2u * kk, bd + 2u * kk, idesc, kk > 0 ? 1u : 0u);
-                    mma_commit(empty_bar(stage));
-                    mma_commit(tfull_bar(buf));
+                        for (int kk = 0; kk < 4; ++kk)
+                            mma_e4m3(d, ad + 2u * kk, bd + 2u * kk, idesc, kk > 0 ? 1u : 0u);
+                        mma_commit(empty_bar(stage));
+                        mma_commit(tfull_bar(buf));
+                    }
                     ++it;
                     if (++stage == STAGES) {
                         stage = 0;
@@ -367,9 +388,11 @@ __global__ void __launch_bounds__(TiledLayout<BN, STAGES, CPW, EB>::kThreads, 1)
                     }
                 }
             }
-            if (!ok) {
-                mma_commit(drain_bar);
-                wait_drain(drain_bar, 0, p.status, p.wait_limit, (SITE_DRAIN << 8) | 4u);
+            if (!ok || *abort_flag) {
+                // an aborting CTA frees its tensor memory only after both
+                // issuers' MMAs have completed
+                mma_commit(drain_bar(w));
+                wait_drain(drain_bar(w), 0, p.status, p.wait_limit, (SITE_DRAIN << 8) | 4u);
             }
         } else if (warp == 2) {
             // ---------------------------------------------------------- scale loader

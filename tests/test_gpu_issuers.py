@@ -144,3 +144,25 @@ def test_fused_long_k_equals_quantise_then_matmul(mt, stages):
     torch.cuda.synchronize()
     assert w8.w8a8_get_device_status()[0] == w8.W8A8_OK
     assert torch.equal(got.view(torch.int16), want.view(torch.int16))
+
+
+# The tiled kernel: lane 0 of warps 1 and 3 take alternate K groups at
+# BN = 128 (4 TMEM buffers) with an even stage count, one issuer otherwise.
+TILED = [(bn, stages, split) for bn, stages in ((256, 4), (256, 3), (192, 4), (128, 6), (128, 5), (128, 4))
+         for split in (1, 2)]
+
+
+@pytest.mark.parametrize("bn,stages,split", TILED)
+def test_tiled_issuers_match_oracle(bn, stages, split):
+    """Whole tiles (split 1) and stream-K ranges that start and end inside a
+    tile (split 2 on a grid of 5 CTAs): both issuers walk the same list."""
+    M, K = 300, 1280                # 3 row tiles, 10 K groups
+    opts = dict(variant=w8.W8A8_VARIANT_TILED, block_n_tile=bn, stages=stages)
+    if split > 1:
+        opts.update(split_k=split, grid_limit=5)
+    if planned(M, K, **opts) is None:
+        pytest.skip("configuration not schedulable")
+    x, ref = case(M, K)
+    c1, c2 = run_twice(x, **opts)
+    assert_close(c1, ref, what=f"tiled bn={bn} stages={stages} split={split}")
+    assert torch.equal(c1.view(torch.int16), c2.view(torch.int16))
