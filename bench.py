@@ -81,8 +81,8 @@ def parse():
 # measured dispatch table).
 KERNEL_SOURCES = {
     "matmul": ("api.cu", "gemm_swapab.cu", "gemm_tiled.cu", "gemm_pair.cu", "epilogue.cuh",
-               "kernels.cuh", "ptx.cuh", "dispatch_table.h", "tuning_table.inc"),
-    "quant": ("quant.cu", "kernels.cuh", "ptx.cuh"),
+               "kernels.cuh", "ptx.cuh", "quant_math.cuh", "dispatch_table.h", "tuning_table.inc"),
+    "quant": ("quant.cu", "quant_math.cuh", "kernels.cuh", "ptx.cuh"),
 }
 
 

@@ -122,11 +122,25 @@ __device__ __forceinline__ uint4 encode16(const uint32_t *w, float s)
 template <int KIND>
 __device__ __forceinline__ float amax16(const uint32_t *w)
 {
-    float m = 0.f;
+    if constexpr (KIND == W8A8_IN_BF16) {
+        // Two bf16 lanes at a time: |x| by clearing the sign bits, then
+        // max.bf16x2, which like fmaxf returns the other operand when one is
+        // NaN and keeps subnormals; the maximum of bf16 values is one of them,
+        // so it is exact and equals the fp32 maximum below.
+        uint32_t m2 = 0u;
 #pragma unroll
-    for (int i = 0; i < 16; ++i)
-        m = fmaxf(m, fabsf(element<KIND>(w, i)));
-    return m;
+        for (int i = 0; i < 8; ++i) {
+            const uint32_t a = w[i] & 0x7fff7fffu;
+            asm("max.bf16x2 %0, %1, %2;" : "=r"(m2) : "r"(m2), "r"(a));
+        }
+        return fmaxf(0.f, fmaxf(__uint_as_float(m2 << 16), __uint_as_float(m2 & 0xffff0000u)));
+    } else {
+        float m = 0.f;
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+            m = fmaxf(m, fabsf(element<KIND>(w, i)));
+        return m;
+    }
 }
 
 }  // namespace quant

@@ -77,6 +77,26 @@ def test_quant_special_values():
     assert a_s[3, 3] == 1.0
 
 
+
+def test_quant_special_values_bf16():
+    """bf16 input: subnormal groups (bf16 has fp32's exponent range), -0, zero
+    groups, huge groups, a group of the smallest subnormal, and a group whose
+    max / 448 underflows."""
+    K = 768
+    X = torch.zeros(6, K, dtype=torch.float32)
+    X[1] = -0.0
+    X[2, 0:128] = torch.linspace(-1e-39, 1e-39, 128, dtype=torch.float64).float()
+    X[2, 128:256] = torch.linspace(-3e38, 3e38, 128, dtype=torch.float64).float()
+    X[2, 256:384] = torch.linspace(-1e-44, 1e-44, 128, dtype=torch.float64).float()
+    X[2, 384:512] = 2.0 ** -133                     # the smallest bf16 subnormal
+    X[2, 512:640] = -(2.0 ** -127)                  # a negative bf16 subnormal group
+    X[3:] = synth.activations(3, K, seed=12, outlier_p=0.05)
+    X[4, 0:128] = 0.0
+    Xb = X.to(torch.bfloat16)
+    A, a_s = _gpu_quant(Xb)
+    _assert_same(Xb, A, a_s, "bf16 special values")
+    assert (A[1] == 0x80).all()
+
 def _e4m3_midpoints():
     pos = [2.0 ** -9 * m for m in range(8)]
     pos += [2.0 ** e * (1 + m / 8) for e in range(-6, 9) for m in range(8)]
