@@ -104,15 +104,15 @@ def source_digest(kernel: str = "matmul") -> str:
 # longer matches).
 MEASURED_TRAFFIC = {
     # profiles/k_swapab_decode_m214.md: read 1.172 MB, write 0 (C stays in L2 within the launch)
-    ("923475950a6c7f0f", "214x4096x256", 2): 1172224,
-    # profiles/k_tiled_prefill_16384x4096x4096.md: read 97.15 MB + write 98.80 MB
-    ("923475950a6c7f0f", "16384x4096x4096", 2): 195958272,
-    # profiles/k_tiled_streamk_prefill_16384x1536x4096.md: read 75.96 MB + write 36.69 MB
-    ("923475950a6c7f0f", "16384x1536x4096", 2): 112642560,
-    # profiles/k_quant_group128_16384x4096_bf16.md: read 134.26 MB + write 37.88 MB
-    ("aa9beb2168bda2f2", "quant_16384x4096", 1): 172138752,
-    # profiles/k_swapab_grouped_moe_decode_256x1536x4096.md: read 1.645 GB + write 25.94 MB
-    ("923475950a6c7f0f", "grouped_decode_masked", 2): 1671069440,
+    ("bb42aa12ef0e5862", "214x4096x256", 2): 1172224,
+    # profiles/k_tiled_prefill_16384x4096x4096.md: read 97.22 MB + write 99.23 MB
+    ("bb42aa12ef0e5862", "16384x4096x4096", 2): 196444160,
+    # profiles/k_tiled_streamk_prefill_16384x1536x4096.md: read 75.98 MB + write 37.13 MB
+    ("bb42aa12ef0e5862", "16384x1536x4096", 2): 113114112,
+    # profiles/k_quant_group128_16384x4096_bf16.md: read 134.26 MB + write 37.81 MB
+    ("f06c1eccb5386d7c", "quant_16384x4096", 1): 172076288,
+    # profiles/k_swapab_grouped_moe_decode_256x1536x4096.md: read 1.645 GB + write 26.04 MB
+    ("bb42aa12ef0e5862", "grouped_decode_masked", 2): 1671146496,
 }
 
 
