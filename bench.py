@@ -86,15 +86,45 @@ KERNEL_SOURCES = {
 }
 
 
-def source_digest(kernel: str = "matmul") -> str:
-    """sha256 over the CUDA sources of one kernel family (first 16 hex digits):
-    identifies the build that a recorded ncu traffic figure belongs to."""
+def strip_comments(text: str) -> str:
+    """C/C++ source without its comments and trailing spaces (string and
+    character literals kept), so that editing a comment does not change the
+    code's digest."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            while i < n and text[i] != "\n":
+                i += 1
+        elif text.startswith("/*", i):
+            end = text.find("*/", i + 2)
+            i = n if end < 0 else end + 2
+        else:
+            out.append(c)
+            i += 1
+    return "\n".join(line.rstrip() for line in "".join(out).splitlines() if line.strip())
+
+
+def source_digest(kernel: str = "matmul", read=None) -> str:
+    """sha256 over the CUDA sources of one kernel family with their comments
+    removed (first 16 hex digits): identifies the code that a recorded ncu
+    traffic figure belongs to.  `read(name)` may supply a file's text (e.g.
+    from an earlier commit); by default the files in the tree are read."""
     import hashlib
     csrc = os.path.join(ROOT, "block_scaled_fp8_w8a8_gb300", "csrc")
+    if read is None:
+        def read(name):
+            with open(os.path.join(csrc, name), encoding="utf-8") as f:
+                return f.read()
     h = hashlib.sha256()
     for name in sorted(KERNEL_SOURCES[kernel]):
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(name.encode() + b"\0" + f.read())
+        h.update(name.encode() + b"\0" + strip_comments(read(name)).encode())
     return h.hexdigest()[:16]
 
 
@@ -104,15 +134,15 @@ def source_digest(kernel: str = "matmul") -> str:
 # longer matches).
 MEASURED_TRAFFIC = {
     # profiles/k_swapab_decode_m214.md: read 1.172 MB, write 0 (C stays in L2 within the launch)
-    ("bb42aa12ef0e5862", "214x4096x256", 2): 1172224,
+    ("b9bc2d79c288420d", "214x4096x256", 2): 1172224,
     # profiles/k_tiled_prefill_16384x4096x4096.md: read 97.22 MB + write 99.23 MB
-    ("bb42aa12ef0e5862", "16384x4096x4096", 2): 196444160,
+    ("b9bc2d79c288420d", "16384x4096x4096", 2): 196444160,
     # profiles/k_tiled_streamk_prefill_16384x1536x4096.md: read 75.98 MB + write 37.13 MB
-    ("bb42aa12ef0e5862", "16384x1536x4096", 2): 113114112,
+    ("b9bc2d79c288420d", "16384x1536x4096", 2): 113114112,
     # profiles/k_quant_group128_16384x4096_bf16.md: read 134.26 MB + write 37.81 MB
-    ("f06c1eccb5386d7c", "quant_16384x4096", 1): 172076288,
+    ("a53393be13d52129", "quant_16384x4096", 1): 172076288,
     # profiles/k_swapab_grouped_moe_decode_256x1536x4096.md: read 1.645 GB + write 26.04 MB
-    ("bb42aa12ef0e5862", "grouped_decode_masked", 2): 1671146496,
+    ("b9bc2d79c288420d", "grouped_decode_masked", 2): 1671146496,
 }
 
 

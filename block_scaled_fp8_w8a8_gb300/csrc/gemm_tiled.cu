@@ -484,8 +484,8 @@ __global__ void __launch_bounds__(TiledLayout<BN, STAGES, CPW, EB>::kThreads, 1)
                 }
                 tc_fence_after_sync();
                 const uint32_t taddr = tmem_base + ((q * 32u) << 16) + buf * BN + h * CPW;
-                // 64-column loads: TMEM load round trips, not FMA issue, bound
-                // this loop, so fewer and larger loads are faster.
+                // 64-column loads (fewer, larger loads measured faster than
+                // 32-column ones); the group's time is its sync and FMA chain.
 #pragma unroll
                 for (int c = 0; c < CPW / 64; ++c) {
                     uint32_t v[64];
