@@ -25,6 +25,7 @@ from ._binding import (  # noqa: F401
     w8a8_quantize_fp8_per_token_group, W8A8_IN_BF16, W8A8_IN_FP16, W8A8_IN_FP32,
     w8a8_block_fp8_grouped_matmul_masked, w8a8_block_fp8_grouped_matmul_contiguous,
     w8a8_launch_floor_kernel, w8a8_block_fp8_quant_matmul,
+    w8a8_block_fp8_quant_matmul_workspace_size,
     w8a8_get_device_status, w8a8_last_error, w8a8_options, w8a8_shutdown, w8a8_status_string,
 )
 
@@ -150,9 +151,11 @@ def grouped_matmul_contiguous(A, a_s, B, b_s, m_indices, out_dtype="bf16", out=N
 
 
 def quant_matmul(X, B, b_s, out_dtype="bf16", out=None, stream=None, **opts):
-    """C = matmul(quantize_fp8_per_token_group(X), B) in one launch, on CUDA
-    tensors: X [M, K] bf16/fp16/fp32, B uint8/float8_e4m3fn [N, K], b_s float32
-    [ceil(N/128), K/128].  Same bits as the two calls in sequence."""
+    """C = matmul(quantize_fp8_per_token_group(X), B) on CUDA tensors: X [M, K]
+    bf16/fp16/fp32, B uint8/float8_e4m3fn [N, K], b_s float32 [ceil(N/128),
+    K/128].  One fused launch for decode sizes, the quantiser then the matmul
+    above them (see w8a8_block_fp8_quant_matmul).  Same bits as the two calls
+    in sequence."""
     import torch
     M, K = X.shape
     N = B.shape[0]

@@ -41,6 +41,7 @@ EXPORTED = (
     "w8a8_launch_floor_kernel",
     "w8a8_block_fp8_quant_matmul",
     "w8a8_block_fp8_host_staging_size",
+    "w8a8_block_fp8_quant_matmul_workspace_size",
     "w8a8_block_fp8_workspace_size",
     "w8a8_block_fp8_plan",
     "w8a8_get_device_status",
@@ -63,7 +64,8 @@ class w8a8_options(ctypes.Structure):
         ("debug_skip_load", ctypes.c_int),
         ("weights_static", ctypes.c_int),
         ("debug_fail_alloc", ctypes.c_int),
-        ("reserved_i", ctypes.c_int * 2),
+        ("splitk_atomic", ctypes.c_int),
+        ("reserved_i", ctypes.c_int),
         ("workspace_dev", ctypes.c_void_p),
         ("workspace_bytes", ctypes.c_size_t),
         ("wait_limit_cycles", ctypes.c_ulonglong),
@@ -121,6 +123,8 @@ def load_library():
     lib.w8a8_quantize_fp8_per_token_group.restype = ctypes.c_int
     lib.w8a8_block_fp8_host_staging_size.argtypes = [i64, i64, i64, i32]
     lib.w8a8_block_fp8_host_staging_size.restype = sz
+    lib.w8a8_block_fp8_quant_matmul_workspace_size.argtypes = [i64, i64, i64, i32, opt_p]
+    lib.w8a8_block_fp8_quant_matmul_workspace_size.restype = sz
     lib.w8a8_block_fp8_workspace_size.argtypes = [i64, i64, i64, opt_p]
     lib.w8a8_block_fp8_workspace_size.restype = sz
     lib.w8a8_block_fp8_plan.argtypes = [i64, i64, i64, i32, opt_p, opt_p]
@@ -248,6 +252,11 @@ def w8a8_quantize_fp8_per_token_group(X, x_dtype, A, a_s, M, K, group_size=128,
 
 def w8a8_block_fp8_host_staging_size(M, N, K, out_dtype=W8A8_OUT_BF16) -> int:
     return load_library().w8a8_block_fp8_host_staging_size(M, N, K, out_dtype)
+
+
+def w8a8_block_fp8_quant_matmul_workspace_size(M, N, K, out_dtype=W8A8_OUT_BF16, opts=None) -> int:
+    return load_library().w8a8_block_fp8_quant_matmul_workspace_size(M, N, K, out_dtype,
+                                                                    _opts(opts))
 
 
 def w8a8_block_fp8_workspace_size(M, N, K, opts=None) -> int:

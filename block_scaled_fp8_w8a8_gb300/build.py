@@ -18,7 +18,7 @@ LIB_NAME = "libw8a8_gb300.so"
 UNITS = ["api.cu", "status.cu", "gemm_tiled.cu", "gemm_swapab.cu", "noalloc.cu", "quant.cu", "hostio.cu",
          "gemm_smallm.cu", "gemm_pair.cu", "gemm_generic.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-HEADERS = ["ptx.cuh", "kernels.cuh", "epilogue.cuh", "dispatch_table.h", "tuning_table.inc"]
+HEADERS = ["ptx.cuh", "kernels.cuh", "epilogue.cuh", "promote.cuh", "dispatch_table.h", "tuning_table.inc"]
 
 
 def nvcc() -> str:

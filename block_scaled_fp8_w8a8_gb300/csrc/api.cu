@@ -60,7 +60,8 @@ std::mutex g_mutex;
 DeviceInfo g_devices[kMaxDevices];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
-// Per-(device, stream) split-K workspace owned by the library.
+// Per-(device, stream) split-K workspace owned by the library, allocated and
+// grown stream-ordered (cudaMallocAsync / cudaFreeAsync on that stream).
 struct Workspace {
     void *ptr = nullptr;
     size_t bytes = 0;
@@ -116,6 +117,65 @@ w8a8_status current_device(int *dev_out, DeviceInfo *info_out)
     return W8A8_OK;
 }
 
+// Encoded tensor maps, cached per host thread by everything that goes into
+// them (base address, element type, rank, sizes, strides, box, swizzle, L2
+// promotion): a map depends on nothing else, so a hit is always the map the
+// driver would encode.  Repeated calls on the same buffers (a decode loop, a
+// benchmark's rotating sets) then skip the driver call.  Direct-mapped by a
+// hash of the key; a collision only costs an encode.
+struct MapKey {
+    const void *base;
+    int dtype, rank, swizzle, promo;
+    cuuint64_t dims[3], strides[2];
+    cuuint32_t box[3];
+};
+constexpr int kMapCacheEntries = 128;
+struct MapCache {
+    MapKey key[kMapCacheEntries];
+    CUtensorMap map[kMapCacheEntries];
+    bool valid[kMapCacheEntries] = {};
+};
+thread_local MapCache g_map_cache;
+
+CUresult encode_cached(CUtensorMap *map, CUtensorMapDataType dt, cuuint32_t rank, void *base,
+                       const cuuint64_t *dims, const cuuint64_t *strides, const cuuint32_t *box,
+                       CUtensorMapSwizzle swizzle, CUtensorMapL2promotion promo)
+{
+    MapKey k;
+    std::memset(&k, 0, sizeof(k));      // padding too: keys are compared bytewise
+    k.base = base;
+    k.dtype = static_cast<int>(dt);
+    k.rank = static_cast<int>(rank);
+    k.swizzle = static_cast<int>(swizzle);
+    k.promo = static_cast<int>(promo);
+    for (cuuint32_t i = 0; i < rank; ++i) {
+        k.dims[i] = dims[i];
+        k.box[i] = box[i];
+        if (i + 1 < rank)
+            k.strides[i] = strides[i];
+    }
+    uint64_t h = 1469598103934665603ull;             // FNV-1a over the key's bytes
+    const unsigned char *b = reinterpret_cast<const unsigned char *>(&k);
+    for (size_t i = 0; i < sizeof(k); ++i)
+        h = (h ^ b[i]) * 1099511628211ull;
+    const int slot = static_cast<int>(h % kMapCacheEntries);
+    MapCache &c = g_map_cache;
+    if (c.valid[slot] && std::memcmp(&c.key[slot], &k, sizeof(k)) == 0) {
+        *map = c.map[slot];
+        return CUDA_SUCCESS;
+    }
+    const cuuint32_t elem[3] = {1u, 1u, 1u};
+    const CUresult r = g_encode(map, dt, rank, base, dims, strides, box, elem,
+                                CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, promo,
+                                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r == CUDA_SUCCESS) {
+        c.key[slot] = k;
+        c.map[slot] = *map;
+        c.valid[slot] = true;
+    }
+    return r;
+}
+
 // 2-D uint8 tensor map over a row-major [rows, cols] matrix; boxes of
 // 128 columns (one K group, 128 bytes) by box_rows rows, 128-byte swizzle,
 // out-of-range elements read as zero.
@@ -131,11 +191,9 @@ w8a8_status encode_u8_map(CUtensorMap *map, const void *base, int64_t rows, int6
                           static_cast<cuuint64_t>(slabs)};
     cuuint64_t strides[2] = {static_cast<cuuint64_t>(pitch), static_cast<cuuint64_t>(pitch * rows)};
     cuuint32_t box[3] = {128u, static_cast<cuuint32_t>(box_rows), 1u};
-    cuuint32_t elem[3] = {1u, 1u, 1u};
-    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, rank, const_cast<void *>(base), dims,
-                          strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    CUresult r = encode_cached(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, rank, const_cast<void *>(base),
+                               dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B,
+                               CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
     if (r != CUDA_SUCCESS)
         return fail(W8A8_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for [%lld, %lld] box %d",
                     static_cast<int>(r), static_cast<long long>(rows),
@@ -162,10 +220,8 @@ w8a8_status encode_out_map(CUtensorMap *map, void *base, int64_t rows, int64_t c
     cuuint64_t strides[2] = {static_cast<cuuint64_t>(pitch) * eb,
                              static_cast<cuuint64_t>(pitch) * eb * static_cast<cuuint64_t>(rows)};
     cuuint32_t box[3] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows), 1u};
-    cuuint32_t elem[3] = {1u, 1u, 1u};
-    CUresult r = g_encode(map, dt, rank, base, dims, strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                          swizzle, CU_TENSOR_MAP_L2_PROMOTION_NONE,
-                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    CUresult r = encode_cached(map, dt, rank, base, dims, strides, box, swizzle,
+                               CU_TENSOR_MAP_L2_PROMOTION_NONE);
     if (r != CUDA_SUCCESS)
         return fail(W8A8_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for C [%lld, %lld]",
                     static_cast<int>(r), static_cast<long long>(rows), static_cast<long long>(cols));
@@ -209,7 +265,7 @@ w8a8_status check_options(const w8a8_options *o)
     if (o->variant < W8A8_VARIANT_AUTO || o->variant > W8A8_VARIANT_GENERIC)
         return fail(W8A8_ERR_INVALID_ARG, "unknown variant %d", o->variant);
     if (o->split_k < 0 || o->stages < 0 || o->stages > 8 || o->grid_limit < 0 || o->m_tile < 0 ||
-        o->debug_skip_load < 0)
+        o->debug_skip_load < 0 || o->splitk_atomic < 0 || o->splitk_atomic > 1)
         return fail(W8A8_ERR_INVALID_ARG, "negative or out-of-range option");
     if (o->block_n_tile != 0 && o->block_n_tile != 128 && o->block_n_tile != 192 &&
         o->block_n_tile != 256)
@@ -224,9 +280,6 @@ int mt_for(int mma_n)
     return mma_n <= 32 ? 32 : mma_n <= 64 ? 64 : mma_n <= 128 ? 128 : 256;
 }
 
-constexpr size_t kCounterWords = 65536;
-constexpr size_t kCounterBytes = kCounterWords * 4;
-
 // The launch plan of one call.
 struct Plan {
     int variant;      // W8A8_VARIANT_TILED / SWAPAB / SPLITK
@@ -237,6 +290,7 @@ struct Plan {
     int64_t sk_len;                        // tiled stream-K: (tile, group) steps per CTA
     int sk_first_tile;                     // tiled stream-K: tiles before it run whole
     int tile_bytes;                        // swap family: bytes per staged C-tile element
+    int atomic;                            // SPLITK: one fp32 plane reduced with red.add
     size_t smem;
 };
 
@@ -396,6 +450,7 @@ w8a8_status make_plan(int64_t M, int64_t N, int64_t K, int out_bytes, const w8a8
     pl->stages = stages;
     pl->smem = swapab_smem_bytes(mt, stages, gps, tile_bytes, x_esize, csplits);
     pl->tile_bytes = tile_bytes;
+    pl->atomic = (variant == W8A8_VARIANT_SPLITK && o && o->splitk_atomic) ? 1 : 0;
     if (splits == 1)
         pl->variant = W8A8_VARIANT_SWAPAB;
     return W8A8_OK;
@@ -413,7 +468,8 @@ size_t splitk_workspace_bytes(int64_t M, int64_t N, const Plan &pl)
         return kCounterBytes + static_cast<size_t>(pl.grid) * 2 * pl.bn * 128 * 4;
     if (pl.variant != W8A8_VARIANT_SPLITK || pl.splits <= 1)
         return 0;
-    const size_t partial = static_cast<size_t>(pl.splits) * M * N * 4;
+    const size_t planes = pl.atomic ? 1 : static_cast<size_t>(pl.splits);
+    const size_t partial = planes * M * N * 4;
     return kCounterBytes + (partial + 255) / 256 * 256;
 }
 
@@ -421,8 +477,8 @@ w8a8_status library_workspace(int dev, cudaStream_t stream, size_t bytes, void *
                               bool inject_failure = false)
 {
     if (inject_failure)     // host-side fault injection (w8a8_options.debug_fail_alloc)
-        return fail(W8A8_ERR_CUDA, "cudaMalloc(workspace) failed: out of memory (injected by "
-                                   "debug_fail_alloc)");
+        return fail(W8A8_ERR_CUDA, "cudaMallocAsync(workspace) failed: out of memory (injected "
+                                   "by debug_fail_alloc)");
     std::lock_guard<std::mutex> lock(g_mutex);
     Workspace &w = g_workspaces[std::make_pair(dev, stream)];
     if (w.bytes >= bytes) {
@@ -437,21 +493,25 @@ w8a8_status library_workspace(int dev, cudaStream_t stream, size_t bytes, void *
         return fail(W8A8_ERR_WORKSPACE,
                     "split-K workspace would have to grow during stream capture; "
                     "pass w8a8_options.workspace_dev or call once before capturing");
+    // Stream-ordered: the old workspace is released after the work already
+    // queued on this stream (the only work that uses it), the new one is
+    // allocated and zeroed in order on the stream; nothing synchronises the
+    // device or the host.
     if (w.ptr) {
-        e = cudaFree(w.ptr);   // synchronises with work still using it
+        e = cudaFreeAsync(w.ptr, stream);
         w.ptr = nullptr;
         w.bytes = 0;
         if (e != cudaSuccess)
-            return cuda_fail(e, "cudaFree(workspace)");
+            return cuda_fail(e, "cudaFreeAsync(workspace)");
     }
-    e = cudaMalloc(&w.ptr, bytes);
+    e = cudaMallocAsync(&w.ptr, bytes, stream);
     if (e != cudaSuccess) {
         w.ptr = nullptr;
-        return cuda_fail(e, "cudaMalloc(workspace)");
+        return cuda_fail(e, "cudaMallocAsync(workspace)");
     }
-    e = cudaMemset(w.ptr, 0, bytes);
+    e = cudaMemsetAsync(w.ptr, 0, bytes, stream);
     if (e != cudaSuccess)
-        return cuda_fail(e, "cudaMemset(workspace)");
+        return cuda_fail(e, "cudaMemsetAsync(workspace)");
     w.bytes = bytes;
     *out = w.ptr;
     return W8A8_OK;
@@ -814,6 +874,13 @@ w8a8_status run(const void *A, const float *a_s, const void *B, const float *b_s
                 return st;
             p.counters = static_cast<unsigned *>(ws);
             p.ws = reinterpret_cast<float *>(static_cast<char *>(ws) + kCounterBytes);
+            if (pl.atomic) {
+                // The plane is shared with other calls on this workspace (whose
+                // partial sums stay there): zero it in order on the stream.
+                e = cudaMemsetAsync(p.ws, 0, static_cast<size_t>(M) * N * 4, stream);
+                if (e != cudaSuccess)
+                    return cuda_fail(e, "cudaMemsetAsync(split-K plane)");
+            }
         }
         p.M = static_cast<int>(M);
         p.N = static_cast<int>(N);
@@ -833,6 +900,7 @@ w8a8_status run(const void *A, const float *a_s, const void *B, const float *b_s
         p.out_kind = out;
         p.out_bytes = pl.tile_bytes;
         p.cluster_reduce = (pl.variant == W8A8_VARIANT_SPLITK_CLUSTER && pl.splits > 1) ? 1 : 0;
+        p.atomic_reduce = (pl.variant == W8A8_VARIANT_SPLITK && pl.splits > 1 && pl.atomic) ? 1 : 0;
         // A masked call learns which experts have tokens only after the wait,
         // so it streams no weights before it (most of them may be unused).
         p.prefetch_weights = (o && o->pdl && o->weights_static && !masked) ? 1 : 0;
@@ -846,6 +914,36 @@ w8a8_status run(const void *A, const float *a_s, const void *B, const float *b_s
     return W8A8_OK;
 }
 
+// The fused quantise-and-multiply call runs in one swap-AB launch up to this
+// many tokens; above it, as the quantiser followed by the planned matmul.  In
+// the fused kernel every CTA quantises its whole token tile (each weight block
+// repeats the same work), so its cost grows with M; measured on GB300 at
+// N = 4096, K = 256 from bf16: fused 4.4 / 5.2 / 5.5 us at M = 1 / 16 / 100
+// against 5.1 / 5.7 / 6.1 us for the two launches, and 6.8 / 6.8 us against
+// 6.3 / 6.4 us at M = 184 / 214.
+constexpr int64_t kFusedMaxM = 128;
+
+// Bytes of device scratch a quant_matmul call takes (0 when it runs fused):
+// the planned matmul's own split-K workspace -- or at least the counter block,
+// which the codes must not overwrite -- then the codes and the scales.
+size_t quant_matmul_scratch(int64_t M, int64_t N, int64_t K, int out, const w8a8_options *o,
+                            const DeviceInfo &info, size_t *mm_bytes)
+{
+    *mm_bytes = 0;
+    const int v = o ? o->variant : W8A8_VARIANT_AUTO;
+    if (v != W8A8_VARIANT_AUTO || M <= kFusedMaxM)
+        return 0;
+    w8a8_options mo = {};
+    if (o)
+        mo = *o;
+    Plan pl;
+    if (make_plan(M, N, K, out == W8A8_OUT_FP32 ? 4 : 2, &mo, info, &pl) != W8A8_OK)
+        return 0;
+    auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+    *mm_bytes = std::max(splitk_workspace_bytes(M, N, pl), kCounterBytes);
+    return *mm_bytes + up(static_cast<size_t>(M) * K) + up(static_cast<size_t>(M) * cdiv(K, 128) * 4);
+}
+
 }  // namespace
 
 namespace w8a8 {
@@ -855,6 +953,8 @@ w8a8_status record_error(w8a8_status st, const char *message)
 {
     return fail(st, "%s", message);
 }
+// Drops the allocation-free entry point's per-device set-up (noalloc.cu).
+void noalloc_forget();
 }  // namespace w8a8
 
 extern "C" {
@@ -908,8 +1008,56 @@ w8a8_status w8a8_block_fp8_quant_matmul(const void *X_dev, w8a8_in_dtype x_dtype
     FusedAct fa;
     fa.X = X_dev;
     fa.kind = x_dtype;
-    return run(nullptr, nullptr, B_dev, b_s_dev, C_dev, M, N, K, block_n, block_k, out_dtype,
-               reinterpret_cast<cudaStream_t>(stream), opts, Grouping(), fa);
+    const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if ((!opts || opts->variant == W8A8_VARIANT_AUTO) && M > kFusedMaxM) {
+        g_last_error[0] = '\0';
+        w8a8_status st = check_problem(M, N, K, block_n, block_k, out_dtype);
+        if (st != W8A8_OK)
+            return st;
+        if ((st = check_options(opts)) != W8A8_OK)
+            return st;
+        int dev;
+        DeviceInfo info;
+        if ((st = current_device(&dev, &info)) != W8A8_OK)
+            return st;
+        size_t mm_bytes = 0;
+        const size_t total = quant_matmul_scratch(M, N, K, out_dtype, opts, info, &mm_bytes);
+        if (total == 0)
+            return fail(W8A8_ERR_UNSUPPORTED, "no matmul plan for %lld x %lld x %lld",
+                        static_cast<long long>(M), static_cast<long long>(N),
+                        static_cast<long long>(K));
+        void *ws = nullptr;
+        if ((st = acquire_workspace(opts, dev, s, total, &ws)) != W8A8_OK)
+            return st;
+        auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+        char *codes = static_cast<char *>(ws) + mm_bytes;
+        float *scales = reinterpret_cast<float *>(codes + up(static_cast<size_t>(M) * K));
+        if ((st = w8a8_quantize_fp8_per_token_group(X_dev, x_dtype, codes, scales, M, K, 128,
+                                                    stream)) != W8A8_OK)
+            return st;
+        w8a8_options mo = {};
+        if (opts)
+            mo = *opts;
+        mo.workspace_dev = ws;
+        mo.workspace_bytes = mm_bytes;
+        return run(codes, scales, B_dev, b_s_dev, C_dev, M, N, K, block_n, block_k, out_dtype, s,
+                   &mo);
+    }
+    return run(nullptr, nullptr, B_dev, b_s_dev, C_dev, M, N, K, block_n, block_k, out_dtype, s,
+               opts, Grouping(), fa);
+}
+
+size_t w8a8_block_fp8_quant_matmul_workspace_size(int64_t M, int64_t N, int64_t K,
+                                                  w8a8_out_dtype out_dtype, const w8a8_options *opts)
+{
+    if (check_problem(M, N, K, 128, 128, out_dtype) != W8A8_OK || check_options(opts) != W8A8_OK)
+        return 0;
+    int dev;
+    DeviceInfo info;
+    if (current_device(&dev, &info) != W8A8_OK)
+        return 0;
+    size_t mm_bytes = 0;
+    return quant_matmul_scratch(M, N, K, out_dtype, opts, info, &mm_bytes);
 }
 
 w8a8_status w8a8_block_fp8_grouped_matmul_masked(const void *A_dev, const float *a_s_dev,
@@ -992,11 +1140,12 @@ w8a8_status w8a8_block_fp8_matmul_host(const void *A_host, const float *a_s_host
                    {das, a_s_host, static_cast<size_t>(M * G * 4)},
                    {dB, B_host, static_cast<size_t>(N * K)},
                    {dbs, b_s_host, static_cast<size_t>(cdiv(N, 128) * G * 4)}};
-    // Host inputs that the device can address -- page-locked mapped memory, or
-    // any host memory where the device reads through the host's page tables
-    // (ATS on a Grace-Blackwell node) -- are gathered by one kernel (one launch
-    // instead of four copies, each with its own latency); anything else goes
-    // through ordinary copies (synchronous for pageable memory).
+    // Page-locked inputs the device can address are gathered by one kernel (one
+    // launch instead of four copies, each with its own latency); the caller
+    // keeps them unchanged until the stream has passed the call.  Anything
+    // else, pageable memory included, goes through cudaMemcpyAsync, which for
+    // pageable memory returns only once the source has been read: the caller
+    // may reuse a pageable input as soon as the call returns.
     int dev = 0;
     DeviceInfo info;
     if ((st = current_device(&dev, &info)) != W8A8_OK)
@@ -1010,8 +1159,6 @@ w8a8_status w8a8_block_fp8_matmul_host(const void *A_host, const float *a_s_host
             cudaGetLastError();     // unknown to CUDA: copied below
         } else if (attr.type == cudaMemoryTypeHost && attr.devicePointer != nullptr) {
             src = attr.devicePointer;
-        } else if (attr.type == cudaMemoryTypeUnregistered && info.host_tables) {
-            src = copies[i].src;    // pageable, read through the host's page tables
         }
         if (!src) {
             mapped = false;
@@ -1120,6 +1267,7 @@ w8a8_status w8a8_block_fp8_plan(int64_t M, int64_t N, int64_t K, w8a8_out_dtype 
     plan_out->stages = pl.stages;
     plan_out->grid_limit = pl.grid;
     plan_out->workspace_bytes = splitk_workspace_bytes(M, N, pl);
+    plan_out->splitk_atomic = (pl.variant == W8A8_VARIANT_SPLITK && pl.splits > 1) ? pl.atomic : 0;
     return W8A8_OK;
 }
 
@@ -1182,6 +1330,7 @@ int w8a8_abi_version(void) { return W8A8_ABI_VERSION; }
 
 void w8a8_shutdown(void)
 {
+    w8a8::noalloc_forget();
     std::lock_guard<std::mutex> lock(g_mutex);
     int cur = -1;
     cudaGetDevice(&cur);

@@ -31,6 +31,7 @@
 // cluster barrier before TMEM is released and either CTA exits.
 #include "epilogue.cuh"
 #include "kernels.cuh"
+#include "promote.cuh"
 #include "ptx.cuh"
 
 namespace w8a8 {
@@ -65,6 +66,9 @@ template <int BN, int STAGES, int CPW, int EB> struct PairLayout {
     static constexpr size_t kEpiBytes = 4 * kPromoWG * 2048 * kEpiBufs;
     static constexpr int kRegsLow = 56;
     static constexpr int kRegsHigh = kThreads == 384 ? 224 : 152;
+    static_assert(128 * kRegsLow + (kThreads - 128) * kRegsHigh <=
+                      kThreads * ((65536 / kThreads) & ~7),
+                  "register split exceeds the launch's registers");
     static constexpr size_t kScaleBytes = kScaleSlots * kSlotFloats * 4;
     // full, pair_full, empty per stage; tfull, tempty per buffer; scale ring; drain
     static constexpr int kBars = 3 * STAGES + 2 * kBufs + 2 * kScaleSlots + 1;
@@ -351,20 +355,12 @@ __global__ void __launch_bounds__(PairLayout<BN, STAGES, CPW, EB>::kThreads, 1)
                 }
                 tc_fence_after_sync();
                 const uint32_t taddr = tmem_base + ((q * 32u) << 16) + buf * BN + h * CPW;
-#pragma unroll
-                for (int c = 0; c < CPW / 64; ++c) {
-                    uint32_t v[64];
-                    tmem_load_64cols(taddr + 64u * c, v);
-#pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        fma2(acc[32 * c + j], s2, pack2(v[2 * j], v[2 * j + 1]));
-                }
-                // Released after the FMAs: handing the buffer back between the
-                // last TMEM load and its FMAs measured slower (2.18 vs 2.32 PFLOP/s).
-                tc_fence_before_sync();
-                __syncwarp();
-                if (lane == 0)
-                    mbar_arrive_remote(cluster_map(tempty_bar(buf), 0));
+                promote_group<L::kPairs>(acc, taddr, s2, [&]() {
+                    tc_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive_remote(cluster_map(tempty_bar(buf), 0));
+                });
                 ++it;
             }
             if (!ok)

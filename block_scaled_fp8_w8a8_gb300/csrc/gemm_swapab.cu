@@ -595,6 +595,40 @@ __global__ void __launch_bounds__(SwapLayout<MT>::kThreads, SwapLayout<MT>::kMin
             for (int j = 0; j < L::kCols; ++j)
                 if (c0 + j < p.mma_n)
                     tile[(c0 + j) * 128 + row] = acc[j];
+        } else if (ok && p.atomic_reduce) {
+            // Non-deterministic split-K (the page's atomic form): add this
+            // split's partial into the one fp32 plane (zeroed on the stream
+            // before the launch), take a ticket; the last arrival casts the
+            // tile's sums into C.
+            const bool n_ok = n < p.N;
+#pragma unroll
+            for (int j = 0; j < L::kCols; ++j) {
+                const int m = m0 + c0 + j;
+                if (n_ok && c0 + j < p.mma_n && m < p.M)
+                    atomicAdd(p.ws + static_cast<size_t>(m) * p.N + n, acc[j]);
+            }
+            __threadfence();
+            named_barrier(1, kPromoThreads);
+            const int tile = blockIdx.z * gridDim.x + blockIdx.x;
+            if (tid == 0) {
+                const unsigned prev = atomicAdd(p.counters + tile, 1u);
+                *last_flag = (prev == static_cast<unsigned>(p.splits - 1)) ? 1 : 0;
+            }
+            named_barrier(1, kPromoThreads);
+            if (*last_flag) {
+                __threadfence();
+                const int rows = min(p.mma_n, p.M - m0);
+                const int c4n = min(128, p.N - nb * 128) / 4;
+                for (int it = tid; it < rows * c4n; it += kPromoThreads) {
+                    const int r = it / c4n, c4 = it - r * c4n;
+                    const float4 sum = __ldcg(reinterpret_cast<const float4 *>(
+                        p.ws + static_cast<size_t>(m0 + r) * p.N + nb * 128 + 4 * c4));
+                    store4(p.C, static_cast<size_t>(m0 + r) * p.ldc + nb * 128 + 4 * c4, sum,
+                           p.out_kind);
+                }
+                if (tid == 0)
+                    p.counters[tile] = 0u;   // ready for the next call
+            }
         } else if (ok) {
             // Deterministic split-K: publish this split's partial tile, take a
             // ticket; the last arrival sums the splits in order 0..S-1.

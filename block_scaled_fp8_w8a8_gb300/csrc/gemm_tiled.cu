@@ -30,6 +30,7 @@
 // elements) cannot represent; hence the per-group software promotion.
 #include "epilogue.cuh"
 #include "kernels.cuh"
+#include "promote.cuh"
 #include "ptx.cuh"
 
 namespace w8a8 {
@@ -207,11 +208,17 @@ template <int BN, int STAGES, int CPW, int EB> struct TiledLayout {
     static constexpr int kEpiBufs = EB;
     static constexpr size_t kEpiBytes = 4 * kPromoWG * 2048 * kEpiBufs;
     // setmaxnreg split (registers per thread) between the first warpgroup
-    // (producer, MMA issuer, scale loader) and the promotion warpgroups; the
-    // sum over all threads equals the launch's registers (kThreads x 65536/kThreads,
-    // rounded down to a multiple of 8): 384 threads x 168, 512 threads x 128.
-    static constexpr int kRegsLow = 56;
-    static constexpr int kRegsHigh = kThreads == 384 ? 224 : 152;
+    // (producer, MMA issuer(s), scale loader) and the promotion warpgroups; the
+    // sum over all threads stays within the launch's registers (kThreads x
+    // 65536/kThreads, rounded down to a multiple of 8): 384 threads x 168,
+    // 512 threads x 128.  With two MMA issuers (BN = 128) the first warpgroup
+    // needs more than 56 to run without spills, and 64-column promotion
+    // threads need far fewer than 224.
+    static constexpr int kRegsLow = (kThreads == 384 && BN == 128) ? 72 : 56;
+    static constexpr int kRegsHigh = kThreads == 384 ? (BN == 128 ? 200 : 224) : 152;
+    static_assert(128 * kRegsLow + (kThreads - 128) * kRegsHigh <=
+                      kThreads * ((65536 / kThreads) & ~7),
+                  "register split exceeds the launch's registers");
     static constexpr size_t kScaleBytes = kScaleSlots * kSlotFloats * 4;
     static constexpr int kBars = 2 * STAGES + 2 * kBufs + 2 * kScaleSlots + 2;
     static constexpr size_t kSmem =
@@ -484,20 +491,12 @@ __global__ void __launch_bounds__(TiledLayout<BN, STAGES, CPW, EB>::kThreads, 1)
                 }
                 tc_fence_after_sync();
                 const uint32_t taddr = tmem_base + ((q * 32u) << 16) + buf * BN + h * CPW;
-                // 64-column loads (fewer, larger loads measured faster than
-                // 32-column ones); the group's time is its sync and FMA chain.
-#pragma unroll
-                for (int c = 0; c < CPW / 64; ++c) {
-                    uint32_t v[64];
-                    tmem_load_64cols(taddr + 64u * c, v);
-#pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        fma2(acc[32 * c + j], s2, pack2(v[2 * j], v[2 * j + 1]));
-                }
-                tc_fence_before_sync();
-                __syncwarp();
-                if (lane == 0)
-                    mbar_arrive(tempty_bar(buf));
+                promote_group<L::kPairs>(acc, taddr, s2, [&]() {
+                    tc_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive(tempty_bar(buf));
+                });
                 ++it;
             }
             if (!ok)

@@ -26,6 +26,13 @@ enum WaitSite : uint32_t {
     SITE_PAIR_PEER = 13,   // CTA-pair kernel: waiting for the other CTA's stage
 };
 
+// Split-K / stream-K workspace layout (the library's, the caller's or the
+// allocation-free entry point's fixed array): a block of kCounterWords per-tile
+// arrival counters at offset 0, then the fp32 partial sums from offset
+// kCounterBytes.  Every call leaves the counters it used at zero.
+constexpr size_t kCounterWords = 65536;
+constexpr size_t kCounterBytes = kCounterWords * 4;
+
 // Tokens on the MMA M side: one CTA per SM walks 128 x BN output tiles.
 struct TiledParams {
     const float *a_s;      // [M, G]
@@ -77,6 +84,9 @@ struct SwapParams {
     int prefetch_weights;  // start the B loads before waiting on the previous grid
     int cluster_reduce;    // splits > 1: the grid.y CTAs of a tile form one cluster and
                            // reduce their partial tiles through distributed shared memory
+    int atomic_reduce;     // splits > 1, workspace form: ws is one [M, N] fp32 plane, zero
+                           // at launch, that every split adds its partial into with
+                           // red.global.add.f32; the last split of a tile casts it into C
     int debug_skip_tma;
     unsigned *status;
     unsigned long long wait_limit;

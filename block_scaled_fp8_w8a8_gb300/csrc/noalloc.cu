@@ -26,7 +26,8 @@ w8a8_status record_error(w8a8_status st, const char *message);
 namespace {
 
 constexpr size_t kScratchBytes = W8A8_NOALLOC_SCRATCH_BYTES;
-constexpr size_t kCounterBytes = 65536 * 4;   // the split-K counter block at the start
+using w8a8::kCounterBytes;   // the split-K counter block at the start of the scratch
+static_assert(kScratchBytes > kCounterBytes, "scratch must hold the counter block");
 
 // The shared scratch.  In host code this name is only a stand-in for the device
 // symbol: its device address comes from cudaGetSymbolAddress below.
@@ -61,6 +62,17 @@ w8a8_status scratch_address(void **out)
 }
 
 }  // namespace
+
+namespace w8a8 {
+// Forget the looked-up addresses (w8a8_shutdown): after a cudaDeviceReset the
+// module is reloaded, possibly elsewhere, so the next call repeats the set-up.
+void noalloc_forget()
+{
+    std::lock_guard<std::mutex> lock(g_mutex);
+    for (void *&p : g_scratch_dev)
+        p = nullptr;
+}
+}  // namespace w8a8
 
 extern "C" w8a8_status w8a8_block_fp8_matmul_splitk_noalloc(
     const void *A_dev, const float *a_s_dev, const void *B_dev, const float *b_s_dev,

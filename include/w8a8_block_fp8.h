@@ -134,12 +134,27 @@ typedef enum {
  *   debug_fail_alloc   test hook: 1 makes a call that would take the library's own
  *                      workspace fail as if cudaMalloc had failed (W8A8_ERR_CUDA,
  *                      nothing launched, the cached workspace untouched).  0 = off.
+ *   splitk_atomic      SPLITK (the workspace form, forced or chosen by the dispatcher):
+ *                      1 = the pages' non-deterministic reduction -- the call zeroes
+ *                      one [M, N] fp32 plane of the workspace (cudaMemsetAsync on
+ *                      the stream), every split adds its fp32 partial tile into it
+ *                      with red.global.add.f32 and the last split of a tile casts
+ *                      it into C.  Within the tolerance,
+ *                      but the bits may change from run to run (the order of the
+ *                      additions is the order the splits arrive in); the
+ *                      workspace holds one plane instead of split_k.  0 = the
+ *                      ordered, bit-reproducible reduction.
  *   workspace_dev      SPLITK and stream-K TILED: caller-owned device scratch of workspace_bytes
  *                      bytes, 256-byte aligned, at least
  *                      w8a8_block_fp8_workspace_size() bytes, all zero before its
  *                      first use (every call leaves its counter words zero again).
  *                      NULL = a per-device, per-stream workspace the library
- *                      allocates on first use (not during stream capture).
+ *                      allocates on first use and grows when a larger problem
+ *                      needs it, stream-ordered on the call's stream
+ *                      (cudaMallocAsync, cudaFreeAsync of the smaller one after
+ *                      the work already queued there); not during stream
+ *                      capture (W8A8_ERR_WORKSPACE: call once before capturing,
+ *                      or pass a workspace).
  *   wait_limit_cycles  bound of every device-side wait in SM clock cycles
  *                      (0 = 2^32 cycles, about 2 s)
  */
@@ -154,7 +169,8 @@ typedef struct {
     int debug_skip_load;
     int weights_static;
     int debug_fail_alloc;
-    int reserved_i[2];
+    int splitk_atomic;
+    int reserved_i;
     void *workspace_dev;
     size_t workspace_bytes;
     unsigned long long wait_limit_cycles;
@@ -206,16 +222,25 @@ w8a8_status w8a8_block_fp8_matmul_strided(const void *A_dev, int64_t lda, const 
 /*
  * End-to-end call on HOST buffers: brings A, a_s, B and b_s from host memory
  * into `staging_dev`, runs the matmul, and copies C back into host memory, all
- * in order on `stream`.  When all four inputs are host memory the device can
- * address -- page-locked memory (e.g. cudaHostAlloc / torch pin_memory) or, on
- * a device that reads through the host's page tables (ATS, as on
- * Grace-Blackwell nodes), also pageable memory -- one gather kernel reads them
- * over the CPU-GPU link; otherwise they are copied with cudaMemcpyAsync
- * (synchronous for pageable memory).  C goes back the same way: one kernel
- * writes it where the device can address C_host, else cudaMemcpyAsync.  The
- * call returns once the work is enqueued; synchronise `stream` before reading
- * C_host.  With page-locked buffers the call can be captured in a CUDA graph
- * (every replay then moves the buffers' current contents).  staging_dev is caller-owned device memory of at least
+ * in order on `stream`.
+ *
+ * Inputs.  When all four are page-locked host memory the device can address
+ * (e.g. cudaHostAlloc / torch pin_memory), one gather kernel reads them over
+ * the CPU-GPU link after the call has returned: they must stay allocated and
+ * unchanged until `stream` has passed the call.  Otherwise (pageable memory,
+ * or a mix) they are copied with cudaMemcpyAsync, which for pageable memory
+ * has read the source before the call returns, so those buffers may be
+ * reused at once.
+ *
+ * Output.  One kernel writes C where the device can address C_host
+ * (page-locked memory, or any host memory on a device that reads and writes
+ * through the host's page tables -- ATS, as on Grace-Blackwell nodes), else
+ * cudaMemcpyAsync.  Either way the write happens after the call has returned:
+ * keep C_host allocated and synchronise `stream` before reading it.
+ *
+ * With page-locked buffers the call can be captured in a CUDA graph (every
+ * replay then moves the buffers' current contents).  staging_dev is
+ * caller-owned device memory of at least
  * w8a8_block_fp8_host_staging_size(M, N, K, out_dtype) bytes, 256-byte aligned.
  */
 w8a8_status w8a8_block_fp8_matmul_host(const void *A_host, const float *a_s_host,
@@ -249,7 +274,10 @@ w8a8_status w8a8_block_fp8_matmul_host(const void *A_host, const float *a_s_host
  *
  * The first call on each device does a one-time set-up (it looks up the
  * array's device address with that device current); make that first call
- * before any stream capture.  All calls share the one array, which keeps the
+ * before any stream capture.  The address is kept for the process: a caller
+ * that resets a device (cudaDeviceReset) must call w8a8_shutdown() before
+ * using this entry point on it again, so that the next call repeats the
+ * set-up instead of launching on a stale address.  All calls share the one array, which keeps the
  * last call's contents (each call zeroes the counters it uses): calls that
  * overlap on the GPU -- e.g. on two streams without ordering between them --
  * race and give wrong results.  Order them (one stream, or events).
@@ -265,24 +293,40 @@ w8a8_status w8a8_block_fp8_matmul_splitk_noalloc(const void *A_dev, const float 
 /*
  * The matmul from an unquantised activation: C = matmul(quantise(X), B) with
  * quantise() exactly as w8a8_quantize_fp8_per_token_group (per token and
- * 128-wide K group, scale amax / 448, E4M3 codes), done inside the swap-AB
- * kernel: the quantiser warps turn X into the MMA operand in shared memory,
- * so that the decode step "quantise the activation, multiply" is one launch.
- * Bit for bit the same C as the two calls in sequence with the same plan.
+ * 128-wide K group, scale amax / 448, E4M3 codes).  Bit for bit the same C as
+ * the two calls in sequence with the same plan.
  *   X_dev    device, row-major [M, K] of x_dtype (bf16, fp16 or fp32), 16-byte aligned
  *   B_dev, b_s_dev, C_dev, shapes and out_dtype as in w8a8_block_fp8_matmul.
- *   opts: variant AUTO (the measured swap-AB plan for the shape, else the swap-AB
- *   rules), SWAPAB or SPLITK_CLUSTER; other variants are W8A8_ERR_UNSUPPORTED.
- *   X must be finite (see the quantiser).  Aimed at decode sizes: every CTA
- *   quantises its token tile, so large M is better served by the quantiser
- *   followed by the tiled matmul.  The pages have no fused form; the
- *   quantiser's reading is the one declared with w8a8_quantize_fp8_per_token_group.
+ *   opts: variant AUTO, SWAPAB or SPLITK_CLUSTER; other variants are
+ *   W8A8_ERR_UNSUPPORTED.
+ * How it runs.  SWAPAB / SPLITK_CLUSTER, and AUTO up to M = 128 tokens: in one
+ * swap-AB launch whose quantiser warps turn X into the MMA operand in shared
+ * memory (the decode step "quantise the activation, multiply" in one kernel).
+ * AUTO above M = 128: the quantiser, then the dispatcher's matmul plan, two
+ * launches in order on `stream`; every CTA of the fused kernel quantises its
+ * whole token tile, which above that size costs more than the separate
+ * launch (measured on GB300).  The codes and scales then live in device
+ * scratch -- opts->workspace_dev if given (at least
+ * w8a8_block_fp8_quant_matmul_workspace_size() bytes, 256-byte aligned, all
+ * zero before its first use), else the library's per-stream workspace, as for
+ * split-K.  X must be finite (see the quantiser).  The pages have no fused
+ * form; the quantiser's reading is the one declared with
+ * w8a8_quantize_fp8_per_token_group.
  */
 w8a8_status w8a8_block_fp8_quant_matmul(const void *X_dev, w8a8_in_dtype x_dtype, const void *B_dev,
                                         const float *b_s_dev, void *C_dev, int64_t M, int64_t N,
                                         int64_t K, int block_n, int block_k,
                                         w8a8_out_dtype out_dtype, w8a8_stream_t stream,
                                         const w8a8_options *opts);
+
+/* Device scratch (bytes) that w8a8_block_fp8_quant_matmul takes for this problem
+ * and options: 0 when the call runs as one fused launch, else the matmul's own
+ * split-K workspace (at least its 256 KiB counter block) followed by the E4M3
+ * codes [M, K] and the scales [M, ceil(K/128)].  0 also for an unsupported
+ * problem. */
+size_t w8a8_block_fp8_quant_matmul_workspace_size(int64_t M, int64_t N, int64_t K,
+                                                  w8a8_out_dtype out_dtype,
+                                                  const w8a8_options *opts);
 
 /*
  * Grouped (mixture-of-experts) forms of the same matmul: E experts, each with
@@ -420,7 +464,10 @@ const char *w8a8_last_error(void);
 /* W8A8_ABI_VERSION of the loaded library. */
 int w8a8_abi_version(void);
 
-/* Releases cached workspaces of every device this thread's calls touched. */
+/* Releases the library's cached split-K workspaces (every device) and forgets
+ * the allocation-free entry point's per-device set-up, so that its next call
+ * on a device looks the scratch address up again (needed after a
+ * cudaDeviceReset). */
 void w8a8_shutdown(void);
 
 #ifdef __cplusplus

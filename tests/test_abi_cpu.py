@@ -44,6 +44,7 @@ def test_options_struct_layout():
     assert ctypes.sizeof(w8.w8a8_options) == 12 * 4 + 8 + 8 + 8 + 32
     assert w8.w8a8_options.workspace_dev.offset == 48
     assert w8.w8a8_options.debug_fail_alloc.offset == 36
+    assert w8.w8a8_options.splitk_atomic.offset == 40
 
 
 @pytest.mark.parametrize("M,N,K,bn,bk,out,status", [

@@ -84,6 +84,41 @@ def test_fused_auto_plan_and_special_rows():
     assert_close(auto.cpu()[ok], ref[ok], rms=float(np.sqrt(np.mean(ref[ok] ** 2))), what="auto")
 
 
+@pytest.mark.parametrize("M,N,K", [(129, 4096, 256), (214, 4096, 256), (300, 8192, 1024),
+                                   (2048, 1536, 4096), (158, 512, 4096)])
+def test_auto_above_cutover_runs_quantiser_then_matmul(M, N, K):
+    """AUTO above 128 tokens runs the quantiser and the dispatcher's matmul as
+    two launches inside the call: the bits of the two public calls with the
+    AUTO plan, in the library's workspace and in a caller's workspace of the
+    size the library reports."""
+    X = synth.activations(M, K, seed=M + K, dtype=torch.bfloat16, outlier_p=1e-3).cuda()
+    w = synth.make_inputs(1, N, K, seed=N)
+    B, b_s = w.B.cuda(), w.b_s.cuda()
+    want = _two_step(X, B, b_s, "bf16", {})
+    got = w8.quant_matmul(X, B, b_s, "bf16")
+    nbytes = w8.w8a8_block_fp8_quant_matmul_workspace_size(M, N, K, w8.W8A8_OUT_BF16)
+    assert nbytes >= M * K + 65536 * 4
+    ws = torch.zeros(nbytes, dtype=torch.uint8, device="cuda")
+    got_ws = w8.quant_matmul(X, B, b_s, "bf16", workspace_dev=ws.data_ptr(), workspace_bytes=nbytes)
+    torch.cuda.synchronize()
+    assert w8.w8a8_get_device_status()[0] == w8.W8A8_OK
+    assert torch.equal(got.view(torch.int16), want.view(torch.int16))
+    assert torch.equal(got_ws.view(torch.int16), want.view(torch.int16))
+    assert torch.count_nonzero(ws[:65536 * 4]) == 0       # the counter block is left zero
+    small = w8.w8a8_options(workspace_dev=ws.data_ptr(), workspace_bytes=nbytes - 256)
+    C = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    assert w8.w8a8_block_fp8_quant_matmul(X, w8.W8A8_IN_BF16, B, b_s, C, M, N, K, 128, 128,
+                                          w8.W8A8_OUT_BF16, None, small) == w8.W8A8_ERR_WORKSPACE
+
+
+def test_fused_needs_no_workspace_up_to_the_cutover():
+    for M in (1, 64, 128):
+        assert w8.w8a8_block_fp8_quant_matmul_workspace_size(M, 4096, 256, w8.W8A8_OUT_BF16) == 0
+    forced = w8.options(variant=w8.W8A8_VARIANT_SWAPAB)
+    assert w8.w8a8_block_fp8_quant_matmul_workspace_size(214, 4096, 256, w8.W8A8_OUT_BF16,
+                                                         forced) == 0
+
+
 def test_fused_invalid_calls():
     X = torch.zeros(4, 256, dtype=torch.bfloat16, device="cuda")
     B = torch.zeros(128, 256, dtype=torch.uint8, device="cuda")

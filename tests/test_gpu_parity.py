@@ -174,10 +174,9 @@ def test_host_buffer_call_matches_device_call():
 
 @pytest.mark.parametrize("kind", ["pageable", "pinned_misaligned", "pageable_all"])
 def test_host_buffer_call_other_host_memory(kind):
-    """Pageable inputs are read by the gather kernel where the device walks the
-    host's page tables (ATS), else copied; pinned inputs at odd addresses take
-    the gather kernel's byte path; a pageable result buffer is written by a
-    kernel (ATS) or copied.  All give the device call's bits."""
+    """Pageable inputs are copied with cudaMemcpyAsync; pinned inputs at odd
+    addresses take the gather kernel's byte path; a pageable result buffer is
+    written by a kernel (ATS) or copied.  All give the device call's bits."""
     M, N, K = 37, 264, 528
     x = synth.make_inputs(M, N, K, seed=2)
     dev = run(x, "bf16")
@@ -200,6 +199,31 @@ def test_host_buffer_call_other_host_memory(kind):
     stream = torch.cuda.current_stream()
     w8.check(w8.w8a8_block_fp8_matmul_host(*ptrs, C_host, M, N, K, staging_dev=staging,
                                            staging_bytes=nbytes, stream=stream))
+    stream.synchronize()
+    assert torch.equal(C_host.view(torch.int16), dev.cpu().view(torch.int16))
+
+
+def test_host_buffer_call_pageable_inputs_reusable_on_return():
+    """The documented contract for pageable inputs: the call has read them
+    before it returns, so the caller may overwrite them at once (here before
+    the stream has even started the matmul: a long kernel is queued first)."""
+    M, N, K = 64, 512, 4096
+    x = synth.make_inputs(M, N, K, seed=3)
+    dev = run(x, "bf16")
+    ins = [t.clone() for t in (x.A, x.a_s, x.B, x.b_s)]
+    C_host = torch.empty((M, N), dtype=torch.bfloat16)
+    nbytes = w8.w8a8_block_fp8_host_staging_size(M, N, K, w8.W8A8_OUT_BF16)
+    staging = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.Stream()
+    busy = torch.randn(4096, 4096, device="cuda")
+    with torch.cuda.stream(stream):
+        for _ in range(20):          # keeps the stream busy while the host goes on
+            busy = busy @ busy * 1e-3
+        w8.check(w8.w8a8_block_fp8_matmul_host(*[t.data_ptr() for t in ins], C_host.data_ptr(),
+                                               M, N, K, staging_dev=staging,
+                                               staging_bytes=nbytes, stream=stream))
+    for t in ins:                    # reuse the input buffers right after the call
+        t.view(torch.uint8).fill_(0x7F)
     stream.synchronize()
     assert torch.equal(C_host.view(torch.int16), dev.cpu().view(torch.int16))
 
@@ -256,6 +280,37 @@ def test_cluster_splitk_matches_oracle_and_workspace_variant(M, N, K, splits):
         assert_close(Cc, ref, what=f"cluster {M}x{N}x{K} S={splits} {out}")
         assert torch.equal(Cc.view(torch.int16 if out == "bf16" else torch.int32),
                            Cw.view(torch.int16 if out == "bf16" else torch.int32))
+
+
+@pytest.mark.parametrize("M,N,K,splits", [(16, 512, 4096, 8), (64, 512, 4096, 4), (158, 512, 4096, 16),
+                                          (7, 144, 384, 3), (300, 392, 2048, 2), (1, 8192, 1024, 8)])
+def test_atomic_splitk_matches_oracle(M, N, K, splits):
+    """The non-deterministic split-K (red.global.add.f32 into one fp32 plane,
+    the page's atomic form) is within the bound on every call, on a
+    caller-owned workspace and on the library's own, which the ordered
+    split-K has just filled with its partial sums; the counter block is zero
+    again after the calls."""
+    x = synth.make_inputs(M, N, K, seed=M * 11 + splits, outlier_p=1e-3)
+    ref = oracle.reference_c(x.A, x.a_s, x.B, x.b_s)
+    o = w8.options(variant=w8.W8A8_VARIANT_SPLITK, split_k=splits, splitk_atomic=1)
+    st, pl = w8.w8a8_block_fp8_plan(M, N, K, w8.W8A8_OUT_BF16, o)
+    assert st == w8.W8A8_OK and pl.splitk_atomic == 1 and pl.split_k > 1
+    ordered = w8.w8a8_block_fp8_workspace_size(
+        M, N, K, w8.options(variant=w8.W8A8_VARIANT_SPLITK, split_k=splits))
+    nbytes = w8.w8a8_block_fp8_workspace_size(M, N, K, o)
+    assert nbytes < ordered       # one plane instead of one per split
+    ws = torch.zeros(nbytes, dtype=torch.uint8, device="cuda")
+    for out in ("fp32", "bf16", "fp32"):
+        C = run(x, out, variant=w8.W8A8_VARIANT_SPLITK, split_k=splits, splitk_atomic=1,
+                workspace_dev=ws.data_ptr(), workspace_bytes=nbytes)
+        assert_close(C, ref, what=f"atomic {M}x{N}x{K} S={splits} {out}")
+    assert torch.count_nonzero(ws[:65536 * 4]) == 0
+    # the library's own workspace, after an ordered split-K call left its
+    # partial sums there
+    C = run(x, "fp32", variant=w8.W8A8_VARIANT_SPLITK, split_k=splits)
+    assert_close(C, ref, what=f"ordered {M}x{N}x{K} S={splits}, library workspace")
+    C = run(x, "fp32", variant=w8.W8A8_VARIANT_SPLITK, split_k=splits, splitk_atomic=1)
+    assert_close(C, ref, what=f"atomic {M}x{N}x{K} S={splits}, library workspace")
 
 
 def test_cluster_splitk_deterministic():
