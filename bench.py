@@ -153,20 +153,20 @@ def source_digest(kernel: str = "matmul", read=None) -> str:
 # The decode-size launches write nothing to DRAM during the launch: their C
 # (<= 1.75 MB) is still in L2 when the kernel ends.
 MEASURED_TRAFFIC = {
-    # k_tiled<256,4>: read 96.53 MB + write 99.16 MB (A + B = 83.9 MB, C = 134.2 MB)
-    ("aa7d93d35d338cba", "16384x4096x4096", 2): 195698176,
-    # k_swapab<32>: read 1.175 MB (B 1.05 MB + A, scales), write 0
-    ("aa7d93d35d338cba", "214x4096x256", 2): 1174784,
+    # k_tiled<256,3> stream-K: read 94.54 MB + write 108.85 MB (A + B = 83.9 MB, C = 134.2 MB)
+    ("5709d9c62325d2d3", "16384x4096x4096", 2): 203395328,
+    # k_swapab<32>: read 1.176 MB (B 1.05 MB + A, scales), write 0
+    ("5709d9c62325d2d3", "214x4096x256", 2): 1175552,
     # k_swapab<32> cluster split-K: read 2.843 MB (B 2.1 MB + A with outliers), write 0
-    ("aa7d93d35d338cba", "158x512x4096", 2): 2842624,
-    # k_tiled<192,4>: read 8.713 MB (B 8.4 MB + A), write 0
-    ("aa7d93d35d338cba", "264x8192x1024", 2): 8713472,
-    # k_swapab<32>: read 0.218 MB, write 0
-    ("aa7d93d35d338cba", "64x512x256", 2): 217856,
+    ("5709d9c62325d2d3", "158x512x4096", 2): 2842624,
+    # k_tiled<192,4>: read 8.714 MB (B 8.4 MB + A), write 0
+    ("5709d9c62325d2d3", "264x8192x1024", 2): 8714496,
+    # k_swapab<32>: read 0.217 MB, write 0
+    ("5709d9c62325d2d3", "64x512x256", 2): 217088,
     # k_quant_group128<bf16>, 16384 x 4096: read 134.26 MB + write 36.33 MB
     ("73a59caf748f3efb", "quant_16384x4096", 1): 170590976,
-    # k_swapab<32, grouped> masked decode, 256 experts of 1536 x 4096: read 1.645 GB + write 22.9 MB
-    ("aa7d93d35d338cba", "grouped_decode_masked", 2): 1668109824,
+    # k_swapab<32, grouped> masked decode, 256 experts of 1536 x 4096: read 1.645 GB + write 25.8 MB
+    ("5709d9c62325d2d3", "grouped_decode_masked", 2): 1670986496,
 }
 
 
@@ -413,9 +413,12 @@ def per_shape_durations(wl, floor_us):
         fl = synth.algorithmic_flops(M, N, K)
         by = synth.algorithmic_bytes(M, N, K, out_bytes=wl.out_bytes)
         plan = wl.plans[i]
+        name = VARIANT_NAMES.get(plan.variant, "?")
+        if plan.variant == 1 and plan.split_k in (2, 3):
+            name += "_streamk" if plan.split_k == 2 else "_half_tail"
         row = {"M": M, "N": N, "K": K, "us": round(t * 1e6, 3),
                "tflops": round(fl / t / 1e12, 3), "gbs": round(by / t / 1e9, 1),
-               "variant": VARIANT_NAMES.get(plan.variant, "?"),
+               "variant": name,
                "split_k": plan.split_k, "m_tile": plan.m_tile,
                "block_n_tile": plan.block_n_tile, "stages": plan.stages}
         if floor_us:

@@ -291,6 +291,7 @@ struct Plan {
     int sk_first_tile;                     // tiled stream-K: tiles before it run whole
     int tile_bytes;                        // swap family: bytes per staged C-tile element
     int atomic;                            // SPLITK: one fp32 plane reduced with red.add
+    int half_first, half_items;            // tiled half-width tail (splits == 3)
     size_t smem;
 };
 
@@ -380,7 +381,18 @@ w8a8_status make_plan(int64_t M, int64_t N, int64_t K, int out_bytes, const w8a8
         // at least G steps long (at most two CTAs per tile).  Off by default:
         // measured, it gains only where a partial last wave is short (e.g.
         // 16384 x 1536 x 4096: 100.2 -> 96.0 us) and loses a little elsewhere.
-        const bool sk = split_hint >= 2;
+        // Half-width tail (split_k == 3): the tiles of a partial last wave run
+        // as two 128 x BN/2 halves each, so that twice as many CTAs share it.
+        // Only for 256-column tiles (a half is one promotion warpgroup's
+        // columns) and when the halves fit in one wave.
+        const bool halves = split_hint == 3;
+        const int64_t full_waves = tiles / grid, rest = tiles - full_waves * grid;
+        if (halves && (bn != 256 || rest == 0 || 2 * rest > grid || tiles >= (1ll << 30)))
+            return fail(W8A8_ERR_UNSUPPORTED,
+                        "half-width tail needs 256-column tiles and a last wave of at most half "
+                        "the CTAs (%lld tiles, %lld CTAs, block_n_tile %d)",
+                        static_cast<long long>(tiles), static_cast<long long>(grid), bn);
+        const bool sk = split_hint == 2 || split_hint > 3;
         if (sk && (tiles < grid || tiles > static_cast<int64_t>(kCounterWords) ||
                    tiles * G >= (1ll << 31)))
             return fail(W8A8_ERR_UNSUPPORTED,
@@ -390,9 +402,11 @@ w8a8_status make_plan(int64_t M, int64_t N, int64_t K, int out_bytes, const w8a8
         pl->bn = bn;
         pl->stages = stages;
         pl->grid = static_cast<int>(grid);
-        pl->splits = sk ? 2 : 1;
+        pl->splits = sk ? 2 : halves ? 3 : 1;
         pl->sk_first_tile = static_cast<int>(sk_first);
         pl->sk_len = sk ? cdiv((tiles - sk_first) * G, grid) : 0;
+        pl->half_first = halves ? static_cast<int>(full_waves * grid) : 0;
+        pl->half_items = halves ? static_cast<int>(2 * rest) : 0;
         pl->smem = tiled_smem_bytes(bn, stages);
         if (pl->smem == 0 || pl->smem > dev.smem_optin)
             return fail(W8A8_ERR_UNSUPPORTED, "tiled kernel needs %zu B of shared memory",
@@ -777,7 +791,7 @@ w8a8_status run(const void *A, const float *a_s, const void *B, const float *b_s
     const unsigned long long limit =
         (o && o->wait_limit_cycles) ? o->wait_limit_cycles : kDefaultWaitLimit;
     const int debug_skip = (o && o->debug_skip_load > 0) ? o->debug_skip_load - 1 : -1;
-    LaunchCfg cfg;
+    LaunchCfg cfg = {};
     cfg.stages = pl.stages;
     cfg.grid = pl.grid;
     cfg.pdl = o ? o->pdl : 0;
@@ -810,7 +824,7 @@ w8a8_status run(const void *A, const float *a_s, const void *B, const float *b_s
         CUtensorMap mA, mB, mC;
         const int chunk_cols = out == W8A8_OUT_FP32 ? 16 : 32;   // 64 bytes of a row
         if ((st = encode_u8_map(&mA, A, M, K, 128, 0, sd.lda)) != W8A8_OK ||
-            (st = encode_u8_map(&mB, B, N, K, pair ? pl.bn / 2 : pl.bn,
+            (st = encode_u8_map(&mB, B, N, K, (pair || pl.splits == 3) ? pl.bn / 2 : pl.bn,
                                 contiguous ? gr.experts : 0, sd.ldb)) != W8A8_OK ||
             (st = encode_out_map(&mC, C, M, N, out, chunk_cols, 32, CU_TENSOR_MAP_SWIZZLE_64B, 0,
                                  sd.ldc)) != W8A8_OK)
@@ -833,6 +847,11 @@ w8a8_status run(const void *A, const float *a_s, const void *B, const float *b_s
         p.wait_limit = limit;
         p.m_indices = contiguous ? gr.ids : nullptr;
         p.experts = contiguous ? static_cast<int>(gr.experts) : 1;
+        if (!pair && pl.splits == 3) {
+            p.sk_first_tile = pl.half_first;
+            p.sk_len = pl.half_items;
+            cfg.half_tail = 1;
+        }
         if (!pair && pl.splits == 2) {
             void *ws = nullptr;
             if ((st = acquire_workspace(o, dev, stream, splitk_workspace_bytes(M, N, pl), &ws)) !=

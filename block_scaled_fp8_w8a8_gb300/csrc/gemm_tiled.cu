@@ -86,7 +86,7 @@ __device__ __forceinline__ int tile_expert(const TiledParams &p, int t)
 // stream-K share to the last one or two waves' worth of tiles keeps the tiles
 // in flight at any time adjacent, so their A and B panels are shared in L2.
 // (The host enables stream-K only when num_tiles * G < 2^31.)
-struct SegWalk {
+template <bool HALVES> struct SegWalk {
     int pos, end, G, dp_end, len;
     bool in_sk;
     __device__ explicit SegWalk(const TiledParams &p)
@@ -97,6 +97,8 @@ struct SegWalk {
         if (len > 0)
             end = p.num_tiles * p.G;     // one past the last step
     }
+    static constexpr int hv = -1;        // never a half item
+    __device__ bool half() const { return false; }
     __device__ bool next(int &t, int &g0, int &g1)
     {
         if (!in_sk) {
@@ -119,6 +121,33 @@ struct SegWalk {
         g0 = pos - t * G;
         g1 = min(G, g0 + (end - pos));
         pos += g1 - g0;
+        return true;
+    }
+};
+
+// The walk of the half-width tail instance: whole tiles below sk_first_tile,
+// then sk_len half items (item j: column half hv = j & 1 of tile
+// sk_first_tile + j / 2), each over all K groups.  A separate type, so that
+// the whole-tile kernels carry none of its state (their promotion threads are
+// at their register limit).
+template <> struct SegWalk<true> {
+    int pos, items, G, dp_end, hv;
+    __device__ explicit SegWalk(const TiledParams &p)
+        : pos(static_cast<int>(blockIdx.x)), items(static_cast<int>(p.sk_len)), G(p.G),
+          dp_end(p.sk_first_tile), hv(-1)
+    {
+    }
+    __device__ bool half() const { return hv >= 0; }
+    __device__ bool next(int &t, int &g0, int &g1)
+    {
+        const int j = pos - dp_end;
+        if (j >= items)
+            return false;
+        hv = j < 0 ? -1 : (j & 1);
+        t = j < 0 ? pos : dp_end + (j >> 1);
+        g0 = 0;
+        g1 = G;
+        pos += static_cast<int>(gridDim.x);
         return true;
     }
 };
@@ -212,8 +241,8 @@ template <int BN, int STAGES, int CPW, int EB> struct TiledLayout {
     // sum over all threads stays within the launch's registers (kThreads x
     // 65536/kThreads, rounded down to a multiple of 8): 384 threads x 168,
     // 512 threads x 128.  With two MMA issuers (BN = 128) the first warpgroup
-    // needs more than 56 to run without spills, and 64-column promotion
-    // threads need far fewer than 224.
+    // needs more than 56 to run without spills; a promotion thread holds 128
+    // (BN = 256) or 64 accumulator registers plus one 32-column TMEM chunk.
     static constexpr int kRegsLow = (kThreads == 384 && BN == 128) ? 72 : 56;
     static constexpr int kRegsHigh = kThreads == 384 ? (BN == 128 ? 200 : 224) : 152;
     static_assert(128 * kRegsLow + (kThreads - 128) * kRegsHigh <=
@@ -225,7 +254,7 @@ template <int BN, int STAGES, int CPW, int EB> struct TiledLayout {
         1024 + kStageBytes + kEpiBytes + kScaleBytes + kBars * 8 + 16;
 };
 
-template <int BN, int STAGES, int CPW, int EB>
+template <int BN, int STAGES, int CPW, int EB, bool HALVES>
 __global__ void __launch_bounds__(TiledLayout<BN, STAGES, CPW, EB>::kThreads, 1)
     k_tiled(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
             const __grid_constant__ CUtensorMap tmC, const TiledParams p)
@@ -302,7 +331,7 @@ __global__ void __launch_bounds__(TiledLayout<BN, STAGES, CPW, EB>::kThreads, 1)
             long long issued = 0;
             bool ok = true;
             int e_next = tile_expert(p, blockIdx.x);
-            SegWalk walk(p);
+            SegWalk<HALVES> walk(p);
             int t, g0, g1;
             while (ok && walk.next(t, g0, g1)) {
                 int mb, nb;
@@ -314,7 +343,20 @@ __global__ void __launch_bounds__(TiledLayout<BN, STAGES, CPW, EB>::kThreads, 1)
                         ok = false;
                         break;
                     }
-                    if (issued != p.debug_skip_tma) {
+                    if (issued != p.debug_skip_tma && HALVES) {
+                        // The half-tail instance's B map has boxes of BN/2 rows:
+                        // two per whole tile, one (the item's column half) per
+                        // half item, which the MMA reads from the stage's start.
+                        const bool hf = walk.half();
+                        mbar_arrive_expect_tx(full_bar(stage),
+                                              L::kABytes + (hf ? L::kBBytes / 2 : L::kBBytes));
+                        tma_load_2d(sA + stage * L::kABytes, &tmA, full_bar(stage), g * 128, mb * 128);
+                        const int brow = nb * BN + (hf && walk.hv > 0 ? BN / 2 : 0);
+                        tma_load_2d(sB + stage * L::kBBytes, &tmB, full_bar(stage), g * 128, brow);
+                        if (!hf)
+                            tma_load_2d(sB + stage * L::kBBytes + L::kBBytes / 2, &tmB,
+                                        full_bar(stage), g * 128, brow + BN / 2);
+                    } else if (issued != p.debug_skip_tma) {
                         mbar_arrive_expect_tx(full_bar(stage), L::kABytes + L::kBBytes);
                         tma_load_2d(sA + stage * L::kABytes, &tmA, full_bar(stage), g * 128, mb * 128);
                         if (p.m_indices)
@@ -361,14 +403,19 @@ __global__ void __launch_bounds__(TiledLayout<BN, STAGES, CPW, EB>::kThreads, 1)
             // same work list) where kTiledIssuers says so.
             constexpr uint32_t n_iss = kTiledIssuers<BN, STAGES>();
             const uint32_t w = warp == 1 ? 0u : 1u;
-            constexpr uint32_t idesc = idesc_e4m3_f32(128, BN);
+            constexpr uint32_t idesc_full = idesc_e4m3_f32(128, BN);
+            constexpr uint32_t idesc_half = idesc_e4m3_f32(128, BN / 2);
             int stage = 0;
             uint32_t phase = 0;
             uint32_t it = 0;
             bool ok = true;
-            SegWalk walk(p);
+            SegWalk<HALVES> walk(p);
             int t, g0, g1;
             while (ok && walk.next(t, g0, g1)) {
+                // a half item writes its BN/2 columns where whole tiles keep them
+                // (columns hv * BN/2 of the buffer)
+                const uint32_t idesc = walk.half() ? idesc_half : idesc_full;
+                const uint32_t dcol = walk.half() ? static_cast<uint32_t>(walk.hv) * (BN / 2) : 0u;
                 for (int g = g0; g < g1; ++g) {
                     if (it % n_iss == w) {
                         const uint32_t buf = it % L::kBufs;
@@ -379,7 +426,7 @@ __global__ void __launch_bounds__(TiledLayout<BN, STAGES, CPW, EB>::kThreads, 1)
                             break;
                         }
                         tc_fence_after_sync();
-                        const uint32_t d = tmem_base + buf * BN;
+                        const uint32_t d = tmem_base + buf * BN + dcol;
                         const uint64_t ad = sw128_kmajor_desc(sA + stage * L::kABytes);
                         const uint64_t bd = sw128_kmajor_desc(sB + stage * L::kBBytes);
 #pragma unroll
@@ -407,7 +454,7 @@ __global__ void __launch_bounds__(TiledLayout<BN, STAGES, CPW, EB>::kThreads, 1)
             uint32_t sphase = 0;
             bool ok = true;
             int e_next = tile_expert(p, blockIdx.x);
-            SegWalk walk(p);
+            SegWalk<HALVES> walk(p);
             int t, g0, g1;
             while (ok && walk.next(t, g0, g1)) {
                 int mb, nb;
@@ -457,11 +504,15 @@ __global__ void __launch_bounds__(TiledLayout<BN, STAGES, CPW, EB>::kThreads, 1)
         uint32_t it = 0;
         int slot = 0;
         uint32_t sphase = 0;
-        SegWalk walk(p);
+        SegWalk<HALVES> walk(p);
         int t, g0, g1;
         while (walk.next(t, g0, g1)) {
             int mb, nb;
             tile_coords(t, p.num_m_tiles, p.num_n_tiles, mb, nb);
+            // A half item (BN/2 == CPW columns) lies where warpgroup hv finds
+            // its share of a whole tile, so that warpgroup promotes and stores
+            // it as usual; the other only keeps the barriers' counts.
+            const bool idle = walk.half() && h != walk.hv;
             const int col0 = nb * BN + h * CPW;
             uint64_t acc[L::kPairs];
 #pragma unroll
@@ -491,17 +542,21 @@ __global__ void __launch_bounds__(TiledLayout<BN, STAGES, CPW, EB>::kThreads, 1)
                 }
                 tc_fence_after_sync();
                 const uint32_t taddr = tmem_base + ((q * 32u) << 16) + buf * BN + h * CPW;
-                promote_group<L::kPairs>(acc, taddr, s2, [&]() {
+                auto release = [&]() {
                     tc_fence_before_sync();
                     __syncwarp();
                     if (lane == 0)
                         mbar_arrive(tempty_bar(buf));
-                });
+                };
+                if (!idle)
+                    promote_group<L::kPairs>(acc, taddr, s2, release);
+                else
+                    release();
                 ++it;
             }
             if (!ok)
                 break;
-            if (g0 > 0 || g1 < p.G) {
+            if (!HALVES && (g0 > 0 || g1 < p.G)) {
                 // Stream-K: a piece of a tile shared with other CTAs.
                 if (!stream_k_fixup<BN, CPW, L::kPairs>(p, acc, t, row, h, last_flag))
                     continue;          // another contributor finishes this tile
@@ -511,7 +566,7 @@ __global__ void __launch_bounds__(TiledLayout<BN, STAGES, CPW, EB>::kThreads, 1)
             // swizzle, conflict-free 16-byte writes) and asynchronous TMA stores,
             // which write whole row segments and clip rows past M / columns past N.
             const int y = mb * 128 + static_cast<int>(q * 32);
-            if (y < p.M && col0 < p.N)
+            if (!idle && y < p.M && col0 < p.N)
                 store_tile_rows<L::kPairs, L::kEpiBufs>(acc, &tmC, epi_buf, lane, col0, y, p.N,
                                                         p.out_kind);
         }
@@ -527,12 +582,12 @@ __global__ void __launch_bounds__(TiledLayout<BN, STAGES, CPW, EB>::kThreads, 1)
     }
 }
 
-template <int BN, int STAGES, int CPW, int EB>
-cudaError_t launch_tiled_t(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmC,
+template <int BN, int STAGES, int CPW, int EB, bool HALVES>
+cudaError_t launch_tiled_h(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmC,
                            const TiledParams &p, const LaunchCfg &cfg)
 {
     using L = TiledLayout<BN, STAGES, CPW, EB>;
-    auto kernel = k_tiled<BN, STAGES, CPW, EB>;
+    auto kernel = k_tiled<BN, STAGES, CPW, EB, HALVES>;
     static volatile int smem_set[kMaxDeviceFlags] = {};
     cudaError_t e = ensure_smem_limit(kernel, smem_set);
     if (e != cudaSuccess)
@@ -548,6 +603,20 @@ cudaError_t launch_tiled_t(const CUtensorMap &tmA, const CUtensorMap &tmB, const
     lc.attrs = attr;
     lc.numAttrs = cfg.pdl ? 1 : 0;
     return cudaLaunchKernelEx(&lc, kernel, tmA, tmB, tmC, p);
+}
+
+// The half-width tail needs one 128-column promotion warpgroup per half.
+template <int BN, int STAGES, int CPW, int EB>
+cudaError_t launch_tiled_t(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmC,
+                           const TiledParams &p, const LaunchCfg &cfg)
+{
+    if (cfg.half_tail) {
+        if constexpr (BN == 256 && CPW == 128)
+            return launch_tiled_h<BN, STAGES, CPW, EB, true>(tmA, tmB, tmC, p, cfg);
+        else
+            return cudaErrorInvalidValue;
+    }
+    return launch_tiled_h<BN, STAGES, CPW, EB, false>(tmA, tmB, tmC, p, cfg);
 }
 
 }  // namespace

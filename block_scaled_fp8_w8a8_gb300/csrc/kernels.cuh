@@ -58,6 +58,14 @@ struct TiledParams {
     // starts in and the one it ends in) and count themselves in
     // counters[tile]; the second adds the first's partial and stores the tile.
     // counters is zero between calls.
+    //
+    // Half-width tail (one-CTA kernel, BN = 256 only, LaunchCfg::half_tail;
+    // its kernel instance reads the two stream-K fields below): tiles below
+    // sk_first_tile (a whole number of waves) are dealt out whole, round
+    // robin; each later tile becomes two 128 x BN/2 items (left and right
+    // column half), dealt out the same way, so that a partial last wave keeps
+    // twice as many CTAs busy; sk_len is then the number of half items,
+    // 2 x (num_tiles - sk_first_tile).
     long long sk_len;
     int sk_first_tile;
     float *ws;
@@ -119,6 +127,7 @@ struct LaunchCfg {
     int grid;        // persistent kernels: number of CTAs
     int pdl;
     cudaStream_t stream;
+    int half_tail;   // tiled kernel: run the half-width tail instance (see TiledParams)
 };
 
 // Small M (at most kSmallMaxM tokens) on the CUDA cores: 32 weight rows per CTA.

@@ -78,6 +78,11 @@ def candidates(M, N, K, sms=152):
             if tiles >= sms and tiles % sms and bn != 128:
                 out.append(dict(variant=b.W8A8_VARIANT_TILED, block_n_tile=bn, stages=stages,
                                 split_k=2))
+            # half-width tail where the last wave holds at most half the CTAs
+            rest = tiles % sms if tiles >= sms else 0
+            if bn == 256 and rest and 2 * rest <= sms:
+                out.append(dict(variant=b.W8A8_VARIANT_TILED, block_n_tile=bn, stages=stages,
+                                split_k=3))
     if M >= 512:
         for bn, stages in ((256, 6), (256, 4), (192, 6)):
             out.append(dict(variant=b.W8A8_VARIANT_TILED_PAIR, block_n_tile=bn, stages=stages))
@@ -163,6 +168,25 @@ class Bench:
         return best, plan
 
 
+def read_table(path):
+    """{(M, N, K): best row} from a table this module wrote: each row's tuned
+    point is the M of its comment."""
+    import re
+    out = {}
+    pat = re.compile(r"\{(\d+), (\d+), (\d+), (\d+), (\d+), (\d+), (\d+), (\d+), (\d+)\},"
+                     r"\s*// M=(\d+): ([0-9.]+) us")
+    with open(path) as f:
+        for line in f:
+            m = pat.search(line)
+            if not m:
+                continue
+            v = [int(x) for x in m.groups()[:10]]
+            out[(v[9], v[2], v[3])] = {"variant": v[4], "split_k": v[5], "m_tile": v[6],
+                                       "block_n_tile": v[7], "stages": v[8],
+                                       "us": float(m.group(11))}
+    return out
+
+
 def write_table(path, lines):
     with open(path, "w") as f:
         f.write("// m_lo, m_hi, n, k, variant, split_k, m_tile, block_n_tile, stages\n")
@@ -187,9 +211,15 @@ def main():
                     help="append each shape's best configuration to this file as it is found")
     ap.add_argument("--table-from", default=None,
                     help="write the table from a --jsonl file instead of measuring")
+    ap.add_argument("--merge", action="store_true",
+                    help="with --grid or --table-from: keep the existing table's entries and "
+                         "replace only the shapes measured now")
+    ap.add_argument("--half-tail-only", action="store_true",
+                    help="with --grid: only the shapes whose 256-column tiles leave a last "
+                         "wave of at most half the SMs (where split_k = 3 applies)")
     args = ap.parse_args()
     if args.table_from:
-        best_by_shape = {}
+        best_by_shape = read_table(args.out) if args.merge else {}
         with open(args.table_from) as f:
             for line in f:
                 r = json.loads(line)
@@ -205,12 +235,20 @@ def main():
         shapes = [s for s in shapes if s[0] <= args.max_m]
     if args.shapes:
         shapes = [tuple(int(v) for v in s.split("x")) for s in args.shapes.split(",")]
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    if args.half_tail_only:
+        def half_tail(M, N):
+            tiles = -(-M // 128) * -(-N // 256)
+            rest = tiles % sms if tiles >= sms else 0
+            return M >= 64 and rest and 2 * rest <= sms
+        shapes = [s for s in shapes if half_tail(s[0], s[1])]
     l2 = torch.cuda.get_device_properties(0).L2_cache_size
-    report, best_by_shape = [], {}
+    report = []
+    best_by_shape = read_table(args.out) if args.merge else {}
     for (M, N, K) in shapes:
         bench = Bench(M, N, K, l2)
         rows = []
-        for cfg in candidates(M, N, K):
+        for cfg in candidates(M, N, K, sms):
             try:
                 us, plan = bench.time(cfg)
             except b.W8A8Error as e:        # e.g. a cluster that cannot be scheduled

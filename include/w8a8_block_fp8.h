@@ -115,7 +115,10 @@ typedef enum {
  *                      finished by the second, which adds the first's fp32
  *                      partial (same bits on every run).  Needs a workspace like
  *                      SPLITK and at least as many tiles as CTAs, else
- *                      W8A8_ERR_UNSUPPORTED
+ *                      W8A8_ERR_UNSUPPORTED.  3 = half-width tail: the tiles
+ *                      of a partial last wave run as two 128 x 128 halves each
+ *                      (block_n_tile 256 only, the halves within one wave;
+ *                      no workspace; same bits as whole tiles)
  *   block_n_tile       TILED / TILED_PAIR: 128, 192 or 256 output columns per tile (0 = choose)
  *   m_tile             SWAPAB/SPLITK only: tokens per tile, multiple of 16, <= 256 (0 = choose)
  *   stages             shared-memory pipeline depth 1..8 (0 = choose)

@@ -40,6 +40,7 @@ VARIANTS = {
     "tiled128s5": (dict(variant=T, block_n_tile=128, stages=5), 300),
     "streamk256": (dict(variant=T, block_n_tile=256, split_k=2, grid_limit=5), 700),
     "streamk192": (dict(variant=T, block_n_tile=192, split_k=2, grid_limit=5), 700),
+    "halves256": (dict(variant=T, block_n_tile=256, split_k=3, grid_limit=5), 700),
     "pair256s6": (dict(variant=P, block_n_tile=256, stages=6), 600),
     "pair256s4": (dict(variant=P, block_n_tile=256, stages=4), 600),
     "pair192": (dict(variant=P, block_n_tile=192), 600),

@@ -166,3 +166,41 @@ def test_grouped_contiguous_rejects_stream_k():
                                                       w8.W8A8_OUT_BF16,
                                                       torch.cuda.current_stream(), o)
     assert st == w8.W8A8_ERR_UNSUPPORTED
+
+
+# ------------------------------------------------------------------ half-width tail (split_k = 3)
+
+@pytest.mark.parametrize("M,N,K,grid", [(1200, 1024, 640, 16), (300, 520, 384, 2),
+                                        (640, 4096, 256, 24), (4096, 1536, 4096, 0),
+                                        (257, 1000, 1040, 5)])
+def test_half_width_tail_matches_oracle_and_whole_tiles(M, N, K, grid):
+    """The tiles of a partial last wave run as two 128-column halves: the
+    result is the oracle's within the bound and bit-equal to whole tiles
+    (same K order, same promotion).  Covers ragged M, N and K tails, a last
+    tile whose right half lies wholly past N, and the real 4096 x 1536 x 4096
+    wave shape (192 tiles on 152 CTAs)."""
+    x = synth.make_inputs(M, N, K, seed=M + N + K)
+    opts = dict(block_n_tile=256, grid_limit=grid)
+    pl = plan(M, N, K, split_k=3, **opts)
+    assert pl.split_k == 3 and pl.workspace_bytes == 0
+    C = run(x, "fp32", split_k=3, **opts)
+    whole = run(x, "fp32", split_k=1, **opts)
+    assert torch.equal(C.view(torch.int32), whole.view(torch.int32))
+    if M * N * K <= 2 ** 31:
+        ref = oracle.reference_c(x.A, x.a_s, x.B, x.b_s)
+        assert_close(C, ref, what=f"halves {M}x{N}x{K} grid {grid}")
+    else:
+        rows = sample_rows(M)
+        ref = reference_rows(x, rows)
+        assert_close(C[torch.from_numpy(rows).cuda()], ref, rms=rms_estimate(ref),
+                     what=f"halves {M}x{N}x{K}")
+
+
+def test_half_width_tail_limits():
+    """Refused before any launch: 128- or 192-column tiles, no partial wave,
+    or a last wave whose halves would not fit in one wave."""
+    for opts in (dict(block_n_tile=128, grid_limit=16), dict(block_n_tile=192, grid_limit=16),
+                 dict(block_n_tile=256, grid_limit=20), dict(block_n_tile=256, grid_limit=7)):
+        st, _ = w8.w8a8_block_fp8_plan(1200, 1024, 640, w8.W8A8_OUT_BF16,
+                                       w8.options(variant=w8.W8A8_VARIANT_TILED, split_k=3, **opts))
+        assert st == w8.W8A8_ERR_UNSUPPORTED, opts
