@@ -163,8 +163,8 @@ MEASURED_TRAFFIC = {
     ("5709d9c62325d2d3", "264x8192x1024", 2): 8714496,
     # k_swapab<32>: read 0.217 MB, write 0
     ("5709d9c62325d2d3", "64x512x256", 2): 217088,
-    # k_quant_group128<bf16>, 16384 x 4096: read 134.26 MB + write 36.33 MB
-    ("73a59caf748f3efb", "quant_16384x4096", 1): 170590976,
+    # k_quant_group128<bf16>, 16384 x 4096: read 134.26 MB + write 36.37 MB
+    ("db0c77fe7e6cb807", "quant_16384x4096", 1): 170631680,
     # k_swapab<32, grouped> masked decode, 256 experts of 1536 x 4096: read 1.645 GB + write 25.8 MB
     ("5709d9c62325d2d3", "grouped_decode_masked", 2): 1670986496,
 }
