@@ -13,12 +13,13 @@ from __future__ import annotations
 
 from ._binding import (  # noqa: F401
     EXPORTED, W8A8Error, W8A8_OK, W8A8_ERR_INVALID_ARG, W8A8_ERR_UNSUPPORTED, W8A8_ERR_CUDA,
-    W8A8_ERR_DEVICE_TIMEOUT, W8A8_ERR_WORKSPACE, W8A8_ERR_NO_DEVICE, W8A8_OUT_BF16,
+    W8A8_ERR_DEVICE_TIMEOUT, W8A8_ERR_WORKSPACE, W8A8_ERR_NO_DEVICE, W8A8_ERR_DEVICE_BOUNDS,
+    W8A8_OUT_BF16,
     W8A8_OUT_FP16, W8A8_OUT_FP32, W8A8_VARIANT_AUTO, W8A8_VARIANT_TILED, W8A8_VARIANT_SWAPAB,
     W8A8_VARIANT_SPLITK, W8A8_VARIANT_SPLITK_CLUSTER, W8A8_VARIANT_SMALLM, W8A8_VARIANT_TILED_PAIR,
     W8A8_VARIANT_GENERIC, w8a8_block_fp8_matmul_strided,
     check, library_path, load_library,
-    w8a8_abi_version,
+    w8a8_abi_version, w8a8_debug_bounds_build, w8a8_env_config, debug_bounds_requested,
     w8a8_block_fp8_host_staging_size, w8a8_block_fp8_matmul, w8a8_block_fp8_matmul_ex,
     w8a8_block_fp8_matmul_host, w8a8_block_fp8_plan, w8a8_block_fp8_workspace_size,
     w8a8_block_fp8_matmul_splitk_noalloc, W8A8_NOALLOC_SCRATCH_BYTES,

@@ -20,6 +20,7 @@ W8A8_ERR_CUDA = 3
 W8A8_ERR_DEVICE_TIMEOUT = 4
 W8A8_ERR_WORKSPACE = 5
 W8A8_ERR_NO_DEVICE = 6
+W8A8_ERR_DEVICE_BOUNDS = 7
 
 W8A8_OUT_BF16, W8A8_OUT_FP16, W8A8_OUT_FP32 = 0, 1, 2
 W8A8_VARIANT_AUTO, W8A8_VARIANT_TILED, W8A8_VARIANT_SWAPAB, W8A8_VARIANT_SPLITK = 0, 1, 2, 3
@@ -48,6 +49,8 @@ EXPORTED = (
     "w8a8_status_string",
     "w8a8_last_error",
     "w8a8_abi_version",
+    "w8a8_debug_bounds_build",
+    "w8a8_env_config",
     "w8a8_shutdown",
 )
 
@@ -65,7 +68,7 @@ class w8a8_options(ctypes.Structure):
         ("weights_static", ctypes.c_int),
         ("debug_fail_alloc", ctypes.c_int),
         ("splitk_atomic", ctypes.c_int),
-        ("reserved_i", ctypes.c_int),
+        ("debug_bad_index", ctypes.c_int),
         ("workspace_dev", ctypes.c_void_p),
         ("workspace_bytes", ctypes.c_size_t),
         ("wait_limit_cycles", ctypes.c_ulonglong),
@@ -82,8 +85,16 @@ class W8A8Error(RuntimeError):
 _lib = None
 
 
+def debug_bounds_requested() -> bool:
+    """W8A8_DEBUG_BOUNDS=1 in the environment selects the debug-bounds library."""
+    v = os.environ.get("W8A8_DEBUG_BOUNDS", "")
+    if v not in ("", "0", "1"):
+        raise RuntimeError(f"W8A8_DEBUG_BOUNDS={v!r}: want 0 or 1")
+    return v == "1"
+
+
 def library_path() -> str:
-    return _build.lib_path()
+    return _build.lib_path(debug_bounds_requested())
 
 
 def load_library():
@@ -93,8 +104,9 @@ def load_library():
         return _lib
     path = library_path()
     if not os.path.exists(path):
+        how = "build(debug_bounds=True)" if debug_bounds_requested() else "build()"
         raise RuntimeError(f"the CUDA library {path} has not been built; "
-                           "run block_scaled_fp8_w8a8_gb300.build.build() first")
+                           f"run block_scaled_fp8_w8a8_gb300.build.{how} first")
     lib = ctypes.CDLL(path)
     vp, i64, i32, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
     opt_p = ctypes.POINTER(w8a8_options)
@@ -134,6 +146,11 @@ def load_library():
     lib.w8a8_last_error.argtypes = []
     lib.w8a8_last_error.restype = ctypes.c_char_p
     lib.w8a8_abi_version.argtypes = []
+    lib.w8a8_debug_bounds_build.argtypes = []
+    lib.w8a8_debug_bounds_build.restype = ctypes.c_int
+    lib.w8a8_env_config.argtypes = [ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int),
+                                    ctypes.POINTER(ctypes.c_ulonglong)]
+    lib.w8a8_env_config.restype = ctypes.c_int
     lib.w8a8_shutdown.argtypes = []
     lib.w8a8_shutdown.restype = None
     for name in ("w8a8_block_fp8_matmul", "w8a8_block_fp8_matmul_ex", "w8a8_block_fp8_matmul_host",
@@ -287,6 +304,17 @@ def w8a8_last_error() -> str:
 
 def w8a8_abi_version() -> int:
     return load_library().w8a8_abi_version()
+
+
+def w8a8_debug_bounds_build() -> int:
+    return load_library().w8a8_debug_bounds_build()
+
+
+def w8a8_env_config():
+    """(status, force_variant, deterministic, wait_limit_cycles) as the library parsed them."""
+    fv, det, wl = ctypes.c_int(0), ctypes.c_int(0), ctypes.c_ulonglong(0)
+    st = load_library().w8a8_env_config(ctypes.byref(fv), ctypes.byref(det), ctypes.byref(wl))
+    return st, fv.value, det.value, wl.value
 
 
 def w8a8_shutdown() -> None:

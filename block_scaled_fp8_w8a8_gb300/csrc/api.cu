@@ -14,6 +14,7 @@
 #include <algorithm>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <map>
 #include <mutex>
@@ -44,6 +45,105 @@ w8a8_status cuda_fail(cudaError_t e, const char *what)
 }
 
 constexpr unsigned long long kDefaultWaitLimit = 1ull << 32;   // ~2 s at 2 GHz
+// The shortest wait bound a caller may set: a kernel that gives up drains the
+// copies it has in flight under the same bound, and those land in far less.
+constexpr unsigned long long kMinWaitLimit = 100000;
+
+// Settings from the environment, parsed once at the first call (see the
+// header): a forced variant for plain calls that leave it AUTO, the
+// deterministic flag, the default wait bound.  A value that does not parse
+// makes every call fail with its message.
+struct EnvConfig {
+    int force_variant = 0;
+    int deterministic = 0;
+    unsigned long long wait_limit = 0;
+    bool bad = false;
+    char message[200] = "";
+};
+
+EnvConfig parse_env()
+{
+    EnvConfig c;
+    auto bad = [&](const char *name, const char *value, const char *want) {
+        c.bad = true;
+        snprintf(c.message, sizeof(c.message), "environment variable %s=\"%s\": %s", name, value,
+                 want);
+    };
+    if (const char *v = getenv("W8A8_FORCE_VARIANT"); v && *v) {
+        static const struct {
+            const char *name;
+            int variant;
+        } names[] = {{"tiled", W8A8_VARIANT_TILED},
+                     {"swapab", W8A8_VARIANT_SWAPAB},
+                     {"splitk", W8A8_VARIANT_SPLITK},
+                     {"splitk_cluster", W8A8_VARIANT_SPLITK_CLUSTER},
+                     {"smallm", W8A8_VARIANT_SMALLM},
+                     {"tiled_pair", W8A8_VARIANT_TILED_PAIR},
+                     {"generic", W8A8_VARIANT_GENERIC}};
+        for (const auto &n : names)
+            if (std::strcmp(v, n.name) == 0)
+                c.force_variant = n.variant;
+        char *end = nullptr;
+        const long num = std::strtol(v, &end, 10);
+        if (!c.force_variant && end && *end == '\0' && num >= W8A8_VARIANT_TILED &&
+            num <= W8A8_VARIANT_GENERIC)
+            c.force_variant = static_cast<int>(num);
+        if (!c.force_variant)
+            bad("W8A8_FORCE_VARIANT", v,
+                "want tiled, swapab, splitk, splitk_cluster, smallm, tiled_pair, generic or 1..7");
+    }
+    if (const char *v = getenv("W8A8_DETERMINISTIC"); v && *v) {
+        if (std::strcmp(v, "0") == 0 || std::strcmp(v, "1") == 0)
+            c.deterministic = v[0] == '1';
+        else if (!c.bad)
+            bad("W8A8_DETERMINISTIC", v, "want 0 or 1");
+    }
+    if (const char *v = getenv("W8A8_WAIT_LIMIT_CYCLES"); v && *v) {
+        char *end = nullptr;
+        const unsigned long long n = std::strtoull(v, &end, 10);
+        if (end && *end == '\0' && v[0] != '-' && n >= kMinWaitLimit)
+            c.wait_limit = n;
+        else if (!c.bad)
+            bad("W8A8_WAIT_LIMIT_CYCLES", v, "want a whole number of cycles, at least 100000");
+    }
+    if (const char *v = getenv("W8A8_DEBUG_BOUNDS"); v && *v) {
+        if (std::strcmp(v, "0") != 0 && std::strcmp(v, "1") != 0 && !c.bad)
+            bad("W8A8_DEBUG_BOUNDS", v, "want 0 or 1");
+    }
+    return c;
+}
+
+const EnvConfig &env_config()
+{
+    static const EnvConfig c = parse_env();
+    return c;
+}
+
+// One call's options with the environment's defaults applied: *out is `o`
+// itself when nothing changes, else `scratch` holding the adjusted copy.  The
+// forced variant applies to plain (ungrouped, unfused) calls only.
+w8a8_status with_env(const w8a8_options *o, bool plain, w8a8_options *scratch,
+                     const w8a8_options **out)
+{
+    const EnvConfig &env = env_config();
+    if (env.bad)
+        return fail(W8A8_ERR_INVALID_ARG, "%s", env.message);
+    const bool force = plain && env.force_variant && (!o || o->variant == W8A8_VARIANT_AUTO);
+    const bool det = env.deterministic && o && o->splitk_atomic;
+    const bool wait = env.wait_limit && (!o || !o->wait_limit_cycles);
+    *out = o;
+    if (!force && !det && !wait)
+        return W8A8_OK;
+    *scratch = o ? *o : w8a8_options{};
+    if (force)
+        scratch->variant = env.force_variant;
+    if (det)
+        scratch->splitk_atomic = 0;
+    if (wait)
+        scratch->wait_limit_cycles = env.wait_limit;
+    *out = scratch;
+    return W8A8_OK;
+}
 constexpr int kMaxDevices = 64;
 
 struct DeviceInfo {
@@ -265,8 +365,12 @@ w8a8_status check_options(const w8a8_options *o)
     if (o->variant < W8A8_VARIANT_AUTO || o->variant > W8A8_VARIANT_GENERIC)
         return fail(W8A8_ERR_INVALID_ARG, "unknown variant %d", o->variant);
     if (o->split_k < 0 || o->stages < 0 || o->stages > 8 || o->grid_limit < 0 || o->m_tile < 0 ||
-        o->debug_skip_load < 0 || o->splitk_atomic < 0 || o->splitk_atomic > 1)
+        o->debug_skip_load < 0 || o->splitk_atomic < 0 || o->splitk_atomic > 1 ||
+        o->debug_bad_index < 0 || o->debug_bad_index > 1)
         return fail(W8A8_ERR_INVALID_ARG, "negative or out-of-range option");
+    if (o->wait_limit_cycles != 0 && o->wait_limit_cycles < kMinWaitLimit)
+        return fail(W8A8_ERR_INVALID_ARG, "wait_limit_cycles %llu: 0 or at least %llu",
+                    o->wait_limit_cycles, kMinWaitLimit);
     if (o->block_n_tile != 0 && o->block_n_tile != 128 && o->block_n_tile != 192 &&
         o->block_n_tile != 256)
         return fail(W8A8_ERR_INVALID_ARG, "block_n_tile must be 0, 128, 192 or 256");
@@ -627,6 +731,7 @@ w8a8_status run_generic(const void *A, const float *a_s, const void *B, const fl
     p.block_n = block_n;
     p.block_k = block_k;
     p.out_kind = out;
+    p.status = info.status;
     LaunchCfg cfg = {};
     cfg.pdl = o ? o->pdl : 0;
     cfg.stream = stream;
@@ -644,6 +749,9 @@ w8a8_status run(const void *A, const float *a_s, const void *B, const float *b_s
     g_last_error[0] = '\0';
     w8a8_status st;
     const bool plain = fa.X == nullptr && gr.mode == Grouping::NONE;
+    w8a8_options env_opts;
+    if ((st = with_env(o, plain, &env_opts, &o)) != W8A8_OK)
+        return st;
     Strides sd;
     if (plain) {
         // Arguments no kernel takes; then the tensor-core kernels' guards, and
@@ -790,7 +898,9 @@ w8a8_status run(const void *A, const float *a_s, const void *B, const float *b_s
     const int NB = static_cast<int>(cdiv(N, 128));
     const unsigned long long limit =
         (o && o->wait_limit_cycles) ? o->wait_limit_cycles : kDefaultWaitLimit;
-    const int debug_skip = (o && o->debug_skip_load > 0) ? o->debug_skip_load - 1 : -1;
+    int debug_skip = (o && o->debug_skip_load > 0) ? o->debug_skip_load - 1 : -1;
+    if (W8A8_DEBUG_BOUNDS && o && o->debug_bad_index && debug_skip < 0)
+        debug_skip = kDebugBadFirstLoad;
     LaunchCfg cfg = {};
     cfg.stages = pl.stages;
     cfg.grid = pl.grid;
@@ -1069,6 +1179,9 @@ w8a8_status w8a8_block_fp8_quant_matmul(const void *X_dev, w8a8_in_dtype x_dtype
 size_t w8a8_block_fp8_quant_matmul_workspace_size(int64_t M, int64_t N, int64_t K,
                                                   w8a8_out_dtype out_dtype, const w8a8_options *opts)
 {
+    w8a8_options env_opts;
+    if (with_env(opts, true, &env_opts, &opts) != W8A8_OK)
+        return 0;
     if (check_problem(M, N, K, 128, 128, out_dtype) != W8A8_OK || check_options(opts) != W8A8_OK)
         return 0;
     int dev;
@@ -1236,6 +1349,9 @@ w8a8_status w8a8_block_fp8_matmul_host(const void *A_host, const float *a_s_host
 
 size_t w8a8_block_fp8_workspace_size(int64_t M, int64_t N, int64_t K, const w8a8_options *opts)
 {
+    w8a8_options env_opts;
+    if (with_env(opts, true, &env_opts, &opts) != W8A8_OK)
+        return 0;
     if (check_problem(M, N, K, 128, 128, W8A8_OUT_BF16) != W8A8_OK || check_options(opts) != W8A8_OK)
         return 0;
     int dev;
@@ -1258,6 +1374,9 @@ w8a8_status w8a8_block_fp8_plan(int64_t M, int64_t N, int64_t K, w8a8_out_dtype 
     if (st == W8A8_ERR_INVALID_ARG)
         return st;
     const w8a8_status guards = st;
+    w8a8_options env_opts;
+    if ((st = with_env(opts, true, &env_opts, &opts)) != W8A8_OK)
+        return st;
     if ((st = check_options(opts)) != W8A8_OK)
         return st;
     const int v = opts ? opts->variant : W8A8_VARIANT_AUTO;
@@ -1339,6 +1458,8 @@ const char *w8a8_status_string(w8a8_status s)
     case W8A8_ERR_DEVICE_TIMEOUT: return "W8A8_ERR_DEVICE_TIMEOUT: a bounded device wait ran out";
     case W8A8_ERR_WORKSPACE: return "W8A8_ERR_WORKSPACE: workspace too small or misaligned";
     case W8A8_ERR_NO_DEVICE: return "W8A8_ERR_NO_DEVICE: no usable sm_100-family device";
+    case W8A8_ERR_DEVICE_BOUNDS:
+        return "W8A8_ERR_DEVICE_BOUNDS: a debug-bounds check found an index outside its buffer";
     default: return "unknown w8a8_status";
     }
 }
@@ -1346,6 +1467,24 @@ const char *w8a8_status_string(w8a8_status s)
 const char *w8a8_last_error(void) { return g_last_error; }
 
 int w8a8_abi_version(void) { return W8A8_ABI_VERSION; }
+
+int w8a8_debug_bounds_build(void) { return W8A8_DEBUG_BOUNDS ? 1 : 0; }
+
+w8a8_status w8a8_env_config(int *force_variant, int *deterministic,
+                            unsigned long long *wait_limit_cycles)
+{
+    g_last_error[0] = '\0';
+    const EnvConfig &env = env_config();
+    if (force_variant)
+        *force_variant = env.force_variant;
+    if (deterministic)
+        *deterministic = env.deterministic;
+    if (wait_limit_cycles)
+        *wait_limit_cycles = env.wait_limit;
+    if (env.bad)
+        return fail(W8A8_ERR_INVALID_ARG, "%s", env.message);
+    return W8A8_OK;
+}
 
 void w8a8_shutdown(void)
 {

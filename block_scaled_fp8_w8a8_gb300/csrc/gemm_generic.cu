@@ -73,9 +73,10 @@ __global__ void __launch_bounds__(256) k_generic(const GenericParams p)
                 float av = 0.f, bv = 0.f;
                 if (c < kc) {
                     const int64_t m = m0 + r, n = n0 + r;
-                    if (m < p.M)
+                    // (the debug-bounds build re-checks each index against K)
+                    if (m < p.M && in_bounds(k0 + c < p.K, p.status, SITE_BOUNDS_A))
                         av = e4m3_to_float(p.A[m * p.lda + k0 + c]);
-                    if (n < p.N)
+                    if (n < p.N && in_bounds(k0 + c < p.K, p.status, SITE_BOUNDS_B))
                         bv = e4m3_to_float(p.B[n * p.ldb + k0 + c]);
                 }
                 As[c][r] = av;
@@ -123,6 +124,8 @@ __global__ void __launch_bounds__(256) k_generic(const GenericParams p)
             if (n >= p.N)
                 continue;
             const int64_t idx = m * p.ldc + n;
+            if (!in_bounds(n < p.ldc, p.status, SITE_BOUNDS_C))   // (debug-bounds build)
+                continue;
             if (p.out_kind == OUT_FP32)
                 static_cast<float *>(p.C)[idx] = acc[i][j];
             else if (p.out_kind == OUT_BF16)

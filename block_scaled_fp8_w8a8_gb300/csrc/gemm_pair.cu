@@ -169,7 +169,7 @@ __global__ void __launch_bounds__(PairLayout<BN, STAGES, CPW, EB>::kThreads, 1)
             for (int t = pair; ok && t < p.num_tiles; t += num_pairs) {
                 int mb, nb;
                 pair_tile_coords(t, p.num_m_tiles, p.num_n_tiles, mb, nb);
-                const int arow = mb * 256 + 128 * static_cast<int>(rank);
+                const int arow0 = mb * 256 + 128 * static_cast<int>(rank);
                 const int brow = nb * BN + (BN / 2) * static_cast<int>(rank);
                 for (int g = 0; g < p.G; ++g) {
                     if (!wait_bounded(empty_bar(stage), phase ^ 1u, guard,
@@ -177,7 +177,17 @@ __global__ void __launch_bounds__(PairLayout<BN, STAGES, CPW, EB>::kThreads, 1)
                         ok = false;
                         break;
                     }
-                    if (issued != p.debug_skip_tma) {
+                    // Debug-bounds build: each box starts inside its tensor
+                    // padded to whole pair tiles (the ragged tail reads zeros).
+                    const int arow = arow0 + ((W8A8_DEBUG_BOUNDS && issued == 0 &&
+                                               p.debug_skip_tma == kDebugBadFirstLoad)
+                                                  ? (1 << 28)
+                                                  : 0);
+                    const bool in =
+                        in_bounds(arow < p.num_m_tiles * 256 && g * 128 < p.K, p.status,
+                                  SITE_BOUNDS_A) &&
+                        in_bounds(brow < p.num_n_tiles * BN, p.status, SITE_BOUNDS_B);
+                    if (issued != p.debug_skip_tma && in) {
                         mbar_arrive_expect_tx(full_bar(stage), L::kABytes + L::kBBytes);
                         tma_load_2d(sA + stage * L::kABytes, &tmA, full_bar(stage), g * 128, arow);
                         tma_load_2d(sB + stage * L::kBBytes, &tmB, full_bar(stage), g * 128, brow);

@@ -110,7 +110,8 @@ __global__ void __launch_bounds__(kThreads)
 
     auto issue_weights = [&]() {
         for (int g = 0; g < G; ++g) {
-            if (g == p.debug_skip_tma)
+            // (debug-bounds build: a box outside B is skipped like a skipped load)
+            if (g == p.debug_skip_tma || !in_bounds(n0 < p.N && g * 128 < p.K, p.status, SITE_BOUNDS_B))
                 continue;
             mbar_arrive_expect_tx(bar0 + 8u * g, kBoxBytes);
             tma_load_2d(sB + g * kBoxBytes, &tmB, bar0 + 8u * g, g * 128, n0);
@@ -127,7 +128,9 @@ __global__ void __launch_bounds__(kThreads)
     const int chunks = K / 16;
     for (int c = tid; c < M * chunks; c += kThreads) {
         const int m = c / chunks, k0 = (c - m * chunks) * 16;
-        const uint4 v = *reinterpret_cast<const uint4 *>(p.A + static_cast<size_t>(m) * p.lda + k0);
+        const uint4 v = in_bounds(m < p.M && k0 + 16 <= p.K, p.status, SITE_BOUNDS_A)
+                            ? *reinterpret_cast<const uint4 *>(p.A + static_cast<size_t>(m) * p.lda + k0)
+                            : make_uint4(0u, 0u, 0u, 0u);
         float f[16];
         decode16(v, f);
         float4 *dst = reinterpret_cast<float4 *>(sA + static_cast<size_t>(m) * K + k0);
@@ -137,7 +140,10 @@ __global__ void __launch_bounds__(kThreads)
     }
     for (int i = tid; i < M * G; i += kThreads) {
         const int m = i / G, g = i - m * G;
-        sS[m * G + g] = p.a_s[static_cast<size_t>(m) * G + g] * p.b_s[static_cast<size_t>(nb) * G + g];
+        sS[m * G + g] = in_bounds(m < p.M && nb * 128 < p.N, p.status, SITE_BOUNDS_SCALES)
+                            ? p.a_s[static_cast<size_t>(m) * G + g] *
+                                  p.b_s[static_cast<size_t>(nb) * G + g]
+                            : 0.f;
     }
     __syncthreads();
 
@@ -215,7 +221,8 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
         for (int w = 0; w < kWarps; ++w)
             s += sRed[(w * MM + m) * kRows + r];
-        store_out(p.C, static_cast<size_t>(m) * p.ldc + n, s, p.out_kind);
+        if (in_bounds(m < p.M, p.status, SITE_BOUNDS_C))
+            store_out(p.C, static_cast<size_t>(m) * p.ldc + n, s, p.out_kind);
     }
 }
 

@@ -320,8 +320,13 @@ __global__ void __launch_bounds__(SwapLayout<MT>::kThreads, SwapLayout<MT>::kMin
             // Weights do not depend on the previous grid when the caller says so:
             // start the first stages' B loads before waiting for it.
             const int pre = p.prefetch_weights ? min(stages, ng) : 0;
+            // Debug-bounds build: this CTA's weight rows and groups lie inside B.
+            auto w_in = [&](int g) {
+                return in_bounds(nb < p.NB && g < p.G && (!grouped || expert < p.experts), p.status,
+                                 SITE_BOUNDS_B);
+            };
             for (int i = 0; i < pre; ++i) {
-                if (i != p.debug_skip_tma) {
+                if (i != p.debug_skip_tma && w_in(g_begin + i)) {
                     mbar_arrive_expect_tx(full_bar(i), tx);
                     if constexpr (grouped)
                         tma_load_3d(sW + i * L::kWBytes, &tmW, full_bar(i), (g_begin + i) * 128,
@@ -343,7 +348,7 @@ __global__ void __launch_bounds__(SwapLayout<MT>::kThreads, SwapLayout<MT>::kMin
                         ok = false;
                         break;
                     }
-                    if (i != p.debug_skip_tma) {
+                    if (i != p.debug_skip_tma && w_in(g)) {
                         mbar_arrive_expect_tx(full_bar(stage), tx);
                         if constexpr (grouped)
                             tma_load_3d(sW + stage * L::kWBytes, &tmW, full_bar(stage), g * 128,
@@ -353,14 +358,25 @@ __global__ void __launch_bounds__(SwapLayout<MT>::kThreads, SwapLayout<MT>::kMin
                                         nb * 128);
                     }
                 }
-                if (i != p.debug_skip_tma) {
+                // Debug-bounds build: the token box starts inside A (X), padded
+                // to whole token tiles, and inside the expert's slab (the
+                // consumer's wait gives up on a load the check skips).
+                const int mrow = m0 + ((W8A8_DEBUG_BOUNDS && i == 0 &&
+                                        p.debug_skip_tma == kDebugBadFirstLoad)
+                                           ? (1 << 28)
+                                           : 0);
+                const bool in_x = in_bounds(
+                    mrow < (grouped ? p.tiles_per_expert : p.num_m_tiles) * p.mma_n &&
+                        g * 128 < p.K && (!grouped || expert < p.experts),
+                    p.status, SITE_BOUNDS_A);
+                if (i != p.debug_skip_tma && in_x) {
                     if constexpr (FUSED)
-                        tma_load_2d(sXs + stage * xs_bytes, &tmX, full_bar(stage), g * 128, m0);
+                        tma_load_2d(sXs + stage * xs_bytes, &tmX, full_bar(stage), g * 128, mrow);
                     else if constexpr (grouped)
-                        tma_load_3d(sX + stage * L::kXBytes, &tmX, full_bar(stage), g * 128, m0,
+                        tma_load_3d(sX + stage * L::kXBytes, &tmX, full_bar(stage), g * 128, mrow,
                                     expert);
                     else
-                        tma_load_2d(sX + stage * L::kXBytes, &tmX, full_bar(stage), g * 128, m0);
+                        tma_load_2d(sX + stage * L::kXBytes, &tmX, full_bar(stage), g * 128, mrow);
                 }
                 ++issued;
                 if (++stage == stages) {
@@ -577,7 +593,8 @@ __global__ void __launch_bounds__(SwapLayout<MT>::kThreads, SwapLayout<MT>::kMin
             }
             fence_async_smem();
             named_barrier(1, kPromoThreads);
-            if (tid == 0) {
+            if (tid == 0 && in_bounds(nb * 128 < p.N && m0 < p.M && (!grouped || expert < p.experts),
+                                      p.status, SITE_BOUNDS_C)) {
                 if constexpr (grouped)
                     tma_store_3d(&tmC, sW, nb * 128, m0, expert);
                 else
@@ -595,6 +612,12 @@ __global__ void __launch_bounds__(SwapLayout<MT>::kThreads, SwapLayout<MT>::kMin
             for (int j = 0; j < L::kCols; ++j)
                 if (c0 + j < p.mma_n)
                     tile[(c0 + j) * 128 + row] = acc[j];
+        } else if (ok && !in_bounds(blockIdx.z * gridDim.x + blockIdx.x <
+                                            static_cast<unsigned>(p.num_m_tiles * p.NB) &&
+                                        split < p.splits,
+                                    p.status, SITE_BOUNDS_WORKSPACE)) {
+            // Debug-bounds build: the tile's counter or this split's plane lies
+            // outside the workspace; the whole split-K step is skipped.
         } else if (ok && p.atomic_reduce) {
             // Non-deterministic split-K (the page's atomic form): add this
             // split's partial into the one fp32 plane (zeroed on the stream
@@ -623,8 +646,10 @@ __global__ void __launch_bounds__(SwapLayout<MT>::kThreads, SwapLayout<MT>::kMin
                     const int r = it / c4n, c4 = it - r * c4n;
                     const float4 sum = __ldcg(reinterpret_cast<const float4 *>(
                         p.ws + static_cast<size_t>(m0 + r) * p.N + nb * 128 + 4 * c4));
-                    store4(p.C, static_cast<size_t>(m0 + r) * p.ldc + nb * 128 + 4 * c4, sum,
-                           p.out_kind);
+                    if (in_bounds(m0 + r < p.M && nb * 128 + 4 * c4 + 4 <= p.N, p.status,
+                                  SITE_BOUNDS_C))
+                        store4(p.C, static_cast<size_t>(m0 + r) * p.ldc + nb * 128 + 4 * c4, sum,
+                               p.out_kind);
                 }
                 if (tid == 0)
                     p.counters[tile] = 0u;   // ready for the next call
@@ -674,8 +699,10 @@ __global__ void __launch_bounds__(SwapLayout<MT>::kThreads, SwapLayout<MT>::kMin
                     }
                     for (; s < p.splits; ++s)
                         add4(sum, __ldcg(reinterpret_cast<const float4 *>(src + s * plane)));
-                    store4(p.C, static_cast<size_t>(m0 + r) * p.ldc + nb * 128 + 4 * c4, sum,
-                           p.out_kind);
+                    if (in_bounds(m0 + r < p.M && nb * 128 + 4 * c4 + 4 <= p.N, p.status,
+                                  SITE_BOUNDS_C))
+                        store4(p.C, static_cast<size_t>(m0 + r) * p.ldc + nb * 128 + 4 * c4, sum,
+                               p.out_kind);
                 }
                 if (tid == 0)
                     p.counters[tile] = 0u;   // ready for the next call
@@ -713,8 +740,11 @@ __global__ void __launch_bounds__(SwapLayout<MT>::kThreads, SwapLayout<MT>::kMin
                          : "r"(tile + static_cast<uint32_t>(r * 128 + 4 * c4) * 4u));
             const uint32_t dst = recv0 + static_cast<uint32_t>(((static_cast<int>(rank) * slot_rows +
                                                                 (r - r_own0)) * 128 + 4 * c4) * 4);
-            st_async_v4(cluster_map(dst, static_cast<uint32_t>(owner)), v,
-                        cluster_map(recv_bar, static_cast<uint32_t>(owner)));
+            if (in_bounds(owner >= 0 && owner < S && r - r_own0 >= 0 && r - r_own0 < slot_rows &&
+                              static_cast<int>(rank) < S,
+                          p.status, SITE_BOUNDS_SMEM))
+                st_async_v4(cluster_map(dst, static_cast<uint32_t>(owner)), v,
+                            cluster_map(recv_bar, static_cast<uint32_t>(owner)));
         }
         const int r0 = rows * static_cast<int>(rank) / S;
         const int r1 = rows * (static_cast<int>(rank) + 1) / S;
@@ -733,7 +763,10 @@ __global__ void __launch_bounds__(SwapLayout<MT>::kThreads, SwapLayout<MT>::kMin
                 for (int s2 = 0; s2 < S; ++s2)
                     add4(sum, *reinterpret_cast<const float4 *>(
                                   recv + (static_cast<size_t>(s2 * slot_rows + rl) * 128 + 4 * c4)));
-                store4(p.C, (c_row0 + r0 + rl) * p.ldc + nb * 128 + 4 * c4, sum, p.out_kind);
+                if (in_bounds(m0 + r0 + rl < p.M && nb * 128 + 4 * c4 + 4 <= p.N &&
+                                  (!grouped || expert < p.experts),
+                              p.status, SITE_BOUNDS_C))
+                    store4(p.C, (c_row0 + r0 + rl) * p.ldc + nb * 128 + 4 * c4, sum, p.out_kind);
             }
         }
     }

@@ -176,6 +176,12 @@ __device__ __forceinline__ bool stream_k_fixup(const TiledParams &p, uint64_t (&
     const int s0 = (t - p.sk_first_tile) * p.G;
     const int c_first = s0 / len;
     const int c_last = (s0 + p.G - 1) / len;
+    // Debug-bounds build: the contributors' slots and the tile's counter lie
+    // inside the workspace (the same for every promotion thread, so all skip).
+    if (!in_bounds(c_first >= 0 && c_last < static_cast<int>(gridDim.x) && t >= 0 &&
+                       t < static_cast<int>(kCounterWords),
+                   p.status, SITE_BOUNDS_WORKSPACE))
+        return false;
     // Slot of CTA c for this tile: 0 if its range starts in tile t, else 1.
     auto slot = [&](int c) {
         const int first_tile = p.sk_first_tile + c * len / p.G;
@@ -343,22 +349,37 @@ __global__ void __launch_bounds__(TiledLayout<BN, STAGES, CPW, EB>::kThreads, 1)
                         ok = false;
                         break;
                     }
-                    if (issued != p.debug_skip_tma && HALVES) {
+                    // Rows of A and B this stage loads (a half item's B rows
+                    // start at its column half); the debug-bounds build checks
+                    // that each box starts inside its tensor padded to whole
+                    // tiles (the ragged tail reads TMA's zero fill; a load the
+                    // check skips ends like a skipped one: the consumer's wait
+                    // gives up).
+                    const int arow = mb * 128 + ((W8A8_DEBUG_BOUNDS && issued == 0 &&
+                                                  p.debug_skip_tma == kDebugBadFirstLoad)
+                                                     ? (1 << 28)
+                                                     : 0);
+                    const int brow = nb * BN + (walk.half() && walk.hv > 0 ? BN / 2 : 0);
+                    const bool in =
+                        in_bounds(arow < p.num_m_tiles * 128 && g * 128 < p.K, p.status,
+                                  SITE_BOUNDS_A) &&
+                        in_bounds(brow < p.num_n_tiles * BN && (!p.m_indices || e < p.experts),
+                                  p.status, SITE_BOUNDS_B);
+                    if (issued != p.debug_skip_tma && in && HALVES) {
                         // The half-tail instance's B map has boxes of BN/2 rows:
                         // two per whole tile, one (the item's column half) per
                         // half item, which the MMA reads from the stage's start.
                         const bool hf = walk.half();
                         mbar_arrive_expect_tx(full_bar(stage),
                                               L::kABytes + (hf ? L::kBBytes / 2 : L::kBBytes));
-                        tma_load_2d(sA + stage * L::kABytes, &tmA, full_bar(stage), g * 128, mb * 128);
-                        const int brow = nb * BN + (hf && walk.hv > 0 ? BN / 2 : 0);
+                        tma_load_2d(sA + stage * L::kABytes, &tmA, full_bar(stage), g * 128, arow);
                         tma_load_2d(sB + stage * L::kBBytes, &tmB, full_bar(stage), g * 128, brow);
                         if (!hf)
                             tma_load_2d(sB + stage * L::kBBytes + L::kBBytes / 2, &tmB,
                                         full_bar(stage), g * 128, brow + BN / 2);
-                    } else if (issued != p.debug_skip_tma) {
+                    } else if (issued != p.debug_skip_tma && in) {
                         mbar_arrive_expect_tx(full_bar(stage), L::kABytes + L::kBBytes);
-                        tma_load_2d(sA + stage * L::kABytes, &tmA, full_bar(stage), g * 128, mb * 128);
+                        tma_load_2d(sA + stage * L::kABytes, &tmA, full_bar(stage), g * 128, arow);
                         if (p.m_indices)
                             tma_load_3d(sB + stage * L::kBBytes, &tmB, full_bar(stage), g * 128,
                                         nb * BN, e);

@@ -5,6 +5,13 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+// 1 in the debug-bounds build (-DW8A8_DEBUG_BOUNDS=1): the kernels check their
+// global-memory and TMA indexes and record W8A8_ERR_DEVICE_BOUNDS instead of
+// an access outside a buffer.
+#ifndef W8A8_DEBUG_BOUNDS
+#define W8A8_DEBUG_BOUNDS 0
+#endif
+
 namespace w8a8 {
 
 enum OutKind : int { OUT_BF16 = 0, OUT_FP16 = 1, OUT_FP32 = 2 };
@@ -24,7 +31,20 @@ enum WaitSite : uint32_t {
     SITE_SMALL_WEIGHTS = 11,
     SITE_SWAP_QUANT = 12,
     SITE_PAIR_PEER = 13,   // CTA-pair kernel: waiting for the other CTA's stage
+    // Access sites of the debug-bounds build's checks (status W8A8_ERR_DEVICE_BOUNDS).
+    SITE_BOUNDS_A = 20,          // a TMA box or a load of A (or X) that starts outside it
+    SITE_BOUNDS_B = 21,          // the same for B
+    SITE_BOUNDS_C = 22,          // a store into C outside it
+    SITE_BOUNDS_SCALES = 23,     // a load of a_s or b_s outside it
+    SITE_BOUNDS_WORKSPACE = 24,  // split-K / stream-K workspace or arrival counters
+    SITE_BOUNDS_SMEM = 25,       // shared memory or another CTA's receive area
 };
+
+// Test hook of the debug-bounds build carried in the kernels' debug_skip_tma
+// field: a value of kDebugBadFirstLoad asks the TMA producer to move its first
+// load of A far outside A (the bounds check must catch it).  Release builds
+// never set it.
+constexpr int kDebugBadFirstLoad = -2;
 
 // Split-K / stream-K workspace layout (the library's, the caller's or the
 // allocation-free entry point's fixed array): a block of kCounterWords per-tile
@@ -160,6 +180,7 @@ struct GenericParams {
     int64_t lda, ldb, ldc, ld_as, ld_bs;
     int64_t block_n, block_k;
     int out_kind;
+    unsigned *status;      // the debug-bounds build's checks record here
 };
 cudaError_t launch_generic(const GenericParams &p, const LaunchCfg &cfg);
 

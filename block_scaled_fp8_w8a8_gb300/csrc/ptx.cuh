@@ -61,6 +61,31 @@ __device__ __forceinline__ bool named_barrier_and(uint32_t id, uint32_t count, b
     return r != 0;
 }
 
+// ------------------------------------------------------------------ debug-bounds checks
+
+#ifndef W8A8_DEBUG_BOUNDS
+#define W8A8_DEBUG_BOUNDS 0
+#endif
+
+// In the debug-bounds build (-DW8A8_DEBUG_BOUNDS=1) an access's index is
+// checked against its buffer before the access: when it is outside, the check
+// records (site << 8) | 7 -- 7 is W8A8_ERR_DEVICE_BOUNDS -- in the device status
+// word unless an earlier error is there, and returns false so that the caller
+// skips the access.  The release build compiles the check to `true`.
+__device__ __forceinline__ bool in_bounds(bool ok, unsigned *status, uint32_t site)
+{
+#if W8A8_DEBUG_BOUNDS
+    if (!ok)
+        atomicCAS(status, 0u, (site << 8) | 7u);
+    return ok;
+#else
+    (void)ok;
+    (void)status;
+    (void)site;
+    return true;
+#endif
+}
+
 // ------------------------------------------------------------------ mbarrier
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)

@@ -48,7 +48,8 @@ template <int KIND> struct InFormat {
 template <int KIND>
 __global__ void __launch_bounds__(kThreads, 3)
     k_quant_group128(const void *__restrict__ X, uint8_t *__restrict__ A,
-                     float *__restrict__ a_s, unsigned M, unsigned K, unsigned G)
+                     float *__restrict__ a_s, unsigned M, unsigned K, unsigned G,
+                     unsigned *status)
 {
     constexpr int kW = InFormat<KIND>::kWords, kU = InFormat<KIND>::kUnroll;
     constexpr int kEsize = KIND == W8A8_IN_FP32 ? 4 : 2;
@@ -80,6 +81,9 @@ __global__ void __launch_bounds__(kThreads, 3)
             grp[j] = gj;
             const unsigned k = gj * 128 + 16 * lane8;
             in[j] = live[j] && k < K;                          // K % 16 == 0: whole chunks
+            // (debug-bounds build: the row and the 16 columns lie inside X and A)
+            if (in[j] && !in_bounds(mj < M && k + 16 <= K, status, SITE_BOUNDS_A))
+                in[j] = false;
             if (in[j]) {
                 const uint4 *src = reinterpret_cast<const uint4 *>(
                     static_cast<const uint8_t *>(X) + (static_cast<size_t>(mj) * K + k) * kEsize);
@@ -108,7 +112,8 @@ __global__ void __launch_bounds__(kThreads, 3)
                 const size_t idx = static_cast<size_t>(row[j]) * K + grp[j] * 128 + 16 * lane8;
                 *reinterpret_cast<uint4 *>(A + idx) = quant::encode16<KIND>(w[j], s);
             }
-            if (live[j] && lane8 == 0)
+            if (live[j] && lane8 == 0 &&
+                in_bounds(row[j] < M && grp[j] < G, status, SITE_BOUNDS_SCALES))
                 a_s[static_cast<size_t>(row[j]) * G + grp[j]] = s;
         }
         m += stride_m;
@@ -148,7 +153,7 @@ extern "C" w8a8_status w8a8_quantize_fp8_per_token_group(const void *X_dev, w8a8
         return record_error(W8A8_ERR_UNSUPPORTED, "X and A must be 16-byte aligned, a_s 4-byte");
     const int G = static_cast<int>((K + 127) / 128);
     const long long units = M * static_cast<long long>(G);
-    void (*kernel)(const void *, uint8_t *, float *, unsigned, unsigned, unsigned) =
+    void (*kernel)(const void *, uint8_t *, float *, unsigned, unsigned, unsigned, unsigned *) =
         x_dtype == W8A8_IN_BF16   ? k_quant_group128<W8A8_IN_BF16>
         : x_dtype == W8A8_IN_FP16 ? k_quant_group128<W8A8_IN_FP16>
                                   : k_quant_group128<W8A8_IN_FP32>;
@@ -179,9 +184,14 @@ extern "C" w8a8_status w8a8_quantize_fp8_per_token_group(const void *X_dev, w8a8
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     lc.attrs = attr;
     lc.numAttrs = 1;
+    // The debug-bounds build's checks record into the device status word; the
+    // release build compiles them away and passes no address.
+    unsigned *status = nullptr;
+    if (W8A8_DEBUG_BOUNDS && status_word_address(&status) != cudaSuccess)
+        status = nullptr;
     e = cudaLaunchKernelEx(&lc, kernel, X_dev, static_cast<uint8_t *>(A_dev), a_s_dev,
                            static_cast<unsigned>(M), static_cast<unsigned>(K),
-                           static_cast<unsigned>(G));
+                           static_cast<unsigned>(G), status);
     if (e != cudaSuccess) {
         char msg[256];
         snprintf(msg, sizeof(msg), "kernel launch: %s", cudaGetErrorString(e));

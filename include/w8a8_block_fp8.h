@@ -70,7 +70,9 @@ typedef enum {
     W8A8_ERR_CUDA = 3,            /* a CUDA runtime/driver call failed               */
     W8A8_ERR_DEVICE_TIMEOUT = 4,  /* a bounded device-side wait ran out              */
     W8A8_ERR_WORKSPACE = 5,       /* caller workspace too small / misaligned         */
-    W8A8_ERR_NO_DEVICE = 6        /* no usable sm_100-family device is current       */
+    W8A8_ERR_NO_DEVICE = 6,       /* no usable sm_100-family device is current       */
+    W8A8_ERR_DEVICE_BOUNDS = 7    /* debug-bounds build only: a kernel found an index
+                                     outside its buffer and skipped the access          */
 } w8a8_status;
 
 typedef enum { W8A8_OUT_BF16 = 0, W8A8_OUT_FP16 = 1, W8A8_OUT_FP32 = 2 } w8a8_out_dtype;
@@ -147,6 +149,13 @@ typedef enum {
  *                      additions is the order the splits arrive in); the
  *                      workspace holds one plane instead of split_k.  0 = the
  *                      ordered, bit-reproducible reduction.
+ *   debug_bad_index    test hook of the debug-bounds build (w8a8_debug_bounds_build()
+ *                      returns 1): 1 = the TMA producer of the tensor-core kernels
+ *                      moves the first A load of the call far outside A, so that
+ *                      the build's bounds check records W8A8_ERR_DEVICE_BOUNDS in
+ *                      the status word and skips the load (its consumer's bounded
+ *                      wait then gives up and the kernel drains as after any
+ *                      timeout).  Ignored by release builds.  0 = off.
  *   workspace_dev      SPLITK and stream-K TILED: caller-owned device scratch of workspace_bytes
  *                      bytes, 256-byte aligned, at least
  *                      w8a8_block_fp8_workspace_size() bytes, all zero before its
@@ -159,7 +168,20 @@ typedef enum {
  *                      capture (W8A8_ERR_WORKSPACE: call once before capturing,
  *                      or pass a workspace).
  *   wait_limit_cycles  bound of every device-side wait in SM clock cycles
- *                      (0 = 2^32 cycles, about 2 s)
+ *                      (0 = the default: W8A8_WAIT_LIMIT_CYCLES from the
+ *                      environment, else 2^32 cycles, about 2 s); at least
+ *                      100000 (a shorter bound could give up on copies still in
+ *                      flight when a kernel drains): else W8A8_ERR_INVALID_ARG
+ *
+ * Environment (read once, at the library's first call; a value that does not
+ * parse makes every call fail with W8A8_ERR_INVALID_ARG and a message):
+ *   W8A8_FORCE_VARIANT      a variant for calls whose options leave it AUTO:
+ *                           tiled, swapab, splitk, splitk_cluster, smallm,
+ *                           tiled_pair, generic, or its number
+ *   W8A8_DETERMINISTIC      1: splitk_atomic requests run the ordered reduction
+ *   W8A8_WAIT_LIMIT_CYCLES  default wait_limit_cycles (at least 100000)
+ *   W8A8_DEBUG_BOUNDS       1: the Python binding loads the debug-bounds build
+ *                           (the C library itself is one build or the other)
  */
 typedef struct {
     int variant;
@@ -173,7 +195,7 @@ typedef struct {
     int weights_static;
     int debug_fail_alloc;
     int splitk_atomic;
-    int reserved_i;
+    int debug_bad_index;
     void *workspace_dev;
     size_t workspace_bytes;
     unsigned long long wait_limit_cycles;
@@ -453,8 +475,10 @@ w8a8_status w8a8_block_fp8_plan(int64_t M, int64_t N, int64_t K, w8a8_out_dtype 
 /*
  * Synchronises the current device, then reads and clears its device status
  * word.  W8A8_OK when no device-side wait has run out since the last read;
- * otherwise W8A8_ERR_DEVICE_TIMEOUT, with *detail_out (if not NULL) set to the
- * raw status word (low byte: status; next byte: the wait site).
+ * otherwise W8A8_ERR_DEVICE_TIMEOUT (or, in the debug-bounds build,
+ * W8A8_ERR_DEVICE_BOUNDS when a bounds check fired first), with *detail_out
+ * (if not NULL) set to the raw status word (low byte: status; next byte: the
+ * wait or access site).
  */
 w8a8_status w8a8_get_device_status(unsigned *detail_out);
 
@@ -466,6 +490,20 @@ const char *w8a8_last_error(void);
 
 /* W8A8_ABI_VERSION of the loaded library. */
 int w8a8_abi_version(void);
+
+/* 1 if this library is the debug-bounds build: every kernel checks the
+ * indexes of its global-memory and TMA accesses against their buffers and,
+ * instead of an access outside one, records W8A8_ERR_DEVICE_BOUNDS (with the
+ * access's site in bits 8..15) in the device status word and skips it.
+ * 0 for the release build, which compiles the checks away. */
+int w8a8_debug_bounds_build(void);
+
+/* The environment settings above as this library parsed them: the forced
+ * variant (0 = none), the deterministic flag and the default wait bound.
+ * W8A8_ERR_INVALID_ARG (with the offending variable in w8a8_last_error())
+ * when one does not parse.  Needs no device. */
+w8a8_status w8a8_env_config(int *force_variant, int *deterministic,
+                            unsigned long long *wait_limit_cycles);
 
 /* Releases the library's cached split-K workspaces (every device) and forgets
  * the allocation-free entry point's per-device set-up, so that its next call
