@@ -49,8 +49,8 @@ template <int MT> struct SwapLayout {
     static constexpr uint32_t kTmemCols = kBufs * MT < 32 ? 32 : kBufs * MT;
     static constexpr int kMaxIssuers = 3;
     // full/empty per stage, tfull/tempty per TMEM buffer, one drain barrier
-    // per MMA issuer, the cluster receive barrier
-    static constexpr int kBars = 2 * kMaxStages + 2 * kBufs + kMaxIssuers + 1;
+    // per MMA issuer, the cluster receive and acknowledge barriers
+    static constexpr int kBars = 2 * kMaxStages + 2 * kBufs + kMaxIssuers + 2;
     // Operand stages; after the main loop the same bytes hold the C tile.
     // Fused activation quantisation adds, per stage, the unquantised token
     // tile as the TMA brings it: MT rows of 128 elements of x_esize bytes.
@@ -218,6 +218,7 @@ __global__ void __launch_bounds__(SwapLayout<MT>::kThreads, SwapLayout<MT>::kMin
     auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * kMaxStages + L::kBufs + b); };
     auto drain_bar = [&](int w) { return bar0 + 8u * (2 * kMaxStages + 2 * L::kBufs + w); };
     const uint32_t recv_bar = bar0 + 8u * (2 * kMaxStages + 2 * L::kBufs + L::kMaxIssuers);
+    const uint32_t ack_bar = recv_bar + 8u;     // cluster split-K: every owner has this CTA's rows
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + L::kBars);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     volatile int *last_flag = reinterpret_cast<volatile int *>(tmem_slot + 2);
@@ -253,8 +254,10 @@ __global__ void __launch_bounds__(SwapLayout<MT>::kThreads, SwapLayout<MT>::kMin
         }
         for (int w = 0; w < L::kMaxIssuers; ++w)
             mbar_init(drain_bar(w), 1);
-        if (p.cluster_reduce)
+        if (p.cluster_reduce) {
             mbar_init(recv_bar, 1);
+            mbar_init(ack_bar, static_cast<uint32_t>(p.splits));
+        }
         if constexpr (FUSED)
             for (int i = 0; i < p.groups_per_split; ++i)
                 mbar_init(ready_bar(i), 2);
@@ -712,15 +715,19 @@ __global__ void __launch_bounds__(SwapLayout<MT>::kThreads, SwapLayout<MT>::kMin
 
     if (p.cluster_reduce && warp >= 4) {
         // Cluster split-K.  The splits of a tile form one cluster; the CTA of
-        // cluster rank r reduces rows [r0, r1) of the tile.  Every split pushes
-        // each row of its partial tile (in shared memory since the promotion)
-        // into the receive area of that row's owner with asynchronous 16-byte
-        // stores counted on the owner's receive barrier; each owner waits for
-        // its barrier, sums the splits' rows in split order 0..S-1 (the same
-        // order, and so the same bits, as the workspace reduction) and stores
-        // them.  No CTA reads another's shared memory, and a CTA leaves only
-        // after everything pushed into it has landed.  (After a timeout the
-        // pushed rows are garbage and the status word already says so.)
+        // cluster rank r reduces rows [r0, r1) of the tile.  Every split sends
+        // the rows each owner reduces -- contiguous in its partial tile (in
+        // shared memory since the promotion) and in the owner's receive slot
+        // for this split -- with one bulk copy per owner, counted on the
+        // owner's receive barrier.  (16-byte asynchronous stores, one per
+        // thread and column quad, measured ~0.8 us per launch to issue: about
+        // three cycles each.)  Each owner waits for its barrier, sums the
+        // splits' rows in split order 0..S-1 (the same order, and so the same
+        // bits, as the workspace reduction) and stores them.  A copy reads its
+        // source until it lands, so each owner, once everything sent to it has
+        // landed, acknowledges every sender, and a CTA leaves only after every
+        // owner's acknowledgement.  (After a timeout the rows are garbage and
+        // the status word already says so.)
         uint32_t rank;
         asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(rank));
         const int tid = static_cast<int>(threadIdx.x) - 128;
@@ -728,23 +735,19 @@ __global__ void __launch_bounds__(SwapLayout<MT>::kThreads, SwapLayout<MT>::kMin
         const int S = p.splits;
         const int rows = grouped ? *rows_slot : min(p.mma_n, p.M - m0);
         const int slot_rows = L::recv_slot_rows(S);
+        fence_async_smem();                           // the partial tile, for the copies
         named_barrier(1, kPromoThreads);              // the whole partial tile is written
         const uint32_t tile = smem_addr(smem);
-        for (int it = tid; it < rows * 32; it += kPromoThreads) {
-            const int r = it >> 5, c4 = it & 31;
-            const int owner = (S * (r + 1) - 1) / rows;
-            const int r_own0 = rows * owner / S;
-            float4 v;
-            asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-                         : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-                         : "r"(tile + static_cast<uint32_t>(r * 128 + 4 * c4) * 4u));
-            const uint32_t dst = recv0 + static_cast<uint32_t>(((static_cast<int>(rank) * slot_rows +
-                                                                (r - r_own0)) * 128 + 4 * c4) * 4);
-            if (in_bounds(owner >= 0 && owner < S && r - r_own0 >= 0 && r - r_own0 < slot_rows &&
-                              static_cast<int>(rank) < S,
-                          p.status, SITE_BOUNDS_SMEM))
-                st_async_v4(cluster_map(dst, static_cast<uint32_t>(owner)), v,
-                            cluster_map(recv_bar, static_cast<uint32_t>(owner)));
+        if (tid < S) {
+            const int o = tid;                        // owner of rows [ra, rb)
+            const int ra = rows * o / S, rb = rows * (o + 1) / S;
+            const uint32_t dst = recv0 + static_cast<uint32_t>(static_cast<int>(rank) * slot_rows) * 512u;
+            if (rb > ra && in_bounds(rb - ra <= slot_rows && static_cast<int>(rank) < S, p.status,
+                                     SITE_BOUNDS_SMEM))
+                bulk_copy_to_cluster(cluster_map(dst, static_cast<uint32_t>(o)),
+                                     tile + static_cast<uint32_t>(ra) * 512u,
+                                     static_cast<uint32_t>(rb - ra) * 512u,
+                                     cluster_map(recv_bar, static_cast<uint32_t>(o)));
         }
         const int r0 = rows * static_cast<int>(rank) / S;
         const int r1 = rows * (static_cast<int>(rank) + 1) / S;
@@ -752,6 +755,10 @@ __global__ void __launch_bounds__(SwapLayout<MT>::kThreads, SwapLayout<MT>::kMin
             mbar_arrive_expect_tx(recv_bar, static_cast<uint32_t>(S * (r1 - r0) * 128 * 4));
         const bool got = __all_sync(0xffffffffu,
                                     wait_bounded_cluster(recv_bar, 0, guard, SITE_SWAP_PROMOTE));
+        // everything sent here has landed: its senders may release their tiles
+        named_barrier(1, kPromoThreads);
+        if (tid < S)
+            mbar_arrive_remote(cluster_map(ack_bar, static_cast<uint32_t>(tid)));
         if (got) {
             const size_t c_row0 = static_cast<size_t>(expert) * p.M + m0;
             const int c4n = min(128, p.N - nb * 128) / 4;
@@ -769,6 +776,8 @@ __global__ void __launch_bounds__(SwapLayout<MT>::kThreads, SwapLayout<MT>::kMin
                     store4(p.C, (c_row0 + r0 + rl) * p.ldc + nb * 128 + 4 * c4, sum, p.out_kind);
             }
         }
+        // every owner has this CTA's rows (so its copies have read the tile)
+        __all_sync(0xffffffffu, wait_bounded_cluster(ack_bar, 0, guard, SITE_SWAP_PROMOTE));
     }
 
     tc_fence_before_sync();

@@ -481,6 +481,21 @@ __device__ __forceinline__ void st_async_v4(uint32_t caddr, float4 v, uint32_t c
                  : "memory");
 }
 
+// Bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned) from
+// this CTA's shared memory into another CTA's of the cluster (`dst_caddr` and
+// its barrier `mbar_caddr` in the cluster's shared window); the bytes count as
+// completed transaction bytes on that barrier.  The source must stay unchanged
+// until the copy has landed, and it is read through the async proxy (the
+// writers' fence.proxy.async comes first).
+__device__ __forceinline__ void bulk_copy_to_cluster(uint32_t dst_caddr, uint32_t src_saddr,
+                                                     uint32_t bytes, uint32_t mbar_caddr)
+{
+    asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes"
+                 " [%0], [%1], %2, [%3];" ::"r"(dst_caddr),
+                 "r"(src_saddr), "r"(bytes), "r"(mbar_caddr)
+                 : "memory");
+}
+
 // Bounded wait with acquire at cluster scope, for a barrier completed by
 // other CTAs of the cluster (st.async transaction bytes).
 __device__ __forceinline__ bool wait_bounded_cluster(uint32_t bar, uint32_t parity,
