@@ -267,11 +267,13 @@ def test_splitk_workspace_reused_across_shapes():
 
 @pytest.mark.parametrize("M,N,K,splits", [(16, 512, 4096, 8), (64, 512, 4096, 4), (158, 512, 4096, 8),
                                           (7, 144, 384, 3), (300, 256, 2048, 2), (1, 8192, 1024, 2),
-                                          (70, 512, 4096, 16)])
+                                          (70, 512, 4096, 16), (3, 512, 4096, 16),
+                                          (17, 256, 2048, 16)])
 def test_cluster_splitk_matches_oracle_and_workspace_variant(M, N, K, splits):
     """The cluster split-K (partials reduced through distributed shared memory)
     agrees with the oracle, and bit for bit with the workspace split-K of the same
-    split count (both sum the splits in order 0..S-1)."""
+    split count (both sum the splits in order 0..S-1).  Includes tiles with
+    fewer rows than splits (owners that receive nothing) and a one-row last tile."""
     x = synth.make_inputs(M, N, K, seed=M * 7 + splits, outlier_p=1e-3)
     ref = oracle.reference_c(x.A, x.a_s, x.B, x.b_s)
     for out in ("fp32", "bf16"):
