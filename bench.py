@@ -170,6 +170,9 @@ MEASURED_TRAFFIC = {
 }
 
 
+HBM_NOMINAL_GBS = 7900.0   # GB300 HBM3e, nominal
+
+
 def peaks():
     """(HBM GB/s, bf16 TFLOP/s burst, bf16 TFLOP/s sustained, 'measured'|'fallback')."""
     try:
@@ -436,7 +439,9 @@ def roofline_of(d, bound, out_bytes, hbm, bf16, bf16_sus, peak_kind):
     r = {"bound": bound}
     if bound == "hbm":
         r.update(achieved=d["gbs"], peak=hbm, unit="GB/s", frac=round(d["gbs"] / hbm, 4),
-                 peak_source=f"{peak_kind} HBM copy rate")
+                 peak_source=f"{peak_kind} HBM copy rate",
+                 peak_nominal=HBM_NOMINAL_GBS, frac_nominal=round(d["gbs"] / HBM_NOMINAL_GBS, 4),
+                 peak_nominal_source="the HBM3e interface's nominal rate")
     else:
         fp8, fp8_sus = 2.0 * bf16, 2.0 * bf16_sus
         r.update(achieved=d["tflops"], peak=fp8, unit="TFLOP/s", frac=round(d["tflops"] / fp8, 4),
