@@ -1300,9 +1300,11 @@ w8a8_status w8a8_block_fp8_matmul_host(const void *A_host, const float *a_s_host
         segs.dst[i] = static_cast<uint8_t *>(copies[i].dst);
         segs.bytes[i] = copies[i].n;
     }
+    // The gather follows the caller's work under programmatic dependent launch
+    // only when the caller asks for it (opts->pdl).
     if (mapped) {
         segs.count = 4;
-        const cudaError_t e = launch_gather(segs, 2 * info.sm_count, s);
+        const cudaError_t e = launch_gather(segs, 2 * info.sm_count, s, opts && opts->pdl);
         if (e != cudaSuccess)
             return cuda_fail(e, "gather of the host inputs");
     } else {
@@ -1312,8 +1314,19 @@ w8a8_status w8a8_block_fp8_matmul_host(const void *A_host, const float *a_s_host
                 return cuda_fail(e, "cudaMemcpyAsync(host to device)");
         }
     }
+    // Inside the call the three launches are chained by programmatic dependent
+    // launch: each waits for its predecessor before its first access, so the
+    // chain is ordered as with plain launches, and each one's launch and
+    // prologue overlap the previous kernel.  The staged B is written by this
+    // call's gather, so the matmul never streams weights before its dependency
+    // wait, whatever the caller's weights_static says.  After cudaMemcpyAsync
+    // copies the matmul launches as the caller asked.
+    w8a8_options chained = opts ? *opts : w8a8_options{};
+    chained.weights_static = 0;
+    if (mapped)
+        chained.pdl = 1;
     st = run(dA, reinterpret_cast<const float *>(das), dB, reinterpret_cast<const float *>(dbs),
-             dC, M, N, K, block_n, block_k, out_dtype, s, opts);
+             dC, M, N, K, block_n, block_k, out_dtype, s, &chained);
     if (st != W8A8_OK)
         return st;
     // The result goes back by one kernel writing the host buffer wherever the
@@ -1338,7 +1351,7 @@ w8a8_status w8a8_block_fp8_matmul_host(const void *A_host, const float *a_s_host
         out_seg.dst[0] = static_cast<uint8_t *>(c_dev);
         out_seg.bytes[0] = cbytes;
         out_seg.count = 1;
-        e = launch_gather(out_seg, 2 * info.sm_count, s);
+        e = launch_gather(out_seg, 2 * info.sm_count, s, 1);
     } else {
         e = cudaMemcpyAsync(C_host, dC, cbytes, cudaMemcpyDeviceToHost, s);
     }

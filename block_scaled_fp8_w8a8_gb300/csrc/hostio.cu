@@ -6,14 +6,20 @@
 #include <cstdint>
 
 #include "kernels.cuh"
+#include "ptx.cuh"
 
 namespace w8a8 {
 namespace {
 
 // 16-byte loads where source and destination allow them, then the tail (or a
-// whole misaligned segment) byte by byte; grid-stride over each segment.
+// whole misaligned segment) byte by byte; grid-stride over each segment.  Under
+// programmatic dependent launch the copy starts once the previous grid has
+// finished and its writes are visible (a no-op without it), and the next grid
+// may start its prologue as soon as every block of this one is running.
 __global__ void __launch_bounds__(256) k_gather(const GatherSegs g)
 {
+    grid_dependency_wait();
+    grid_launch_dependents();
     const size_t tid = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
     for (int i = 0; i < g.count; ++i) {
@@ -31,10 +37,19 @@ __global__ void __launch_bounds__(256) k_gather(const GatherSegs g)
 
 }  // namespace
 
-cudaError_t launch_gather(const GatherSegs &segs, int grid, cudaStream_t stream)
+cudaError_t launch_gather(const GatherSegs &segs, int grid, cudaStream_t stream, int pdl)
 {
-    k_gather<<<grid, 256, 0, stream>>>(segs);
-    return cudaGetLastError();
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = dim3(static_cast<unsigned>(grid));
+    lc.blockDim = dim3(256);
+    lc.dynamicSmemBytes = 0;
+    lc.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    lc.attrs = attr;
+    lc.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&lc, k_gather, segs);
 }
 
 }  // namespace w8a8

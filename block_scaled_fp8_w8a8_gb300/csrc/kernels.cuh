@@ -140,7 +140,9 @@ struct GatherSegs {
     size_t bytes[4];
     int count;
 };
-cudaError_t launch_gather(const GatherSegs &segs, int grid, cudaStream_t stream);
+// pdl = 1: launched with programmatic dependent launch; the kernel waits for
+// the previous grid before its first access and lets the next one start early.
+cudaError_t launch_gather(const GatherSegs &segs, int grid, cudaStream_t stream, int pdl);
 
 struct LaunchCfg {
     int stages;

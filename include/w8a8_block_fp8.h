@@ -263,6 +263,13 @@ w8a8_status w8a8_block_fp8_matmul_strided(const void *A_dev, int64_t lda, const 
  * cudaMemcpyAsync.  Either way the write happens after the call has returned:
  * keep C_host allocated and synchronise `stream` before reading it.
  *
+ * Ordering.  With page-locked inputs the call's three kernels (gather, matmul,
+ * write-back) are chained by programmatic dependent launch: each waits for
+ * its predecessor before touching memory, so they run in order while their
+ * launches overlap.  opts->pdl decides only whether the gather may overlap the
+ * caller's previous kernel on `stream`; opts->weights_static is ignored (the
+ * staged weights are written by the call itself).
+ *
  * With page-locked buffers the call can be captured in a CUDA graph (every
  * replay then moves the buffers' current contents).  staging_dev is
  * caller-owned device memory of at least

@@ -228,6 +228,45 @@ def test_host_buffer_call_pageable_inputs_reusable_on_return():
     assert torch.equal(C_host.view(torch.int16), dev.cpu().view(torch.int16))
 
 
+HOST_CHAIN = [("tiled", 300, 520, 384, dict(variant=w8.W8A8_VARIANT_TILED)),
+              ("swapab", 100, 1024, 256, dict(variant=w8.W8A8_VARIANT_SWAPAB)),
+              ("cluster", 40, 512, 2048, dict(variant=w8.W8A8_VARIANT_SPLITK_CLUSTER, split_k=4)),
+              ("splitk_atomic", 40, 512, 2048, dict(variant=w8.W8A8_VARIANT_SPLITK, split_k=4,
+                                                    splitk_atomic=1)),
+              ("smallm", 3, 512, 384, dict(variant=w8.W8A8_VARIANT_SMALLM)),
+              ("generic", 33, 104, 256, dict(variant=w8.W8A8_VARIANT_GENERIC))]
+
+
+@pytest.mark.parametrize("pdl", [0, 1])
+def test_host_buffer_calls_chained_on_one_stream(pdl):
+    """Inside a host-buffer call the gather, the matmul and the write-back are
+    chained by programmatic dependent launch, and the matmul never streams the
+    staged weights before its dependency wait even when the caller declares
+    its weights static: here every kernel family runs twice back to back on
+    one stream through ONE staging buffer with different inputs (stale staged
+    weights would give the first call's B), with no host synchronisation
+    between the calls, and each result matches the oracle."""
+    stream = torch.cuda.Stream()
+    big = max(w8.w8a8_block_fp8_host_staging_size(M, N, K, w8.W8A8_OUT_BF16)
+              for _, M, N, K, _ in HOST_CHAIN)
+    staging = torch.empty(big, dtype=torch.uint8, device="cuda")
+    pending = []
+    for i, (name, M, N, K, opts) in enumerate(HOST_CHAIN):
+        for rep in range(2):
+            x = synth.make_inputs(M, N, K, seed=40 + 2 * i + rep)
+            pin = [t.pin_memory() for t in (x.A, x.a_s, x.B, x.b_s)]
+            C_host = torch.full((M, N), float("nan"), dtype=torch.bfloat16).pin_memory()
+            o = w8.options(pdl=pdl, weights_static=1, **opts)
+            w8.check(w8.w8a8_block_fp8_matmul_host(*pin, C_host, M, N, K, staging_dev=staging,
+                                                   staging_bytes=big, stream=stream, opts=o))
+            pending.append((name, x, pin, C_host))
+    stream.synchronize()
+    st, word = w8.w8a8_get_device_status()
+    assert st == w8.W8A8_OK, f"device status {word:#x}"
+    for name, x, _, C_host in pending:
+        assert_close(C_host, oracle.reference_c(x.A, x.a_s, x.B, x.b_s), what=name)
+
+
 def test_invalid_calls_do_not_launch():
     x = synth.make_inputs(8, 128, 256, seed=0)
     A, a_s, B, b_s = to_device(x)
