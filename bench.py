@@ -153,20 +153,20 @@ def source_digest(kernel: str = "matmul", read=None) -> str:
 # The decode-size launches write nothing to DRAM during the launch: their C
 # (<= 1.75 MB) is still in L2 when the kernel ends.
 MEASURED_TRAFFIC = {
-    # k_tiled<256,3> stream-K: read 95.54 MB + write 108.15 MB (A + B = 83.9 MB, C = 134.2 MB)
-    ("85906cd6cdebc0e6", "16384x4096x4096", 2): 203687168,
-    # k_swapab<32>: read 1.176 MB (B 1.05 MB + A, scales), write 0
-    ("85906cd6cdebc0e6", "214x4096x256", 2): 1175808,
+    # k_tiled<256,3> stream-K: read 94.61 MB + write 108.08 MB (A + B = 83.9 MB, C = 134.2 MB)
+    ("c6076fccd0cbb570", "16384x4096x4096", 2): 202690304,
+    # k_swapab<32>: read 1.175 MB (B 1.05 MB + A, scales), write 0
+    ("c6076fccd0cbb570", "214x4096x256", 2): 1175040,
     # k_swapab<32> cluster split-K (8 splits): read 2.839 MB (B 2.1 MB + A with outliers), write 0
-    ("85906cd6cdebc0e6", "158x512x4096", 2): 2839040,
-    # k_tiled<192,4>: read 8.724 MB (B 8.4 MB + A), write 0
-    ("85906cd6cdebc0e6", "264x8192x1024", 2): 8724480,
+    ("c6076fccd0cbb570", "158x512x4096", 2): 2839296,
+    # k_tiled<192,4>: read 8.715 MB (B 8.4 MB + A), write 0
+    ("c6076fccd0cbb570", "264x8192x1024", 2): 8714752,
     # k_swapab<32>: read 0.218 MB, write 0
-    ("85906cd6cdebc0e6", "64x512x256", 2): 217600,
-    # k_quant_group128<bf16>, 16384 x 4096: read 134.27 MB + write 36.80 MB
-    ("5809172c0a9b9321", "quant_16384x4096", 1): 171061504,
-    # k_swapab<32, grouped> masked decode, 256 experts of 1536 x 4096: read 1.645 GB + write 23.1 MB
-    ("85906cd6cdebc0e6", "grouped_decode_masked", 2): 1668409600,
+    ("c6076fccd0cbb570", "64x512x256", 2): 217856,
+    # k_quant_group128<bf16>, 16384 x 4096: read 134.28 MB + write 36.37 MB
+    ("687aa1b9ef079874", "quant_16384x4096", 1): 170641664,
+    # k_swapab<32, grouped> masked decode, 256 experts of 1536 x 4096: read 1.645 GB + write 22.9 MB
+    ("c6076fccd0cbb570", "grouped_decode_masked", 2): 1668022784,
 }
 
 
