@@ -361,13 +361,14 @@ class Workload:
         torch.cuda.synchronize()
         return g
 
-    def capture_single(self, i, count):
-        """A graph of `count` launches of shape i, rotating over the sets."""
+    def capture_single(self, i, count, hot=False):
+        """A graph of `count` launches of shape i, rotating over the sets (hot:
+        all on set 0, whose operands then stay resident in L2)."""
         stream = torch.cuda.Stream()
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
             for j in range(count):
-                self.launch(j % self.sets, i, torch.cuda.current_stream())
+                self.launch(0 if hot else j % self.sets, i, torch.cuda.current_stream())
         torch.cuda.synchronize()
         return g
 
@@ -394,6 +395,12 @@ def time_blocks(fn, steps, world, min_seconds):
     return statistics.median(times), len(times)
 
 
+HOT_L2_MAX_BYTES = 16 << 20   # shapes also timed with their operands resident in L2
+PER_SHAPE_TIMING = ("us: one CUDA graph of >= 64 launches of the shape rotating over input sets "
+                    "larger than 2 x L2 (operands cold), divided by the launch count; us_hot_l2 "
+                    "(shapes of at most 16 MB): the same launches all on one input set, operands "
+                    "resident in L2")
+
 VARIANT_NAMES = {1: "tiled", 2: "swapab", 3: "splitk", 4: "splitk_cluster", 5: "smallm",
                  6: "tiled_pair", 7: "generic"}
 
@@ -405,16 +412,28 @@ def per_shape_durations(wl, floor_us):
     shape's time above that floor and the bytes moved per second of it."""
     out = []
     L = max(wl.sets, 64)
-    for i, (M, N, K) in enumerate(wl.shapes):
-        g = wl.capture_single(i, L)
+
+    def graph_time(g):
         for _ in range(2):
             g.replay()
         torch.cuda.synchronize()
         t_blk, _ = time_blocks(lambda k: g.replay(), 5, 1, 0.2)
-        t = t_blk / (5 * L)
+        return t_blk / (5 * L)
+
+    for i, (M, N, K) in enumerate(wl.shapes):
+        g = wl.capture_single(i, L)
+        t = graph_time(g)
         del g
         fl = synth.algorithmic_flops(M, N, K)
         by = synth.algorithmic_bytes(M, N, K, out_bytes=wl.out_bytes)
+        # Hot-L2 time (labelled as such, beside the cold one): the same launch
+        # repeated on one input set, for the small shapes whose operands fit
+        # in L2 many times over.
+        t_hot = None
+        if by <= HOT_L2_MAX_BYTES:
+            g = wl.capture_single(i, L, hot=True)
+            t_hot = graph_time(g)
+            del g
         plan = wl.plans[i]
         name = VARIANT_NAMES.get(plan.variant, "?")
         if plan.variant == 1 and plan.split_k in (2, 3):
@@ -424,6 +443,8 @@ def per_shape_durations(wl, floor_us):
                "variant": name,
                "split_k": plan.split_k, "m_tile": plan.m_tile,
                "block_n_tile": plan.block_n_tile, "stages": plan.stages}
+        if t_hot is not None:
+            row["us_hot_l2"] = round(t_hot * 1e6, 3)
         if floor_us:
             above = t * 1e6 - floor_us
             row["us_above_floor"] = round(above, 3)
@@ -508,6 +529,7 @@ def measure_workload(name, args, world, rank, l2, floor_us, cpu_seconds, shapes=
         "l2": f"rotating {wl.sets} input sets of {nbytes / 1e6:.2f} MB (> 2x L2 {l2 / 1e6:.0f} MB); "
               f"the K timed steps are one CUDA graph",
         "timed_blocks": nblocks,
+        "per_shape_timing": PER_SHAPE_TIMING,
         "per_shape": per_shape,
         "roofline": roofline,
         "clocks": clocks,
@@ -560,6 +582,7 @@ def run_ours(args, rank, world):
         "config": {"workload": headline, "shapes": [list(s) for s in shapes],
                    "parallelism": f"replicas x{world}"},
         "timing": {"l2": res["l2"], "timed_blocks": res["timed_blocks"],
+                   "per_shape": PER_SHAPE_TIMING,
                    "launch": "pdl=1, weights_static=1 (B streamed before the predecessor finishes)"},
         "gpu_launches": res["gpu_launches"],
         "tflops": res["tflops"], "gbs": res["gbs"],
