@@ -130,3 +130,33 @@ def test_nan_codes_propagate_like_the_oracle(name):
     assert np.isnan(ref).any() and not np.isnan(ref).all()
     got = _run(A, a_s, B, b_s, "fp32", opts)
     _check_rows(got, ref, f"{name}: NaN codes")
+
+
+@pytest.mark.parametrize("name", list(VARIANTS))
+def test_fp16_output_overflows_to_inf_like_the_oracle(name):
+    """fp16 output of results beyond its range: random E4M3 codes with unit
+    scales give |C| up to ~1e7, far past fp16's 65504, so the epilogue's cast
+    must give +-inf exactly where the oracle's round-to-nearest cast of the
+    exact result does (a saturating cast would give +-65504), and the
+    finite values stay within the bound.  Elements within 1e-4 of the
+    rounding threshold 65520 are left out of the inf comparison, since the
+    kernels' fp32 accumulation may fall on either side of it."""
+    opts, M = VARIANTS[name]
+    A = synth.random_codes(M, K, seed=400)
+    B = synth.random_codes(N, K, seed=401)
+    G, NB = -(-K // 128), -(-N // 128)
+    a_s = torch.ones((M, G), dtype=torch.float32)
+    b_s = torch.ones((NB, G), dtype=torch.float32)
+    ref = oracle.reference_c(A, a_s, B, b_s)
+    want = oracle.round_to_format(ref, "fp16")
+    assert np.isinf(want).any() and np.isfinite(want).any()
+    got = _run(A, a_s, B, b_s, "fp16", opts)
+    near = np.abs(np.abs(ref) / 65520.0 - 1.0) < 1e-4
+    inf_want, inf_got = np.isinf(want) & ~near, np.isinf(got) & ~near
+    assert np.array_equal(inf_got, inf_want), \
+        f"{name}: inf at {np.argwhere(inf_got != inf_want)[:4].tolist()}"
+    assert np.array_equal(np.sign(got[inf_want]), np.sign(want[inf_want]))
+    fin = np.isfinite(want) & ~near
+    err = np.abs(got[fin] - ref[fin])
+    bound = RTOL * np.abs(ref[fin]) + ATOL_RMS * np.sqrt(np.mean(ref[fin] ** 2))
+    assert (err <= bound).all(), f"{name}: {(err > bound).sum()} finite values outside the bound"
