@@ -172,6 +172,29 @@ def test_host_buffer_call_matches_device_call():
     assert torch.equal(C_host.view(torch.int16), dev.cpu().view(torch.int16))
 
 
+@pytest.mark.parametrize("out", ["bf16", "fp16", "fp32"])
+@pytest.mark.parametrize("M,N,K", [(1, 264, 384), (77, 520, 640), (300, 1032, 256)])
+def test_host_buffer_call_every_output_type_ragged(out, M, N, K):
+    """The host-buffer call on ragged shapes (M and N not multiples of any
+    tile, staging offsets not multiples of the tiles' bytes) in every output
+    type, with the staging area sized for that type, against the oracle."""
+    code = w8.out_code(out)
+    x = synth.make_inputs(M, N, K, seed=M + N)
+    pin = [t.pin_memory() for t in (x.A, x.a_s, x.B, x.b_s)]
+    C_host = torch.empty((M, N), dtype=OUT_TORCH[out]).pin_memory()
+    nbytes = w8.w8a8_block_fp8_host_staging_size(M, N, K, code)
+    assert nbytes > 0
+    staging = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.Stream()
+    w8.check(w8.w8a8_block_fp8_matmul_host(*pin, C_host, M, N, K, out_dtype=code,
+                                           staging_dev=staging, staging_bytes=nbytes,
+                                           stream=stream))
+    stream.synchronize()
+    st, word = w8.w8a8_get_device_status()
+    assert st == w8.W8A8_OK, f"device status {word:#x}"
+    assert_close(C_host, oracle.reference_c(x.A, x.a_s, x.B, x.b_s), what=f"host {out}")
+
+
 @pytest.mark.parametrize("kind", ["pageable", "pinned_misaligned", "pageable_all"])
 def test_host_buffer_call_other_host_memory(kind):
     """Pageable inputs are copied with cudaMemcpyAsync; pinned inputs at odd
