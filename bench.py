@@ -237,7 +237,8 @@ class ClockSampler:
 
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,"
+             "enforced.power.limit")
 
     def __init__(self, index: int):
         self.index = index
@@ -268,7 +269,7 @@ class ClockSampler:
     def summary(self):
         if not self.path or not os.path.exists(self.path):
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
-        sm, smax, reasons = [], None, set()
+        sm, smax, reasons, power, limit = [], None, set(), [], None
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         with open(self.path) as f:
             for line in f:
@@ -280,6 +281,15 @@ class ClockSampler:
                     smax = float(parts[2])
                 except ValueError:
                     continue
+                try:
+                    power.append(float(parts[3]))
+                except ValueError:
+                    pass
+                if len(parts) > 9:
+                    try:
+                        limit = float(parts[9])
+                    except ValueError:
+                        pass
                 for n, v in zip(names, parts[5:9]):
                     if v.lower().startswith("active"):
                         reasons.add(n)
@@ -287,8 +297,14 @@ class ClockSampler:
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
         loaded = [s for s in sm if smax and s > 0.5 * smax] or sm
-        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": smax,
-                "reasons": sorted(reasons), "samples": len(sm)}
+        out = {"sm_mhz": statistics.median(loaded), "sm_max_mhz": smax,
+               "reasons": sorted(reasons), "samples": len(sm)}
+        if power:
+            out["power_w"] = round(statistics.median(power), 1)
+            out["power_max_w"] = round(max(power), 1)
+        if limit:
+            out["power_limit_w"] = limit
+        return out
 
 
 # ---------------------------------------------------------------------- our implementation
