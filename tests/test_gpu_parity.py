@@ -195,11 +195,14 @@ def test_host_buffer_call_every_output_type_ragged(out, M, N, K):
     assert_close(C_host, oracle.reference_c(x.A, x.a_s, x.B, x.b_s), what=f"host {out}")
 
 
+@pytest.mark.parametrize("pdl", [0, 1])
 @pytest.mark.parametrize("kind", ["pageable", "pinned_misaligned", "pageable_all"])
-def test_host_buffer_call_other_host_memory(kind):
+def test_host_buffer_call_other_host_memory(kind, pdl):
     """Pageable inputs are copied with cudaMemcpyAsync; pinned inputs at odd
     addresses take the gather kernel's byte path; a pageable result buffer is
-    written by a kernel (ATS) or copied.  All give the device call's bits."""
+    written by a kernel (ATS) or copied.  All give the device call's bits, also
+    when the caller asks for programmatic dependent launch (the matmul then
+    follows the copies, and the write-back kernel the matmul)."""
     M, N, K = 37, 264, 528
     x = synth.make_inputs(M, N, K, seed=2)
     dev = run(x, "bf16")
@@ -221,7 +224,8 @@ def test_host_buffer_call_other_host_memory(kind):
     staging = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
     stream = torch.cuda.current_stream()
     w8.check(w8.w8a8_block_fp8_matmul_host(*ptrs, C_host, M, N, K, staging_dev=staging,
-                                           staging_bytes=nbytes, stream=stream))
+                                           staging_bytes=nbytes, stream=stream,
+                                           opts=w8.options(pdl=pdl, weights_static=pdl)))
     stream.synchronize()
     assert torch.equal(C_host.view(torch.int16), dev.cpu().view(torch.int16))
 
