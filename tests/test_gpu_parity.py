@@ -314,6 +314,26 @@ def test_invalid_calls_do_not_launch():
     assert w8.w8a8_get_device_status()[0] == w8.W8A8_OK
 
 
+def test_shutdown_releases_and_later_calls_set_up_again():
+    """w8a8_shutdown() frees the library's split-K workspaces and forgets the
+    allocation-free entry point's set-up; the calls after it allocate and set
+    up again and give the oracle's result."""
+    M, N, K = 40, 512, 2048
+    x = synth.make_inputs(M, N, K, seed=120)
+    ref = oracle.reference_c(x.A, x.a_s, x.B, x.b_s)
+    A, a_s, B, b_s = to_device(x)
+    for _ in range(2):
+        C = w8.matmul(A, a_s, B, b_s, out_dtype="fp32", variant=w8.W8A8_VARIANT_SPLITK, split_k=4)
+        C2 = torch.empty((M, N), dtype=torch.float32, device="cuda")
+        w8.check(w8.w8a8_block_fp8_matmul_splitk_noalloc(A, a_s, B, b_s, C2, M, N, K,
+                                                         out_dtype=w8.W8A8_OUT_FP32, split_k=4))
+        torch.cuda.synchronize()
+        assert w8.w8a8_get_device_status()[0] == w8.W8A8_OK
+        assert_close(C, ref, what="split-K, library workspace")
+        assert_close(C2, ref, what="split-K, allocation-free")
+        w8.w8a8_shutdown()
+
+
 def test_splitk_workspace_reused_across_shapes():
     """One caller-owned workspace serves a sequence of different split-K shapes:
     the counter block stays zero between calls."""
