@@ -1073,6 +1073,69 @@ size_t quant_matmul_scratch(int64_t M, int64_t N, int64_t K, int out, const w8a8
     return *mm_bytes + up(static_cast<size_t>(M) * K) + up(static_cast<size_t>(M) * cdiv(K, 128) * 4);
 }
 
+// The pipelined host-buffer path (w8a8_block_fp8_matmul_host): per host
+// thread and device, an auxiliary stream for the chunks' input gathers and the
+// events that order them, made on first use and kept for the thread.
+constexpr int kHostChunks = 4;
+struct HostPipe {
+    cudaStream_t aux = nullptr;
+    cudaEvent_t start = nullptr;
+    cudaEvent_t landed[kHostChunks] = {};
+};
+thread_local HostPipe g_host_pipe[kMaxDevices];
+
+// Rows per chunk of a host-buffer call, or 0 for one piece.  Only calls that
+// move at least 16 MB of A and C are cut, into at most kHostChunks pieces of a
+// multiple of 128 rows (at least 1024), and only where no chunk's plan needs a
+// split-K workspace (a caller's is sized for the whole call).  The stream and
+// events are never made during a stream capture: such a call stays in one
+// piece until the thread has made them outside one.
+int64_t host_chunk_rows(int64_t M, int64_t N, int64_t K, size_t ob, const w8a8_options *o,
+                        cudaStream_t s, int dev, const DeviceInfo &info)
+{
+    if (static_cast<double>(M) * static_cast<double>(K + N * static_cast<int64_t>(ob)) < 16e6)
+        return 0;
+    const int64_t rows = std::max<int64_t>(1024, cdiv(cdiv(M, kHostChunks), 128) * 128);
+    if (rows >= M)
+        return 0;
+    const int64_t last = M - (cdiv(M, rows) - 1) * rows;
+    w8a8_options env_opts;
+    const w8a8_options *eo = o;
+    if (with_env(o, true, &env_opts, &eo) != W8A8_OK)
+        return 0;
+    for (const int64_t m : {rows, last}) {
+        Plan pl;
+        if (make_plan(m, N, K, static_cast<int>(ob), eo, info, &pl) != W8A8_OK ||
+            splitk_workspace_bytes(m, N, pl) != 0)
+            return 0;
+    }
+    HostPipe &hp = g_host_pipe[dev];
+    if (!hp.aux) {
+        cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+        if (cudaStreamIsCapturing(s, &cap) != cudaSuccess || cap != cudaStreamCaptureStatusNone) {
+            cudaGetLastError();
+            return 0;
+        }
+        bool ok = cudaStreamCreateWithFlags(&hp.aux, cudaStreamNonBlocking) == cudaSuccess;
+        ok = ok && cudaEventCreateWithFlags(&hp.start, cudaEventDisableTiming) == cudaSuccess;
+        for (cudaEvent_t &e : hp.landed)
+            ok = ok && cudaEventCreateWithFlags(&e, cudaEventDisableTiming) == cudaSuccess;
+        if (!ok) {            // undo what was made; the call runs in one piece
+            cudaGetLastError();
+            for (cudaEvent_t &e : hp.landed)
+                if (e)
+                    cudaEventDestroy(e);
+            if (hp.start)
+                cudaEventDestroy(hp.start);
+            if (hp.aux)
+                cudaStreamDestroy(hp.aux);
+            hp = HostPipe{};
+            return 0;
+        }
+    }
+    return rows;
+}
+
 }  // namespace
 
 namespace w8a8 {
@@ -1300,6 +1363,105 @@ w8a8_status w8a8_block_fp8_matmul_host(const void *A_host, const float *a_s_host
         segs.dst[i] = static_cast<uint8_t *>(copies[i].dst);
         segs.bytes[i] = copies[i].n;
     }
+    // Inside the call the launches are chained by programmatic dependent
+    // launch: each waits for its predecessor before its first access, so the
+    // chain is ordered as with plain launches, and each one's launch and
+    // prologue overlap the previous kernel.  The staged B is written by this
+    // call's gather, so the matmul never streams weights before its dependency
+    // wait, whatever the caller's weights_static says.  After cudaMemcpyAsync
+    // copies the matmul launches as the caller asked.
+    w8a8_options chained = opts ? *opts : w8a8_options{};
+    chained.weights_static = 0;
+    if (mapped)
+        chained.pdl = 1;
+    // The result goes back by one kernel writing the host buffer wherever the
+    // device can address it (page-locked mapped memory, or any host memory
+    // through the host's page tables): measured on the CPU-GPU link of a
+    // GB300 node, five such calls on five streams finish a step sooner than
+    // five copy-engine copies (70 vs 77 us for the decode sweep), and a copy
+    // to pageable memory would be synchronous.  Otherwise cudaMemcpyAsync.
+    const size_t row_c = static_cast<size_t>(N) * ob;
+    cudaPointerAttributes cattr = {};
+    uint8_t *c_dev = nullptr;
+    if (cudaPointerGetAttributes(&cattr, C_host) != cudaSuccess)
+        cudaGetLastError();
+    else if (cattr.type == cudaMemoryTypeHost && cattr.devicePointer)
+        c_dev = static_cast<uint8_t *>(cattr.devicePointer);
+    else if (cattr.type == cudaMemoryTypeUnregistered && info.host_tables)
+        c_dev = static_cast<uint8_t *>(C_host);
+    auto write_back = [&](int64_t r0, int64_t rows) -> w8a8_status {
+        const size_t off = static_cast<size_t>(r0) * row_c, bytes = static_cast<size_t>(rows) * row_c;
+        cudaError_t e;
+        if (c_dev) {
+            GatherSegs out_seg = {};
+            out_seg.src[0] = reinterpret_cast<const uint8_t *>(dC) + off;
+            out_seg.dst[0] = c_dev + off;
+            out_seg.bytes[0] = bytes;
+            out_seg.count = 1;
+            e = launch_gather(out_seg, 2 * info.sm_count, s, 1);
+        } else {
+            e = cudaMemcpyAsync(static_cast<char *>(C_host) + off, dC + off, bytes,
+                                cudaMemcpyDeviceToHost, s);
+        }
+        return e == cudaSuccess ? W8A8_OK : cuda_fail(e, "copy of the result to host memory");
+    };
+
+    // Large problems are cut into row chunks whose inputs come in on the
+    // thread's auxiliary stream while the previous chunk's result goes back on
+    // the call's stream: the CPU-GPU link carries both directions at once
+    // (measured on a GB300 node: ~210 GB/s in and ~190 GB/s out alone, ~330
+    // GB/s together), which one gather-multiply-write-back sequence leaves
+    // unused.  The chunks move by copy engine: a copy kernel could not run
+    // beside the multiplies, whose CTAs hold every register of their SMs.
+    const bool c_pinned = cattr.type == cudaMemoryTypeHost && c_dev;
+    w8a8_options plain_piece = chained;
+    plain_piece.pdl = 0;
+    const int64_t chunk =
+        mapped && c_pinned ? host_chunk_rows(M, N, K, ob, &plain_piece, s, dev, info) : 0;
+    if (chunk > 0) {
+        // Every piece follows copies and event waits on its stream, so it is
+        // launched as an ordinary dependent of all of them.
+        const w8a8_options &piece = plain_piece;
+        HostPipe &hp = g_host_pipe[dev];
+        cudaError_t e = cudaEventRecord(hp.start, s);      // the caller's earlier work first
+        if (e == cudaSuccess)
+            e = cudaStreamWaitEvent(hp.aux, hp.start, 0);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "ordering the chunked host-buffer call");
+        const int n = static_cast<int>(cdiv(M, chunk));
+        for (int c = 0; c < n && e == cudaSuccess; ++c) {
+            const int64_t r0 = c * chunk, rows = std::min<int64_t>(chunk, M - r0);
+            auto in = [&](int i, size_t off, size_t bytes) {
+                if (e == cudaSuccess)
+                    e = cudaMemcpyAsync(static_cast<char *>(copies[i].dst) + off,
+                                        static_cast<const char *>(copies[i].src) + off, bytes,
+                                        cudaMemcpyHostToDevice, hp.aux);
+            };
+            if (c == 0) {                                                           // weights once
+                in(2, 0, copies[2].n);
+                in(3, 0, copies[3].n);
+            }
+            in(0, static_cast<size_t>(r0) * K, static_cast<size_t>(rows) * K);          // A rows
+            in(1, static_cast<size_t>(r0) * G * 4, static_cast<size_t>(rows) * G * 4);  // a_s rows
+            if (e == cudaSuccess)
+                e = cudaEventRecord(hp.landed[c], hp.aux);
+            if (e == cudaSuccess)
+                e = cudaStreamWaitEvent(s, hp.landed[c], 0);
+            if (e != cudaSuccess)
+                break;
+            st = run(dA + static_cast<size_t>(r0) * K,
+                     reinterpret_cast<const float *>(das) + static_cast<size_t>(r0) * G, dB,
+                     reinterpret_cast<const float *>(dbs), dC + static_cast<size_t>(r0) * row_c,
+                     rows, N, K, block_n, block_k, out_dtype, s, &piece);
+            if (st != W8A8_OK)
+                return st;
+            const size_t off = static_cast<size_t>(r0) * row_c;
+            e = cudaMemcpyAsync(static_cast<char *>(C_host) + off, dC + off,
+                                static_cast<size_t>(rows) * row_c, cudaMemcpyDeviceToHost, s);
+        }
+        return e == cudaSuccess ? W8A8_OK : cuda_fail(e, "copies of the chunked host-buffer call");
+    }
+
     // The gather follows the caller's work under programmatic dependent launch
     // only when the caller asks for it (opts->pdl).
     if (mapped) {
@@ -1314,50 +1476,11 @@ w8a8_status w8a8_block_fp8_matmul_host(const void *A_host, const float *a_s_host
                 return cuda_fail(e, "cudaMemcpyAsync(host to device)");
         }
     }
-    // Inside the call the three launches are chained by programmatic dependent
-    // launch: each waits for its predecessor before its first access, so the
-    // chain is ordered as with plain launches, and each one's launch and
-    // prologue overlap the previous kernel.  The staged B is written by this
-    // call's gather, so the matmul never streams weights before its dependency
-    // wait, whatever the caller's weights_static says.  After cudaMemcpyAsync
-    // copies the matmul launches as the caller asked.
-    w8a8_options chained = opts ? *opts : w8a8_options{};
-    chained.weights_static = 0;
-    if (mapped)
-        chained.pdl = 1;
     st = run(dA, reinterpret_cast<const float *>(das), dB, reinterpret_cast<const float *>(dbs),
              dC, M, N, K, block_n, block_k, out_dtype, s, &chained);
     if (st != W8A8_OK)
         return st;
-    // The result goes back by one kernel writing the host buffer wherever the
-    // device can address it (page-locked mapped memory, or any host memory
-    // through the host's page tables): measured on the CPU-GPU link of a
-    // GB300 node, five such calls on five streams finish a step sooner than
-    // five copy-engine copies (70 vs 77 us for the decode sweep), and a copy
-    // to pageable memory would be synchronous.  Otherwise cudaMemcpyAsync.
-    const size_t cbytes = static_cast<size_t>(M * N * ob);
-    cudaPointerAttributes cattr = {};
-    void *c_dev = nullptr;
-    if (cudaPointerGetAttributes(&cattr, C_host) != cudaSuccess)
-        cudaGetLastError();
-    else if (cattr.type == cudaMemoryTypeHost && cattr.devicePointer)
-        c_dev = cattr.devicePointer;
-    else if (cattr.type == cudaMemoryTypeUnregistered && info.host_tables)
-        c_dev = C_host;
-    cudaError_t e;
-    if (c_dev) {
-        GatherSegs out_seg = {};
-        out_seg.src[0] = reinterpret_cast<const uint8_t *>(dC);
-        out_seg.dst[0] = static_cast<uint8_t *>(c_dev);
-        out_seg.bytes[0] = cbytes;
-        out_seg.count = 1;
-        e = launch_gather(out_seg, 2 * info.sm_count, s, 1);
-    } else {
-        e = cudaMemcpyAsync(C_host, dC, cbytes, cudaMemcpyDeviceToHost, s);
-    }
-    if (e != cudaSuccess)
-        return cuda_fail(e, "copy of the result to host memory");
-    return W8A8_OK;
+    return write_back(0, M);
 }
 
 size_t w8a8_block_fp8_workspace_size(int64_t M, int64_t N, int64_t K, const w8a8_options *opts)
@@ -1505,6 +1628,17 @@ void w8a8_shutdown(void)
     std::lock_guard<std::mutex> lock(g_mutex);
     int cur = -1;
     cudaGetDevice(&cur);
+    for (int d = 0; d < kMaxDevices; ++d) {          // the calling thread's host-path streams
+        HostPipe &hp = g_host_pipe[d];
+        if (!hp.aux)
+            continue;
+        cudaSetDevice(d);
+        for (cudaEvent_t e : hp.landed)
+            cudaEventDestroy(e);
+        cudaEventDestroy(hp.start);
+        cudaStreamDestroy(hp.aux);
+        hp = HostPipe{};
+    }
     for (auto &kv : g_workspaces) {
         cudaSetDevice(kv.first.first);
         cudaFree(kv.second.ptr);

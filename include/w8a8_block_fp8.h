@@ -270,6 +270,15 @@ w8a8_status w8a8_block_fp8_matmul_strided(const void *A_dev, int64_t lda, const 
  * caller's previous kernel on `stream`; opts->weights_static is ignored (the
  * staged weights are written by the call itself).
  *
+ * Large calls (at least 16 MB of A and C) are cut into up to four row chunks:
+ * the chunks' inputs come in on an auxiliary stream of the calling thread,
+ * ordered after the work already on `stream`, while each earlier chunk is
+ * multiplied and written back on `stream`, so both directions of the CPU-GPU
+ * link are busy at once.  The call is still complete, in order, when `stream`
+ * has passed it.  Chunks are used only where no chunk's plan needs a split-K
+ * workspace, and the thread's auxiliary stream is made outside a stream
+ * capture (a first large call inside a capture runs in one piece).
+ *
  * With page-locked buffers the call can be captured in a CUDA graph (every
  * replay then moves the buffers' current contents).  staging_dev is
  * caller-owned device memory of at least
@@ -512,9 +521,10 @@ int w8a8_debug_bounds_build(void);
 w8a8_status w8a8_env_config(int *force_variant, int *deterministic,
                             unsigned long long *wait_limit_cycles);
 
-/* Releases the library's cached split-K workspaces (every device) and forgets
- * the allocation-free entry point's per-device set-up, so that its next call
- * on a device looks the scratch address up again (needed after a
+/* Releases the library's cached split-K workspaces (every device) and the
+ * calling thread's host-buffer streams and events, and forgets the
+ * allocation-free entry point's per-device set-up, so that its next call on a
+ * device looks the scratch address up again (needed after a
  * cudaDeviceReset). */
 void w8a8_shutdown(void);
 

@@ -195,6 +195,55 @@ def test_host_buffer_call_every_output_type_ragged(out, M, N, K):
     assert_close(C_host, oracle.reference_c(x.A, x.a_s, x.B, x.b_s), what=f"host {out}")
 
 
+@pytest.mark.parametrize("out", ["bf16", "fp32"])
+@pytest.mark.parametrize("M", [4096, 3000])
+def test_host_buffer_call_in_row_chunks(M, out):
+    """A large host-buffer call (at least 16 MB of A and C) runs in row chunks:
+    inputs on the thread's auxiliary stream, multiply and write-back on the
+    call's stream.  Two such calls back to back on one stream, through one
+    staging area and different inputs, with no host synchronisation, each
+    against the oracle on rows that cover every 128-row tile (3000: a ragged
+    last chunk); then the same call captured in a CUDA graph and replayed over
+    new input contents."""
+    N, K = 2048, 1024
+    code = w8.out_code(out)
+    xs = [synth.make_inputs(M, N, K, seed=130 + i) for i in range(3)]
+    pins = [[t.pin_memory() for t in (x.A, x.a_s, x.B, x.b_s)] for x in xs]
+    outs = [torch.empty((M, N), dtype=OUT_TORCH[out]).pin_memory() for _ in xs]
+    nbytes = w8.w8a8_block_fp8_host_staging_size(M, N, K, code)
+    staging = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.Stream()
+    rows = sample_rows(M)
+
+    def call(i, s_):
+        w8.check(w8.w8a8_block_fp8_matmul_host(*pins[i], outs[i], M, N, K, out_dtype=code,
+                                               staging_dev=staging, staging_bytes=nbytes,
+                                               stream=s_, opts=w8.options(pdl=1)))
+
+    def check(i, what):
+        st, word = w8.w8a8_get_device_status()
+        assert st == w8.W8A8_OK, f"device status {word:#x}"
+        ref = reference_rows(xs[i], rows)
+        assert_close(outs[i][torch.from_numpy(rows)], ref, rms=rms_estimate(ref), what=what)
+
+    call(0, stream)
+    call(1, stream)
+    stream.synchronize()
+    check(0, "first call")
+    check(1, "second call")
+    # captured once, replayed over the inputs' new contents
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        call(2, torch.cuda.current_stream())
+    for dst, src in zip(pins[2], pins[0]):
+        dst.copy_(src)
+    xs[2] = xs[0]
+    outs[2].fill_(float("nan"))
+    g.replay()
+    torch.cuda.synchronize()
+    check(2, "graph replay")
+
+
 @pytest.mark.parametrize("pdl", [0, 1])
 @pytest.mark.parametrize("kind", ["pageable", "pinned_misaligned", "pageable_all"])
 def test_host_buffer_call_other_host_memory(kind, pdl):
