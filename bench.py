@@ -153,20 +153,20 @@ def source_digest(kernel: str = "matmul", read=None) -> str:
 # The decode-size launches write nothing to DRAM during the launch: their C
 # (<= 1.75 MB) is still in L2 when the kernel ends.
 MEASURED_TRAFFIC = {
-    # k_tiled<256,3> stream-K: read 94.61 MB + write 108.08 MB (A + B = 83.9 MB, C = 134.2 MB)
-    ("c6076fccd0cbb570", "16384x4096x4096", 2): 202690304,
+    # k_tiled<256,3> stream-K: read 95.78 MB + write 107.43 MB (A + B = 83.9 MB, C = 134.2 MB)
+    ("76a5aa2d82ebd232", "16384x4096x4096", 2): 203213056,
     # k_swapab<32>: read 1.175 MB (B 1.05 MB + A, scales), write 0
-    ("c6076fccd0cbb570", "214x4096x256", 2): 1175040,
-    # k_swapab<32> cluster split-K (8 splits): read 2.839 MB (B 2.1 MB + A with outliers), write 0
-    ("c6076fccd0cbb570", "158x512x4096", 2): 2839296,
-    # k_tiled<192,4>: read 8.715 MB (B 8.4 MB + A), write 0
-    ("c6076fccd0cbb570", "264x8192x1024", 2): 8714752,
-    # k_swapab<32>: read 0.218 MB, write 0
-    ("c6076fccd0cbb570", "64x512x256", 2): 217856,
-    # k_quant_group128<bf16>, 16384 x 4096: read 134.28 MB + write 36.37 MB
-    ("687aa1b9ef079874", "quant_16384x4096", 1): 170641664,
-    # k_swapab<32, grouped> masked decode, 256 experts of 1536 x 4096: read 1.645 GB + write 22.9 MB
-    ("c6076fccd0cbb570", "grouped_decode_masked", 2): 1668022784,
+    ("76a5aa2d82ebd232", "214x4096x256", 2): 1175296,
+    # k_swapab<32> cluster split-K (8 splits): read 2.840 MB (B 2.1 MB + A with outliers), write 0
+    ("76a5aa2d82ebd232", "158x512x4096", 2): 2839552,
+    # k_tiled<192,4>: read 8.714 MB (B 8.4 MB + A), write 0
+    ("76a5aa2d82ebd232", "264x8192x1024", 2): 8714496,
+    # k_swapab<32>: read 0.217 MB, write 0
+    ("76a5aa2d82ebd232", "64x512x256", 2): 217344,
+    # k_quant_group128<bf16>, 16384 x 4096: read 134.27 MB + write 36.57 MB
+    ("687aa1b9ef079874", "quant_16384x4096", 1): 170833664,
+    # k_swapab<32, grouped> masked decode, 256 experts of 1536 x 4096: read 1.645 GB + write 23.0 MB
+    ("76a5aa2d82ebd232", "grouped_decode_masked", 2): 1668159744,
 }
 
 
