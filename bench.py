@@ -934,7 +934,8 @@ def run_e2e(wl, args, world):
             "path": "w8a8_block_fp8_matmul_host (C ABI, pinned host buffers) called once per "
                     "shape per step from Python, one stream per shape; each call checks its "
                     "arguments, plans, encodes its tensor maps, gathers its inputs from host "
-                    "memory, runs the matmul and writes the result back into host memory; the "
+                    "memory, runs the matmul and writes the result back into host memory (large "
+                    "calls in row chunks, inputs and results crossing the link at once); the "
                     "host waits for the step's results",
             "graph_replay": {"value": round(rate(t_graph), 3),
                              "ms_per_step": round(t_graph * 1e3, 4),
