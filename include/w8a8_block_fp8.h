@@ -270,12 +270,13 @@ w8a8_status w8a8_block_fp8_matmul_strided(const void *A_dev, int64_t lda, const 
  * caller's previous kernel on `stream`; opts->weights_static is ignored (the
  * staged weights are written by the call itself).
  *
- * Large calls (at least 16 MB of A and C) are cut into up to four row chunks:
- * the chunks' inputs come in on an auxiliary stream of the calling thread,
- * ordered after the work already on `stream`, while each earlier chunk is
- * multiplied and written back on `stream`, so both directions of the CPU-GPU
- * link are busy at once.  The call is still complete, in order, when `stream`
- * has passed it.  Chunks are used only where no chunk's plan needs a split-K
+ * Large calls (at least 16 MB of A and C, with page-locked inputs and C_host)
+ * are cut into up to four row chunks moved by copy engine: the chunks' inputs
+ * come in on an auxiliary stream of the calling thread, ordered after the
+ * work already on `stream`, while each earlier chunk is multiplied and its
+ * rows of C copied back on `stream`, so both directions of the CPU-GPU link
+ * are busy at once.  The call is still complete, in order, when `stream` has
+ * passed it.  Chunks are used only where no chunk's plan needs a split-K
  * workspace, and the thread's auxiliary stream is made outside a stream
  * capture (a first large call inside a capture runs in one piece).
  *
